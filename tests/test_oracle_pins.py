@@ -1,0 +1,388 @@
+"""Pins that tie the CPU oracle to the pages and to mathematics, not to itself.
+
+Each test checks an oracle function against something independent of its own
+code: values printed on the pages (tests/golden), a library routine (torch's
+float8 cast, scipy's Hadamard matrix, numpy's fp64 matmul and float32
+arithmetic), closed forms, invariants, or brute force on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def minifloat_values(ebits, mbits, nan_all_ones=False):
+    """Generic sign/exponent/mantissa decoder with IEEE-style bias, subnormals and
+    no infinities; written independently of the oracle's per-format decoders."""
+    bias = 2 ** (ebits - 1) - 1
+    vals = {}
+    for code in range(2 ** (1 + ebits + mbits)):
+        s = code >> (ebits + mbits)
+        e = (code >> mbits) & ((1 << ebits) - 1)
+        m = code & ((1 << mbits) - 1)
+        if nan_all_ones and e == (1 << ebits) - 1 and m == (1 << mbits) - 1:
+            vals[code] = float("nan")
+            continue
+        if e == 0:
+            mag = m * 2.0 ** (1 - bias - mbits)
+        else:
+            mag = (1 + m / 2.0 ** mbits) * 2.0 ** (e - bias)
+        vals[code] = -mag if s else mag
+    return vals
+
+
+# ------------------------------------------------------------------ formats ---
+def test_e4m3_grid_matches_generic_minifloat_and_page_range():
+    g = gold("e4m3_range.json")
+    ref = minifloat_values(4, 3, nan_all_ones=True)
+    for code in range(256):
+        v = orc.decode("e4m3", code)
+        if math.isnan(ref[code]):
+            assert math.isnan(v), code
+        else:
+            assert v == ref[code], code
+    finite = [abs(orc.decode("e4m3", c)) for c in range(256) if not math.isnan(orc.decode("e4m3", c))]
+    assert max(finite) == g["max"]
+    mn = min(v for v in finite if v > 0)
+    assert round(mn, 5) == g["min_printed"] and mn == 2.0 ** -9
+    ratio = max(finite) / mn
+    assert ratio == 229376 and abs(ratio - g["range_printed"]) / g["range_printed"] < 0.2
+    assert orc.decode("e4m3", 0x7E) == 448.0 and math.isnan(orc.decode("e4m3", 0x7F))
+    assert math.isnan(orc.decode("e4m3", 0xFF))
+
+
+def test_e2m1_grid_from_page_bit_layout():
+    lay = gold("fp4_layouts.json")["E2M1"]
+    ref = minifloat_values(lay["exponent"], lay["mantissa"])
+    got = {c: orc.decode("e2m1", c) for c in range(16)}
+    assert got == ref
+    assert sorted({abs(v) for v in got.values()}) == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+
+
+def test_e8m0_is_power_of_two():
+    for b in range(255):
+        assert orc.decode("e8m0", b) == math.ldexp(1.0, b - 127)
+    assert math.isnan(orc.decode("e8m0", 255))
+
+
+def test_power_of_two_dequant_is_exact_shift():
+    g = gold("pow2_shift.json")
+    # the page's example: value 50, k = 3
+    assert g["value"] * 2 ** g["k"] == g["result"]
+    assert math.ldexp(g["value"], g["k"]) == g["result"]
+    for elem in ("e4m3", "e2m1"):
+        for code in range(256 if elem == "e4m3" else 16):
+            v = orc.decode(elem, code)
+            if math.isnan(v):
+                continue
+            for k in range(-20, 21):
+                s = orc.decode("e8m0", 127 + k)
+                assert np.float32(v) * np.float32(s) == math.ldexp(v, k)
+
+
+# ------------------------------------------------------------- RNE casting ---
+def test_e4m3_rne_matches_torch_float8_on_every_bf16():
+    x = workloads.all_bf16_patterns().float()
+    ref = x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.encode_rne("e4m3", float(v)) for v in x.numpy()], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("elem,nmax", [("e4m3", 0x7E), ("e2m1", 7)])
+def test_rne_midpoints_ties_even_and_saturation(elem, nmax):
+    grid = [orc.decode(elem, c) for c in range(nmax + 1)]
+    for c in range(nmax):
+        lo, hi = grid[c], grid[c + 1]
+        mid = (lo + hi) / 2
+        below = np.nextafter(np.float32(mid), np.float32(-1))
+        above = np.nextafter(np.float32(mid), np.float32(1e9))
+        assert orc.encode_rne(elem, below) == c
+        assert orc.encode_rne(elem, above) == c + 1
+        assert orc.encode_rne(elem, mid) == (c if c % 2 == 0 else c + 1)
+        neg = orc.encode_rne(elem, -float(above))
+        assert neg == (c + 1) | (0x80 if elem == "e4m3" else 0x8)
+    top = grid[nmax]
+    for v in (top, top * 1.01, top * 2, 3.0e38):
+        assert orc.encode_rne(elem, v) == nmax
+    sign = 0x80 if elem == "e4m3" else 0x8
+    assert orc.encode_rne(elem, -0.0) == sign
+    assert orc.encode_rne(elem, -1e-30) == sign
+    assert orc.encode_rne(elem, 0.0) == 0
+
+
+def test_e2m1_rne_brute_force_random_values():
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([rng.uniform(-7, 7, 4000), rng.normal(0, 1, 4000)]).astype(np.float32)
+    grid = np.array([orc.decode("e2m1", c) for c in range(8)])
+    for v in vals:
+        a = min(abs(float(v)), 6.0)
+        d = np.abs(grid - a)
+        best = np.flatnonzero(d == d.min())
+        c = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+        assert orc.encode_rne("e2m1", v) == (c | (0x8 if np.signbit(v) else 0))
+
+
+# ------------------------------------------------------------ scale rules ---
+def _bs():
+    rng = np.random.default_rng(5)
+    b = np.concatenate([np.exp2(rng.uniform(-140, 127, 3000)), [448, 6, 449, 447.9, 2 ** -133,
+                                                               3.38e38, 1.0, 5.99, 6.01]])
+    return b.astype(np.float32)
+
+
+@pytest.mark.parametrize("elem,Q,emax", [("e4m3", 448.0, 8), ("e2m1", 6.0, 2)])
+def test_scale_rules_properties(elem, Q, emax):
+    for b in _bs():
+        b = float(b)
+        e = orc.pow2_exponent(b, "floor", elem)
+        if -127 <= math.floor(math.log2(b)) - emax <= 127:
+            s = math.ldexp(b, -e)
+            assert 2.0 ** emax <= s < 2.0 ** (emax + 1), (b, e)
+        e = orc.pow2_exponent(b, "ceil", elem)
+        if -127 < e < 127:
+            assert math.ldexp(b, -e) <= Q < math.ldexp(b, -(e - 1)), (b, e)
+        e = orc.pow2_exponent(b, "nearest", elem)
+        if -127 < e < 127:
+            assert abs(math.log2(b / Q) - e) <= 0.5 + 1e-12, (b, e)
+    for rule in ("floor", "ceil", "nearest"):
+        assert orc.pow2_exponent(0.0, rule, elem) == 0
+        assert orc.pow2_exponent(2.0 ** -140, rule, elem) == -127
+
+
+# -------------------------------------------------------------- Philox/SR ---
+def test_philox_statistics_and_counter_sensitivity():
+    key = np.array([42, 0], dtype=np.uint32)
+    outs = np.array([orc.philox4x32_10([i, 0, 0, 0], key) for i in range(4096)], dtype=np.uint32)
+    # bit balance of 4096*4 words: each of 32 bits is set ~half the time
+    bits = ((outs.reshape(-1, 1) >> np.arange(32, dtype=np.uint32)) & 1).mean(axis=0)
+    assert np.all(np.abs(bits - 0.5) < 0.02)
+    # 16-bit halves are uniform (chi-square over 64 bins)
+    u16 = np.concatenate([outs.reshape(-1) & 0xFFFF, outs.reshape(-1) >> 16])
+    h = np.bincount(u16 >> 10, minlength=64)
+    exp = len(u16) / 64
+    chi2 = ((h - exp) ** 2 / exp).sum()
+    assert chi2 < 130  # 63 dof: p ~ 1e-6
+    # every counter word and key word changes the output (avalanche)
+    base = orc.philox4x32_10([7, 8, 9, 10], [1, 2])
+    for i in range(4):
+        c = [7, 8, 9, 10]
+        c[i] ^= 1
+        flips = np.unpackbits((orc.philox4x32_10(c, [1, 2]) ^ base).view(np.uint8)).sum()
+        assert 30 < flips < 98
+    for i in range(2):
+        k = [1, 2]
+        k[i] ^= 1
+        flips = np.unpackbits((orc.philox4x32_10([7, 8, 9, 10], k) ^ base).view(np.uint8)).sum()
+        assert 30 < flips < 98
+
+
+def test_sr_unbiased_and_probability():
+    grid = [orc.decode("e2m1", c) for c in range(8)]
+    rng = np.random.default_rng(11)
+    for v in [0.2, 0.74, 1.1, 1.9, 2.25, 3.5, 4.001, 5.9, -2.6, -0.01]:
+        n = 4000
+        us = rng.integers(0, 65536, n)
+        codes = np.array([orc.encode_e2m1_sr(v, int(u)) for u in us])
+        dec = np.array([orc.decode("e2m1", int(c)) for c in codes])
+        a = abs(v)
+        lo = max(g for g in grid if g <= a)
+        hi = min(g for g in grid if g > a)
+        p = (a - lo) / (hi - lo)
+        assert set(np.abs(dec)) <= {lo, hi}
+        frac_up = np.mean(np.abs(dec) == hi)
+        assert abs(frac_up - p) < 4 * math.sqrt(p * (1 - p) / n) + 1e-3
+        sd = (hi - lo) * math.sqrt(p * (1 - p) / n)
+        assert abs(dec.mean() - v) < 4 * sd + 1e-4
+    # deterministic edges: u16 = 0 always rounds an off-grid value up,
+    # grid points and saturated values never move
+    assert orc.decode("e2m1", orc.encode_e2m1_sr(0.25, 0)) == 0.5
+    assert orc.decode("e2m1", orc.encode_e2m1_sr(0.25, 32768)) == 0.0
+    assert orc.decode("e2m1", orc.encode_e2m1_sr(0.25, 32767)) == 0.5
+    for g in grid:
+        for u in (0, 65535):
+            assert orc.decode("e2m1", orc.encode_e2m1_sr(g, u)) == g
+    assert orc.decode("e2m1", orc.encode_e2m1_sr(9.0, 0)) == 6.0
+
+
+def test_sr_bits_use_one_philox_block_per_8_elements():
+    seed, sid = 42, 3
+    vals = [orc.sr_u16(seed, sid, L) for L in range(64)]
+    assert len(set(vals)) > 56
+    # the 8 elements of a group are distinct halves of one 128-bit block
+    for g in range(8):
+        blk = orc.philox4x32_10([g, 0, sid, 0], [seed, 0])
+        halves = []
+        for w in blk:
+            halves += [int(w) & 0xFFFF, int(w) >> 16]
+        assert vals[8 * g:8 * g + 8] == halves
+
+
+# -------------------------------------------------------------- Hadamard ---
+def test_fwht_equals_scipy_hadamard_exactly():
+    from scipy.linalg import hadamard
+    H = hadamard(32).astype(np.float64)
+    assert np.array_equal(H @ H.T, 32 * np.eye(32))
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        x = rng.integers(-1000, 1000, 32).astype(np.float32)
+        assert np.array_equal(orc.fwht32(x).astype(np.float64), H @ x.astype(np.float64))
+    x = rng.integers(-50, 50, 32).astype(np.float32)
+    assert np.array_equal(orc.fwht32(orc.fwht32(x)), 32 * x)
+
+
+# ------------------------------------------------------------ SF layout ---
+def test_sf_layout_is_a_bijection_onto_512_byte_tiles():
+    for rows, kb in ((128, 4), (256, 8), (130, 3), (384, 12)):
+        n = orc.sf_bytes(rows, kb)
+        assert n == math.ceil(rows / 128) * math.ceil(kb / 4) * 512
+        seen = set()
+        for r in range(rows):
+            for b in range(kb):
+                i = orc.sf_index(r, b, kb)
+                assert 0 <= i < n and i not in seen
+                seen.add(i)
+                # same 16-byte row for rows r, r+32, r+64, r+96 of a tile
+                assert (i % 512) // 16 == r % 32
+    # a tile is contiguous: all scales of rows 0..127, blocks 0..3 fill bytes 0..511
+    assert sorted(orc.sf_index(r, b, 8) for r in range(128) for b in range(4)) == list(range(512))
+
+
+# ------------------------------------------------------------- quantizer ---
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_colwise_is_rowwise_of_transpose():
+    x = workloads.draw("student_t3", (96, 64), 1)
+    for fmt in ("mxfp8", "mxfp4", "nvfp4", "moss"):
+        a = orc.quantize(_bits(x), fmt, "col")
+        b = orc.quantize(_bits(x.t().contiguous()), fmt, "row")
+        assert np.array_equal(a.codes, b.codes) and np.array_equal(a.sf_logical, b.sf_logical)
+        assert a.amax == b.amax and a.tensor_scale == b.tensor_scale
+
+
+def test_mx_quantize_is_nearest_at_the_chosen_scale():
+    """Brute force on tiny blocks: every code is the nearest grid point to
+    x * 2^-e (ties even, saturating) and the scale byte is the FLOOR rule."""
+    x = workloads.draw("outliers", (4, 64), 7)
+    xf = x.float().numpy().astype(np.float64)
+    for fmt, elem, nmax in (("mxfp8", "e4m3", 0x7E), ("mxfp4", "e2m1", 7)):
+        q = orc.quantize(_bits(x), fmt, "row")
+        grid = np.array([orc.decode(elem, c) for c in range(nmax + 1)])
+        for r in range(4):
+            for kb in range(2):
+                blk = xf[r, 32 * kb:32 * kb + 32]
+                e = int(q.sf_logical[r, kb]) - 127
+                assert e == math.floor(math.log2(np.abs(blk).max())) - (8 if elem == "e4m3" else 2)
+                for i, v in enumerate(blk):
+                    k = 32 * kb + i
+                    c = q.codes[r, k] if elem == "e4m3" else (q.codes[r, k // 2] >> (4 * (k % 2))) & 0xF
+                    a = min(abs(math.ldexp(v, -e)), grid[-1])
+                    d = np.abs(grid - a)
+                    best = np.flatnonzero(d == d.min())
+                    want = int(best[0]) if len(best) == 1 else int(best[best % 2 == 0][0])
+                    sign = (0x80 if elem == "e4m3" else 0x8) if np.signbit(v) else 0
+                    assert c == want | sign
+
+
+def test_moss_two_level_scales():
+    g = gold("moss_two_level.json")
+    x = workloads.draw("lognormal_cols", (64, 128), 9)
+    xf = x.float().numpy()
+    q = orc.quantize(_bits(x), "moss", "row")
+    amax = np.float32(np.abs(xf).max())
+    assert q.amax == amax
+    assert np.float32(q.tensor_scale) == np.float32(amax) / np.float32(g["fp8_max"])
+    e = q.sf_logical.astype(int) - 127
+    assert e.max() <= 1  # micro scales: fine adjustment below the tensor scale
+    dq = q.dequantize() * q.tensor_scale
+    # E4M3 keeps 4 significant bits: relative error <= 2^-4 above the subnormal range
+    big = np.abs(xf) > 2.0 ** -6 * q.tensor_scale * 2.0 ** e.repeat(32, axis=1)
+    rel = np.abs(dq - xf)[big] / np.abs(xf)[big]
+    assert rel.max() <= 2.0 ** -4 + 1e-9
+
+
+def test_nvfp4_scales():
+    x = workloads.draw("student_t3", (32, 64), 4)
+    xf = x.float().numpy()
+    q = orc.quantize(_bits(x), "nvfp4", "row")
+    amax = np.float32(np.abs(xf).max())
+    assert np.float32(q.tensor_scale) == np.float32(amax) / np.float32(2688.0)
+    sfv = np.array([[orc.decode("e4m3", s) for s in row] for row in q.sf_logical])
+    assert sfv.max() <= 448 and (q.sf_logical < 0x80).all()
+    dq = q.dequantize() * q.tensor_scale
+    blkmax = np.abs(xf).reshape(32, 4, 16).max(axis=2)
+    # E2M1 step is at most 2^-1 of the block's top binade: error <= block max / 4 * (1 + 1/8)
+    err = np.abs(dq - xf).reshape(32, 4, 16).max(axis=2)
+    assert np.all(err <= blkmax / 4 * 1.126 + 1e-12)
+
+
+def test_quantize_rejects_unsupported():
+    x = _bits(workloads.draw("normal", (32, 32), 1))
+    with pytest.raises(ValueError):
+        orc.quantize(x, "mxfp8", rounding="sr")
+    with pytest.raises(ValueError):
+        orc.quantize(x, "nvfp4", hadamard=True)
+    with pytest.raises(ValueError):
+        orc.quantize(_bits(workloads.draw("normal", (32, 24), 1)), "mxfp8")
+
+
+def test_hadamard_wgrad_identity():
+    """(H a)^T (H b) = 32 a^T b: transforming both operands along K and scaling
+    the product by 1/32 leaves dW unchanged up to quantization error."""
+    dy = workloads.draw("student_t3", (64, 32), 21, 1e-3)
+    xx = workloads.draw("normal", (64, 48), 22)
+    exact = dy.double().t() @ xx.double()
+    qa = orc.quantize(_bits(dy), "mxfp4", "col", hadamard=True)
+    qb = orc.quantize(_bits(xx), "mxfp4", "col", hadamard=True)
+    c, _ = orc.gemm(qa, qb, extra_alpha=1.0 / 32)
+    rel = np.linalg.norm(c - exact.numpy()) / np.linalg.norm(exact.numpy())
+    assert rel < 0.3
+    qa0 = orc.quantize(_bits(dy), "mxfp8", "col", hadamard=True)
+    qb0 = orc.quantize(_bits(xx), "mxfp8", "col", hadamard=True)
+    c0, _ = orc.gemm(qa0, qb0, extra_alpha=1.0 / 32)
+    assert np.linalg.norm(c0 - exact.numpy()) / np.linalg.norm(exact.numpy()) < 0.05
+
+
+# ------------------------------------------------------------------ GEMM ---
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4", "moss"])
+def test_gemm_matches_numpy_fp64_matmul(fmt):
+    a = workloads.draw("student_t3", (40, 64), 31)
+    b = workloads.draw("normal", (24, 64), 32, 0.02)
+    qa, qb = orc.quantize(_bits(a), fmt), orc.quantize(_bits(b), fmt)
+    c, cabs = orc.gemm(qa, qb, extra_alpha=0.5)
+    alpha = np.float32(np.float32(np.float32(qa.tensor_scale or 1) * np.float32(qb.tensor_scale or 1)) * np.float32(0.5))
+    ref = float(alpha) * (qa.dequantize() @ qb.dequantize().T)
+    assert np.allclose(c, ref, rtol=1e-12, atol=1e-300)
+    assert np.allclose(cabs, abs(float(alpha)) * (np.abs(qa.dequantize()) @ np.abs(qb.dequantize()).T), rtol=1e-12)
+    rows, cols = [3, 17, 39], [0, 5, 23]
+    cs, _ = orc.gemm(qa, qb, extra_alpha=0.5, rows=rows, cols=cols)
+    assert np.array_equal(cs, c[np.ix_(rows, cols)])
+
+
+def test_gemm_exact_on_small_integers():
+    # codes that are small integers with unit scales: every partial sum exact
+    rng = np.random.default_rng(8)
+    vals = np.array([-6, -4, -3, -2, -1, 0, 1, 2, 3, 4, 6])  # representable in E2M1 too
+    a = torch.tensor(rng.choice(vals, (16, 64)), dtype=torch.float32).to(torch.bfloat16)
+    b = torch.tensor(rng.choice(vals, (8, 64)), dtype=torch.float32).to(torch.bfloat16)
+    exact = (a.double() @ b.double().t()).numpy()
+    for fmt in ("mxfp8", "mxfp4"):
+        qa = orc.quantize(_bits(a), fmt, rule="ceil")
+        qb = orc.quantize(_bits(b), fmt, rule="ceil")
+        assert np.array_equal(qa.dequantize(), a.double().numpy())
+        c, _ = orc.gemm(qa, qb)
+        assert np.array_equal(c, exact)
