@@ -1,0 +1,272 @@
+"""GB300-native block-scaled (MXFP8 / MXFP4 / NVFP4 / MOSS two-level FP8) linear layer.
+
+A thin ctypes binding over ``libmx_gb300.so`` (C ABI in ``include/mx.h``).  This
+module only marshals arguments: every step of quantize, GEMM and the linear
+layer's passes runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams.  There is no CPU fallback: without the built library (see
+``build()``) or an sm_103 GPU every call raises ``MXError``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmx_gb300.so")
+
+FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3}
+BLOCK = {"mxfp8": 32, "mxfp4": 32, "nvfp4": 16, "moss": 32}
+FP4 = ("mxfp4", "nvfp4")
+ROUNDING = {"rne": 0, "sr": 1}
+RULES = {"default": 0, "floor": 1, "ceil": 2, "nearest": 3}
+DIRS = {"row": 0, "col": 1}
+OUT = {torch.float32: 0, torch.bfloat16: 1}
+
+MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
+MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
+
+EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_dequantize", "mx_gemm",
+            "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_bwd", "mx_strerror",
+            "mx_last_device_status", "mx_selftest_bounded_wait", "mx_debug_set_gemm_tile_n")
+
+
+class MXError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (mx_status {code})" if what else strerror(code))
+
+
+class _CTensor(C.Structure):
+    _fields_ = [("codes", C.c_void_p), ("sf", C.c_void_p), ("amax", C.c_void_p),
+                ("tensor_scale", C.c_void_p), ("rows", C.c_int64), ("k", C.c_int64),
+                ("fmt", C.c_int32), ("block", C.c_int32), ("hadamard", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
+class _CBwdOpts(C.Structure):
+    _fields_ = [("wgrad_hadamard", C.c_int32), ("wgrad_dy_rounding", C.c_int32),
+                ("seed", C.c_uint64), ("stream_id", C.c_uint32), ("reserved", C.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libmx_gb300.so in-tree for sm_103a (nvcc)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise MXError(MX_ERR_NO_DEVICE, f"{LIB_PATH} is not built (call build())")
+            L = C.CDLL(LIB_PATH)
+            p, i64, i32, u64, u32, sz = C.c_void_p, C.c_int64, C.c_int, C.c_uint64, C.c_uint32, C.c_size_t
+            L.mx_codes_bytes.restype = sz
+            L.mx_codes_bytes.argtypes = [i32, i64, i64]
+            L.mx_sf_bytes.restype = sz
+            L.mx_sf_bytes.argtypes = [i32, i64, i64]
+            L.mx_amax.restype = i32
+            L.mx_amax.argtypes = [p, i64, i64, i64, p, p]
+            L.mx_quantize.restype = i32
+            L.mx_quantize.argtypes = [p, i64, i64, i64, i32, i32, i32, i32, i32, u64, u32, i32, p,
+                                      C.POINTER(_CTensor), p]
+            L.mx_dequantize.restype = i32
+            L.mx_dequantize.argtypes = [C.POINTER(_CTensor), p, p]
+            L.mx_gemm.restype = i32
+            L.mx_gemm.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float, p, i64, i32, p]
+            L.mx_linear_workspace_bytes.restype = sz
+            L.mx_linear_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
+            L.mx_linear_fwd.restype = i32
+            L.mx_linear_fwd.argtypes = [p, p, i64, i64, i64, i32, p, i32, p, sz, p]
+            L.mx_linear_bwd.restype = i32
+            L.mx_linear_bwd.argtypes = [p, p, p, i64, i64, i64, i32, C.POINTER(_CBwdOpts), p, i32, p,
+                                        i32, p, sz, p]
+            L.mx_strerror.restype = C.c_char_p
+            L.mx_strerror.argtypes = [i32]
+            L.mx_last_device_status.restype = i32
+            L.mx_last_device_status.argtypes = [p]
+            L.mx_selftest_bounded_wait.restype = i32
+            L.mx_selftest_bounded_wait.argtypes = [u64, p]
+            L.mx_debug_set_gemm_tile_n.restype = None
+            L.mx_debug_set_gemm_tile_n.argtypes = [i32]
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().mx_strerror(int(code)).decode()
+    except Exception:
+        return f"mx_status {code}"
+
+
+def _check(rc: int, what: str):
+    if rc != MX_OK:
+        raise MXError(rc, what)
+
+
+def _stream(stream=None):
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None  # the library reports MX_ERR_NO_DEVICE
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _on_gpu(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise MXError(MX_ERR_NO_DEVICE if not torch.cuda.is_available() else MX_ERR_INVALID_ARG,
+                          "tensors must live on a CUDA device (there is no CPU path)")
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+class MXTensor:
+    """A quantized K-major operand: codes, swizzled block scales, amax and tensor scale."""
+
+    def __init__(self, fmt: str, rows: int, k: int, device=None):
+        device = device or torch.device("cuda")
+        self.fmt, self.rows, self.k = fmt, int(rows), int(k)
+        self.block = BLOCK[fmt]
+        self.hadamard = False
+        L = lib()
+        nc = L.mx_codes_bytes(FORMATS[fmt], self.rows, self.k)
+        ns = L.mx_sf_bytes(FORMATS[fmt], self.rows, self.k)
+        if (nc == 0 or ns == 0) and self.rows * self.k > 0:
+            raise MXError(MX_ERR_INVALID_ARG, f"operand shape {rows}x{k} for {fmt}")
+        kb = self.k // 2 if fmt in FP4 else self.k
+        self.codes = torch.empty((self.rows, kb), dtype=torch.uint8, device=device)
+        self.sf = torch.empty(max(ns, 1), dtype=torch.uint8, device=device)
+        self.scalars = torch.zeros(2, dtype=torch.float32, device=device)  # amax, tensor scale
+
+    @property
+    def amax(self):
+        return self.scalars[0:1]
+
+    @property
+    def tensor_scale(self):
+        return self.scalars[1:2]
+
+    def _c(self) -> _CTensor:
+        t = _CTensor()
+        t.codes = self.codes.data_ptr()
+        t.sf = self.sf.data_ptr()
+        t.amax = self.scalars.data_ptr()
+        t.tensor_scale = self.scalars.data_ptr() + 4
+        t.rows, t.k = self.rows, self.k
+        t.fmt, t.block, t.hadamard = FORMATS[self.fmt], self.block, int(self.hadamard)
+        return t
+
+
+def amax(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _on_gpu(x)
+    out = out if out is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().mx_amax(_ptr(x), x.shape[0], x.shape[1], x.stride(0), _ptr(out), _stream(stream)),
+           "mx_amax")
+    return out
+
+
+def quantize(x: torch.Tensor, fmt: str, direction: str = "row", rounding: str = "rne",
+             rule: str = "default", seed: int = 0, stream_id: int = 0, hadamard: bool = False,
+             amax_in: torch.Tensor | None = None, out: MXTensor | None = None, stream=None) -> MXTensor:
+    """bf16 [R, C] -> block-scaled K-major operand (rowwise: [R, C]; colwise: [C, R])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _on_gpu(x, amax_in)
+    R, Cc = x.shape
+    rows, k = (R, Cc) if direction == "row" else (Cc, R)
+    q = out if out is not None else MXTensor(fmt, rows, k, x.device)
+    ct = q._c()
+    rc = lib().mx_quantize(_ptr(x), R, Cc, x.stride(0), DIRS[direction], FORMATS[fmt], BLOCK[fmt],
+                           ROUNDING[rounding], RULES[rule], seed, stream_id, int(bool(hadamard)),
+                           _ptr(amax_in), C.byref(ct), _stream(stream))
+    _check(rc, "mx_quantize")
+    q.rows, q.k, q.hadamard = ct.rows, ct.k, bool(ct.hadamard)
+    return q
+
+
+def dequantize(q: MXTensor, stream=None) -> torch.Tensor:
+    out = torch.empty((q.rows, q.k), dtype=torch.float32, device=q.codes.device)
+    ct = q._c()
+    _check(lib().mx_dequantize(C.byref(ct), _ptr(out), _stream(stream)), "mx_dequantize")
+    return out
+
+
+def gemm(a: MXTensor, b: MXTensor, extra_alpha: float = 1.0, out_dtype=torch.float32,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C[M, N] = alpha * dq(a) dq(b)^T on the tensor cores."""
+    out = out if out is not None else torch.empty((a.rows, b.rows), dtype=out_dtype,
+                                                  device=a.codes.device)
+    ca, cb = a._c(), b._c()
+    rc = lib().mx_gemm(C.byref(ca), C.byref(cb), float(extra_alpha), _ptr(out), out.stride(0),
+                       OUT[out.dtype], _stream(stream))
+    _check(rc, "mx_gemm")
+    return out
+
+
+def workspace_bytes(T: int, Kin: int, Nout: int, fmt: str, pass_: str = "fwd") -> int:
+    return int(lib().mx_linear_workspace_bytes(T, Kin, Nout, FORMATS[fmt], 0 if pass_ == "fwd" else 1))
+
+
+def linear_fwd(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloat16,
+               workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """Y = X W^T with X [T, Kin], W [Nout, Kin] (bf16, contiguous)."""
+    _on_gpu(X, W)
+    T, Kin = X.shape
+    Nout = W.shape[0]
+    n = workspace_bytes(T, Kin, Nout, fmt, "fwd")
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=X.device)
+    Y = out if out is not None else torch.empty((T, Nout), dtype=out_dtype, device=X.device)
+    rc = lib().mx_linear_fwd(_ptr(X), _ptr(W), T, Kin, Nout, FORMATS[fmt], _ptr(Y), OUT[Y.dtype],
+                             _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mx_linear_fwd")
+    return Y
+
+
+def linear_bwd(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor, fmt: str,
+               wgrad_hadamard: bool = False, wgrad_dy_rounding: str = "rne", seed: int = 0,
+               stream_id: int = 0, dx_dtype=torch.bfloat16, dw_dtype=torch.float32,
+               need_dx: bool = True, need_dw: bool = True, workspace: torch.Tensor | None = None,
+               dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None):
+    """dX = dY W and dW = dY^T X for the layer Y = X W^T."""
+    _on_gpu(dY, X, W)
+    T, Kin = X.shape
+    Nout = W.shape[0]
+    n = workspace_bytes(T, Kin, Nout, fmt, "bwd")
+    ws = workspace if workspace is not None else torch.empty(n, dtype=torch.uint8, device=X.device)
+    if need_dx and dX is None:
+        dX = torch.empty((T, Kin), dtype=dx_dtype, device=X.device)
+    if need_dw and dW is None:
+        dW = torch.empty((Nout, Kin), dtype=dw_dtype, device=X.device)
+    o = _CBwdOpts(int(bool(wgrad_hadamard)), ROUNDING[wgrad_dy_rounding], seed, stream_id, 0)
+    rc = lib().mx_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), T, Kin, Nout, FORMATS[fmt], C.byref(o),
+                             _ptr(dX) if need_dx else None, OUT[dX.dtype] if need_dx else 0,
+                             _ptr(dW) if need_dw else None, OUT[dW.dtype] if need_dw else 0,
+                             _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mx_linear_bwd")
+    return dX, dW
+
+
+def last_device_status(stream=None) -> int:
+    return int(lib().mx_last_device_status(_stream(stream)))
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> int:
+    return int(lib().mx_selftest_bounded_wait(int(limit_ns), _stream(stream)))
+
+
+def set_gemm_tile_n(bn: int) -> None:
+    lib().mx_debug_set_gemm_tile_n(int(bn))

@@ -1,0 +1,385 @@
+// gemm.cu -- the block-scaled GEMM of the linear layer on sm_103a tensor cores.
+//
+// C[M, N] = alpha * sum_k (codeA * sfA)(codeB * sfB), both operands K-major.
+// The main loop is pure tensor-core work: the per-block scales are applied
+// inside tcgen05.mma (kind::mxf8f6f4 / mxf4 / mxf4nvf4 with block_scale) and
+// the single remaining dequantisation, the fp32 factor alpha from the tensor
+// scales, happens once in the epilogue ("MOSS: 用微缩放和自动缩放实现无损 FP8
+// 训练", section GEMM Kernel 优化: the main loop is 100% tensor core, the
+// output is dequantised once in the epilogue).
+//
+// One CTA computes a 128 x BN tile with three warp roles:
+//   warp 0 (one thread)  TMA producer: per K-stage, the A and B code tiles
+//                        (128-byte swizzled rows) by cp.async.bulk.tensor and
+//                        the matching 512-byte scale-factor chunks by
+//                        cp.async.bulk, all completing on the stage's mbarrier.
+//   warp 1 (one thread)  MMA issuer: copies the stage's scale factors into
+//                        TMEM with tcgen05.cp, issues four block-scaled MMAs
+//                        into the TMEM accumulator, and frees the stage with
+//                        tcgen05.commit.  Warp 1 also owns the TMEM allocation.
+//   warps 2-5            epilogue: tcgen05.ld of the accumulator (each warp
+//                        reads its 32-lane quarter), x alpha, fp32 or bf16 store.
+// Every mbarrier wait is bounded (mbar_wait_bounded); a wait that gives up
+// records MX_ERR_TIMEOUT, stops issuing, drains what is in flight and frees
+// TMEM before the CTA exits.
+#include <algorithm>
+#include <cstdio>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "mx_internal.cuh"
+#include "mx_ptx.cuh"
+
+namespace mx {
+namespace {
+
+// KIND: 0 = E4M3 with E8M0 scales per 32 (MXFP8, MOSS), 1 = E2M1 with E8M0 per
+// 32 (MXFP4), 2 = E2M1 with UE4M3 per 16 (NVFP4).
+template <int KIND, int BN_, int STAGES_>
+struct Cfg {
+    static constexpr int BM = 128, BN = BN_, STAGES = STAGES_;
+    static constexpr int BKB = 128;                       // K bytes of codes per stage
+    static constexpr int EPB = KIND == 0 ? 1 : 2;          // elements per byte
+    static constexpr int BK = BKB * EPB;                   // K elements per stage
+    static constexpr int BLOCK = KIND == 2 ? 16 : 32;
+    static constexpr int MMA_K_BYTES = 32;                 // K bytes per tcgen05.mma
+    static constexpr int MMAS = BKB / MMA_K_BYTES;         // 4
+    static constexpr int BPM = MMA_K_BYTES * EPB / BLOCK;  // scale blocks per MMA: 1, 2, 4
+    static constexpr int NCHUNK = MMAS * BPM / 4;          // 512-byte SF chunks per 128 rows per stage
+    static constexpr int NRT_B = BN / 128;                 // 128-row B tiles per CTA tile
+    static constexpr int A_BYTES = BM * BKB;
+    static constexpr int B_BYTES = BN * BKB;
+    static constexpr int SFA_BYTES = NCHUNK * 512;
+    static constexpr int SFB_BYTES = NRT_B * NCHUNK * 512;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + (2 * STAGES + 1) * 8 + 16;
+    static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // room to align the base to 1024
+    // TMEM columns: fp32 accumulator, then per-stage SFA and SFB regions.
+    static constexpr int SFA_COLS = 4 * NCHUNK;
+    static constexpr int SFB_COLS = 4 * NCHUNK * NRT_B;
+    static constexpr int TM_SFA = BN;
+    static constexpr int TM_SFB = TM_SFA + STAGES * SFA_COLS;
+    static constexpr int TM_USED = TM_SFB + STAGES * SFB_COLS;
+    static constexpr int TM_ALLOC = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
+                                  : TM_USED <= 256 ? 256 : 512;
+    static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;  // E4M3 (f8f6f4) / E2M1 (mxf4*)
+    static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
+    static_assert(TM_USED <= 512, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(BN % 128 == 0 && BN <= 256, "tile N");
+};
+
+struct GemmParams {
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    const float* tsa;
+    const float* tsb;
+    float extra;
+    void* c;
+    int64_t ldc;
+    int M, N, K;
+    int out_bf16;
+    int64_t kgroups;  // 4-block SF groups along K (same for A and B)
+    int* status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void record_timeout(const GemmParams& p, volatile int* abort_flag)
+{
+    atomicExch(p.status, MX_ERR_TIMEOUT);
+    *abort_flag = 1;
+}
+
+template <int KIND, int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p)
+{
+    using G = Cfg<KIND, BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t bar0 = s0 + G::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t accf = bar0 + 8u * (2 * STAGES);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_BAR + 8 * (2 * STAGES + 1));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.y, n_tile = blockIdx.x;
+    const int num_kt = p.K / G::BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(accf, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), G::TM_ALLOC);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // B row tiles that exist in the padded scale-factor buffer.
+            const int nrt_b = min(G::NRT_B, (p.N + 127) / 128 - n_tile * G::NRT_B);
+            const uint32_t tx = G::A_BYTES + G::B_BYTES + G::SFA_BYTES + nrt_b * G::NCHUNK * 512;
+            int kt = 0;
+            for (; kt < num_kt; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t round = static_cast<uint32_t>(kt / STAGES);
+                if (kt >= STAGES && !mbar_wait_bounded(empty(s), (round - 1) & 1u, p.wait_ns)) {
+                    record_timeout(p, abort_flag);
+                    break;
+                }
+                if (*abort_flag)
+                    break;
+                mbar_arrive_expect_tx(full(s), tx);
+                tma_load_2d(s0 + G::OFF_A + s * G::A_BYTES, &tmA, full(s), kt * G::BKB, m_tile * G::BM);
+                tma_load_2d(s0 + G::OFF_B + s * G::B_BYTES, &tmB, full(s), kt * G::BKB, n_tile * BN);
+                bulk_load(s0 + G::OFF_SFA + s * G::SFA_BYTES,
+                          p.sfa + (static_cast<int64_t>(m_tile) * p.kgroups + static_cast<int64_t>(kt) * G::NCHUNK) * 512,
+                          G::SFA_BYTES, full(s));
+                for (int rt = 0; rt < nrt_b; ++rt)
+                    bulk_load(s0 + G::OFF_SFB + s * G::SFB_BYTES + rt * G::NCHUNK * 512,
+                              p.sfb + (static_cast<int64_t>(n_tile * G::NRT_B + rt) * p.kgroups +
+                                       static_cast<int64_t>(kt) * G::NCHUNK) * 512,
+                              G::NCHUNK * 512, full(s));
+            }
+            if (*abort_flag) {
+                // Let the copies already issued land before the CTA can exit.
+                for (int k2 = max(0, kt - STAGES); k2 < kt; ++k2)
+                    (void)mbar_wait_bounded(full(k2 % STAGES), static_cast<uint32_t>(k2 / STAGES) & 1u, kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int kt = 0; kt < num_kt; ++kt) {
+                const int s = kt % STAGES;
+                const uint32_t round = static_cast<uint32_t>(kt / STAGES);
+                if (!mbar_wait_bounded(full(s), round & 1u, p.wait_ns)) {
+                    record_timeout(p, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
+                const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
+#pragma unroll
+                for (int c = 0; c < G::NCHUNK; ++c)
+                    tc_cp_sf(sfa_t + 4 * c, sdesc_sf(s0 + G::OFF_SFA + s * G::SFA_BYTES + c * 512));
+#pragma unroll
+                for (int rt = 0; rt < G::NRT_B; ++rt)
+#pragma unroll
+                    for (int c = 0; c < G::NCHUNK; ++c)
+                        tc_cp_sf(sfb_t + 4 * (c * G::NRT_B + rt),
+                                 sdesc_sf(s0 + G::OFF_SFB + s * G::SFB_BYTES + (rt * G::NCHUNK + c) * 512));
+                const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES);
+                const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES);
+#pragma unroll
+                for (int i = 0; i < G::MMAS; ++i) {
+                    const int fb = i * G::BPM;  // first scale block of this MMA in the stage
+                    const int chunk = fb / 4;
+                    const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
+                    const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, G::BM, BN, sf_id, sf_id);
+                    // advance the start address by 32 bytes of K inside the swizzled rows
+                    const uint64_t koff = static_cast<uint64_t>((i * G::MMA_K_BYTES) >> 4);
+                    mma_bs<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk,
+                                 sfb_t + 4 * G::NRT_B * chunk, (kt > 0 || i > 0) ? 1u : 0u);
+                }
+                tc_commit(empty(s));
+            }
+            tc_commit(accf);  // fires once every MMA issued above has completed
+        }
+        __syncwarp();
+    } else {
+        // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows.
+        const int q = warp & 3;
+        const int row = m_tile * G::BM + q * 32 + lane;
+        if (!mbar_wait_bounded(accf, 0, p.wait_ns)) {
+            record_timeout(p, abort_flag);
+        } else {
+            tc_fence_after();
+            const float ta = p.tsa ? *p.tsa : 1.0f, tb = p.tsb ? *p.tsb : 1.0f;
+            const float alpha = __fmul_rn(__fmul_rn(ta, tb), p.extra);
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + j * 32, r);
+                tmem_ld_wait();
+                const int col0 = n_tile * BN + j * 32;
+                if (row < p.M && col0 < p.N) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+                    const bool full_chunk = col0 + 32 <= p.N;
+                    if (p.out_bf16) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
+                        if (full_chunk) {
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * w + 2 * h], v[8 * w + 2 * h + 1]);
+                                    pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    dst[i] = __float2bfloat16_rn(v[i]);
+                        }
+                    } else {
+                        float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
+                        if (full_chunk) {
+#pragma unroll
+                            for (int w = 0; w < 8; ++w)
+                                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    dst[i] = v[i];
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        if (*abort_flag && lane == 0)
+            (void)mbar_wait_bounded(accf, 0, kWaitLimitNs);  // no MMA may still write TMEM
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, G::TM_ALLOC);
+    }
+}
+
+// ------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 2-D map over a row-major byte matrix [rows, row_bytes] with 128-byte swizzled
+// boxes of box_rows x 128 bytes.
+bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int BN, int STAGES>
+int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
+                const Device& d, cudaStream_t s)
+{
+    using G = Cfg<KIND, BN, STAGES>;
+    static int configured_device = -1;  // attribute set once per device for this instantiation
+    if (configured_device != d.id) {
+        if (cudaFuncSetAttribute(bs_gemm_kernel<KIND, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 G::SMEM_ALLOC) != cudaSuccess)
+            return MX_ERR_CUDA;
+        configured_device = d.id;
+    }
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    const int64_t kbytes = K / G::EPB;
+    CUtensorMap ta, tb;
+    if (!make_code_map(&ta, A->codes, M, kbytes, G::BM) || !make_code_map(&tb, B->codes, N, kbytes, BN))
+        return MX_ERR_CUDA;
+    GemmParams p;
+    p.sfa = A->sf;
+    p.sfb = B->sf;
+    p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
+    p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
+    p.extra = extra;
+    p.c = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.out_bf16 = out_dtype == MX_OUT_BF16;
+    p.kgroups = sf_kgroups(K / G::BLOCK);
+    p.status = d.status;
+    p.wait_ns = kWaitLimitNs;
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + G::BM - 1) / G::BM));
+    bs_gemm_kernel<KIND, BN, STAGES><<<grid, 192, G::SMEM_ALLOC, s>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+template <int KIND>
+int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
+                const Device& d, cudaStream_t s, int bn)
+{
+    if (bn == 128)
+        return launch_tile<KIND, 128, 4>(A, B, extra, C, ldc, out_dtype, d, s);
+    return launch_tile<KIND, 256, 4>(A, B, extra, C, ldc, out_dtype, d, s);
+}
+
+}  // namespace
+
+// Tile width override for tests (0 = automatic).
+static int g_force_bn = 0;
+
+int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
+                const Device& d, cudaStream_t s)
+{
+    if (A->rows == 0 || B->rows == 0)
+        return MX_OK;
+    const int bn = g_force_bn ? g_force_bn : (B->rows > 128 ? 256 : 128);
+    switch (A->fmt) {
+    case MX_FMT_MXFP8_E4M3:
+    case MX_FMT_MOSS_FP8:
+        return launch_kind<0>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    case MX_FMT_MXFP4_E2M1:
+        return launch_kind<1>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    case MX_FMT_NVFP4:
+        return launch_kind<2>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    default:
+        return MX_ERR_INVALID_ARG;
+    }
+}
+
+void set_gemm_tile_n(int bn) { g_force_bn = (bn == 128 || bn == 256) ? bn : 0; }
+
+}  // namespace mx

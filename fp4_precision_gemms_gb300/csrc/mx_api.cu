@@ -1,0 +1,417 @@
+// mx_api.cu -- the extern "C" entry points declared in include/mx.h: argument
+// validation on the host, the per-device status word, and the composition of
+// quantize + GEMM into a linear layer's forward, data-gradient and
+// weight-gradient passes.
+#include <cstring>
+#include <mutex>
+
+#include "mx_internal.cuh"
+
+namespace mx {
+
+// Per-device status word written by kernels whose bounded waits give up.
+__device__ int g_status_word;
+
+void set_gemm_tile_n(int bn);
+
+int current_device(Device* d)
+{
+    static std::mutex mu;
+    static Device cache[64];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return MX_ERR_NO_DEVICE;
+    }
+    if (dev >= 64)
+        return MX_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].id == dev) {
+        *d = cache[dev];
+        return MX_OK;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MX_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3)
+        return MX_ERR_UNSUPPORTED;
+    void* status = nullptr;
+    if (cudaGetSymbolAddress(&status, g_status_word) != cudaSuccess)
+        return MX_ERR_CUDA;
+    cache[dev].id = dev;
+    cache[dev].sms = sms;
+    cache[dev].status = static_cast<int*>(status);
+    *d = cache[dev];
+    return MX_OK;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_fmt(int fmt) { return fmt >= MX_FMT_MXFP8_E4M3 && fmt <= MX_FMT_MOSS_FP8; }
+
+int64_t codes_row_bytes(int fmt, int64_t k) { return fmt_is_fp4(fmt) ? k / 2 : k; }
+
+// K granularity the GEMM consumes per pipeline stage.
+int64_t gemm_k_multiple(int fmt) { return fmt_is_fp4(fmt) ? 256 : 128; }
+
+int check_operand(const mx_tensor* t)
+{
+    if (!t || !valid_fmt(t->fmt) || t->rows < 0 || t->k < 0 || t->block != fmt_block(t->fmt))
+        return MX_ERR_INVALID_ARG;
+    if ((t->rows > 0 && t->k > 0) && (!t->codes || !t->sf))
+        return MX_ERR_INVALID_ARG;
+    if (fmt_has_tensor_scale(t->fmt) && !t->tensor_scale)
+        return MX_ERR_INVALID_ARG;
+    if (!aligned16(t->codes) || !aligned16(t->sf))
+        return MX_ERR_ALIGNMENT;
+    return MX_OK;
+}
+
+struct Operand {  // an mx_tensor carved out of a workspace
+    mx_tensor t;
+};
+
+// Carves the buffers of one quantized operand out of `ws` (256-byte aligned
+// pieces); returns the bytes used.  With ws == NULL only counts.
+size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
+{
+    size_t off = 0;
+    const size_t cb = round_up(mx_codes_bytes(fmt, rows, k), 256);
+    const size_t sb = round_up(mx_sf_bytes(fmt, rows, k), 256);
+    if (t) {
+        std::memset(t, 0, sizeof *t);
+        t->codes = ws ? ws + off : nullptr;
+        t->sf = ws ? ws + off + cb : nullptr;
+        t->amax = ws ? reinterpret_cast<float*>(ws + off + cb + sb) : nullptr;
+        t->tensor_scale = ws ? reinterpret_cast<float*>(ws + off + cb + sb + 16) : nullptr;
+    }
+    off += cb + sb + 256;
+    return off;
+}
+
+int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fmt, int block, int rounding,
+                  int rule, uint64_t seed, uint32_t stream_id, int hadamard, const float* amax_in, mx_tensor* out,
+                  const Device& d, cudaStream_t s)
+{
+    if (!out || !valid_fmt(fmt) || (dir != MX_ROWWISE && dir != MX_COLWISE) || R < 0 || C < 0 || ld < C)
+        return MX_ERR_INVALID_ARG;
+    if (rounding != MX_ROUND_RNE && rounding != MX_ROUND_SR)
+        return MX_ERR_INVALID_ARG;
+    if (rule < MX_SCALE_DEFAULT || rule > MX_SCALE_NEAREST)
+        return MX_ERR_INVALID_ARG;
+    if (block != fmt_block(fmt))
+        return MX_ERR_UNSUPPORTED;
+    if (rounding == MX_ROUND_SR && !fmt_is_fp4(fmt))
+        return MX_ERR_UNSUPPORTED;
+    if (hadamard && !(fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MXFP4_E2M1))
+        return MX_ERR_UNSUPPORTED;
+    if (fmt == MX_FMT_NVFP4 && rule != MX_SCALE_DEFAULT)
+        return MX_ERR_UNSUPPORTED;
+    const int64_t rows = dir == MX_ROWWISE ? R : C;
+    const int64_t k = dir == MX_ROWWISE ? C : R;
+    if (k % block != 0 || (dir == MX_COLWISE && R % 32 != 0))
+        return MX_ERR_ALIGNMENT;
+    if (ld % 8 != 0 || !aligned16(x) || !aligned16(out->codes))
+        return MX_ERR_ALIGNMENT;
+    if (R > 0 && C > 0 && (!x || !out->codes || !out->sf))
+        return MX_ERR_INVALID_ARG;
+    const bool ts = fmt_has_tensor_scale(fmt);
+    if (ts && (!out->amax || !out->tensor_scale))
+        return MX_ERR_INVALID_ARG;
+    if (rule == MX_SCALE_DEFAULT)
+        rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
+    out->rows = rows;
+    out->k = k;
+    out->fmt = fmt;
+    out->block = block;
+    out->hadamard = hadamard ? 1 : 0;
+    if (ts) {
+        if (amax_in) {
+            if (amax_in != out->amax &&
+                cudaMemcpyAsync(out->amax, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+                return MX_ERR_CUDA;
+        } else {
+            const int rc = launch_amax(x, R, C, ld, out->amax, d, s);
+            if (rc != MX_OK)
+                return rc;
+        }
+    }
+    if (R == 0 || C == 0) {  // nothing to encode; the tensor scale of an all-zero tensor is 1
+        static const float one = 1.0f;
+        if (ts && cudaMemcpyAsync(out->tensor_scale, &one, sizeof one, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+        return MX_OK;
+    }
+    QuantArgs q;
+    q.x = static_cast<const uint16_t*>(x);
+    q.R = R;
+    q.C = C;
+    q.ld = ld;
+    q.dir = dir;
+    q.fmt = fmt;
+    q.rounding = rounding;
+    q.rule = rule;
+    q.hadamard = hadamard ? 1 : 0;
+    q.seed = seed;
+    q.stream_id = stream_id;
+    q.amax = out->amax;
+    q.tensor_scale = out->tensor_scale;
+    q.codes = static_cast<uint8_t*>(out->codes);
+    q.sf = out->sf;
+    return launch_quantize(q, d, s);
+}
+
+int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
+              const Device& d, cudaStream_t s)
+{
+    int rc = check_operand(A);
+    if (rc != MX_OK)
+        return rc;
+    rc = check_operand(B);
+    if (rc != MX_OK)
+        return rc;
+    if (A->fmt != B->fmt || A->k != B->k || A->hadamard != B->hadamard)
+        return MX_ERR_INVALID_ARG;
+    if (out_dtype != MX_OUT_F32 && out_dtype != MX_OUT_BF16)
+        return MX_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    if (M == 0 || N == 0)
+        return MX_OK;
+    if (!C || ldc < N)
+        return MX_ERR_INVALID_ARG;
+    if (ldc % 8 != 0 || !aligned16(C) || K % gemm_k_multiple(A->fmt) != 0)
+        return MX_ERR_ALIGNMENT;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return MX_ERR_UNSUPPORTED;
+    const size_t esz = out_dtype == MX_OUT_BF16 ? 2 : 4;
+    if (K == 0)
+        return cudaMemset2DAsync(C, ldc * esz, 0, N * esz, M, s) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+    const float extra = A->hadamard ? extra_alpha * (1.0f / 32.0f) : extra_alpha;
+    return launch_gemm(A, B, extra, C, ldc, out_dtype, d, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mx_codes_bytes(int fmt, int64_t rows, int64_t k)
+{
+    if (!valid_fmt(fmt) || rows < 0 || k < 0 || (fmt_is_fp4(fmt) && k % 2))
+        return 0;
+    return static_cast<size_t>(rows) * static_cast<size_t>(codes_row_bytes(fmt, k));
+}
+
+size_t mx_sf_bytes(int fmt, int64_t rows, int64_t k)
+{
+    if (!valid_fmt(fmt) || rows < 0 || k < 0 || k % fmt_block(fmt))
+        return 0;
+    return static_cast<size_t>(sf_layout_bytes(rows, k / fmt_block(fmt)));
+}
+
+int mx_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, void* stream)
+{
+    if (!amax || R < 0 || C < 0 || ld < C || (R > 0 && C > 0 && !x))
+        return MX_ERR_INVALID_ARG;
+    if (ld % 8 != 0 || C % 8 != 0 || !aligned16(x))
+        return MX_ERR_ALIGNMENT;
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return launch_amax(x, R, C, ld, amax, d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_quantize(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fmt, int block, int rounding,
+                int scale_rule, uint64_t seed, uint32_t stream_id, int hadamard, const float* amax_in,
+                mx_tensor* out, void* stream)
+{
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return quantize_impl(x, R, C, ld, dir, fmt, block, rounding, scale_rule, seed, stream_id, hadamard, amax_in, out,
+                         d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_dequantize(const mx_tensor* A, float* out, void* stream)
+{
+    int rc = check_operand(A);
+    if (rc != MX_OK)
+        return rc;
+    if (!out && A->rows * A->k > 0)
+        return MX_ERR_INVALID_ARG;
+    Device d;
+    rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return launch_dequantize(A, out, d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
+            void* stream)
+{
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return gemm_impl(A, B, extra_alpha, C, ldc, out_dtype, d, static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return 0;
+    if (pass == 0)
+        return carve(nullptr, fmt, T, Kin, nullptr) + carve(nullptr, fmt, Nout, Kin, nullptr);
+    // dgrad: dY rowwise [T, Nout], W^T [Kin, Nout]; wgrad: dY^T [Nout, T], X^T [Kin, T]
+    return carve(nullptr, fmt, T, Nout, nullptr) + carve(nullptr, fmt, Kin, Nout, nullptr) +
+           carve(nullptr, fmt, Nout, T, nullptr) + carve(nullptr, fmt, Kin, T, nullptr);
+}
+
+int mx_linear_fwd(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt, void* Y,
+                  int out_dtype, void* workspace, size_t ws_bytes, void* stream)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return MX_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < mx_linear_workspace_bytes(T, Kin, Nout, fmt, 0))
+        return MX_ERR_WORKSPACE;
+    Device d;
+    int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mx_tensor xq, wq;
+    const size_t off = carve(ws, fmt, T, Kin, &xq);
+    carve(ws + off, fmt, Nout, Kin, &wq);
+    const int block = fmt_block(fmt);
+    rc = quantize_impl(X, T, Kin, Kin, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0, nullptr, &xq,
+                       d, s);
+    if (rc != MX_OK)
+        return rc;
+    rc = quantize_impl(W, Nout, Kin, Kin, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0, nullptr,
+                       &wq, d, s);
+    if (rc != MX_OK)
+        return rc;
+    return gemm_impl(&xq, &wq, 1.0f, Y, Nout, out_dtype, d, s);
+}
+
+int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt,
+                  const mx_bwd_opts* opts, void* dX, int dx_dtype, void* dW, int dw_dtype, void* workspace,
+                  size_t ws_bytes, void* stream)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return MX_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < mx_linear_workspace_bytes(T, Kin, Nout, fmt, 1))
+        return MX_ERR_WORKSPACE;
+    mx_bwd_opts o;
+    std::memset(&o, 0, sizeof o);
+    if (opts)
+        o = *opts;
+    Device d;
+    int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mx_tensor dyr, wt, dyt, xt;
+    size_t off = carve(ws, fmt, T, Nout, &dyr);
+    off += carve(ws + off, fmt, Kin, Nout, &wt);
+    off += carve(ws + off, fmt, Nout, T, &dyt);
+    carve(ws + off, fmt, Kin, T, &xt);
+    const int block = fmt_block(fmt);
+    const bool ts = fmt_has_tensor_scale(fmt);
+    if (dX) {
+        rc = quantize_impl(dY, T, Nout, Nout, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
+                           nullptr, &dyr, d, s);
+        if (rc != MX_OK)
+            return rc;
+        rc = quantize_impl(W, Nout, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
+                           nullptr, &wt, d, s);
+        if (rc != MX_OK)
+            return rc;
+        rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s);
+        if (rc != MX_OK)
+            return rc;
+    }
+    if (dW) {
+        // dY's tensor amax is shared by its rowwise and colwise quantizations.
+        const float* dy_amax = (dX && ts) ? dyr.amax : nullptr;
+        rc = quantize_impl(dY, T, Nout, Nout, MX_COLWISE, fmt, block, o.wgrad_dy_rounding, MX_SCALE_DEFAULT, o.seed,
+                           o.stream_id, o.wgrad_hadamard, dy_amax, &dyt, d, s);
+        if (rc != MX_OK)
+            return rc;
+        rc = quantize_impl(X, T, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0,
+                           o.wgrad_hadamard, nullptr, &xt, d, s);
+        if (rc != MX_OK)
+            return rc;
+        rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s);
+    }
+    return rc;
+}
+
+const char* mx_strerror(int status)
+{
+    switch (status) {
+    case MX_OK: return "ok";
+    case MX_ERR_INVALID_ARG: return "invalid argument";
+    case MX_ERR_UNSUPPORTED: return "unsupported format, option or device";
+    case MX_ERR_ALIGNMENT: return "alignment or size-multiple rule violated";
+    case MX_ERR_CUDA: return "CUDA call failed";
+    case MX_ERR_TIMEOUT: return "device-side bounded wait timed out";
+    case MX_ERR_NO_DEVICE: return "no usable CUDA device";
+    case MX_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+int mx_last_device_status(void* stream)
+{
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MX_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess)
+        return MX_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess)
+        return MX_ERR_CUDA;
+    return v;
+}
+
+int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream)
+{
+    Device d;
+    int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = launch_wait_selftest(limit_ns, d, s);
+    if (rc != MX_OK)
+        return rc;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess)
+        return MX_ERR_CUDA;
+    return v;
+}
+
+// Test hook: force the GEMM tile width (128 or 256; 0 = automatic).
+void mx_debug_set_gemm_tile_n(int bn) { set_gemm_tile_n(bn); }
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// mx_internal.cuh -- declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mx.h"
+
+namespace mx {
+
+// Element encodings and block sizes per format.
+__host__ __device__ constexpr bool fmt_is_fp4(int fmt) { return fmt == MX_FMT_MXFP4_E2M1 || fmt == MX_FMT_NVFP4; }
+__host__ __device__ constexpr int fmt_block(int fmt) { return fmt == MX_FMT_NVFP4 ? 16 : 32; }
+__host__ __device__ constexpr bool fmt_has_tensor_scale(int fmt) { return fmt == MX_FMT_NVFP4 || fmt == MX_FMT_MOSS_FP8; }
+
+// Scale-factor layout of the tensor core: 512-byte tiles of 128 rows x 4 K-blocks.
+__host__ __device__ inline int64_t sf_kgroups(int64_t kblocks) { return (kblocks + 3) / 4; }
+__host__ __device__ inline int64_t sf_layout_bytes(int64_t rows, int64_t kblocks)
+{
+    return ((rows + 127) / 128) * sf_kgroups(kblocks) * 512;
+}
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t kb, int64_t kgroups)
+{
+    return ((r >> 7) * kgroups + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+
+struct Device {
+    int id = -1;
+    int sms = 0;
+    int* status = nullptr;  // device address of the per-device status word
+};
+
+// Current device after checking it is an sm_103 part; MX_OK or an error.
+int current_device(Device* d);
+
+// Default bound on every device-side wait (ns).  Healthy waits are microseconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct QuantArgs {
+    const uint16_t* x;
+    int64_t R, C, ld;
+    int dir, fmt, rounding, rule, hadamard;
+    uint64_t seed;
+    uint32_t stream_id;
+    const float* amax;     // device: tensor amax (NVFP4/MOSS), already final
+    float* tensor_scale;   // device output (NVFP4/MOSS)
+    uint8_t* codes;
+    uint8_t* sf;
+};
+
+int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d,
+                cudaStream_t s);
+int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s);
+int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStream_t s);
+int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
+                int out_dtype, const Device& d, cudaStream_t s);
+int launch_wait_selftest(uint64_t limit_ns, const Device& d, cudaStream_t s);
+
+}  // namespace mx

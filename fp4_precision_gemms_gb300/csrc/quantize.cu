@@ -1,0 +1,563 @@
+// quantize.cu -- the fused quantize producer of the block-scaled linear layer.
+//
+//   amax_kernel        max |x| over a bf16 tensor (level-1 scale input of MOSS
+//                      and NVFP4; "MOSS: 用微缩放和自动缩放实现无损 FP8 训练",
+//                      section 两级缩放实现).
+//   quant_row_kernel   bf16 [R, C] -> K-major operand [R, C]: each thread owns
+//                      8 consecutive elements (one 16-byte load); the 2 or 4
+//                      threads of a scale block combine their maxima with warp
+//                      shuffles; codes leave as one coalesced 8- or 4-byte store.
+//   quant_col_kernel   bf16 [R, C] -> transposed operand [C, R] (quantized along
+//                      R): each thread owns one input column and 32 bytes of
+//                      output codes, so the transpose costs no shared memory.
+// Both write the block scales straight into the tensor core's scale-factor
+// layout ("格式感知融合:让FP4预训练提速两倍的工程实践", section
+// 格式感知融合的设计思路: the producer writes the consumer's layout), and both
+// can apply the fixed-sign 32-point Hadamard transform and Philox stochastic
+// rounding (same page, section 两个关键的数值技巧).
+//
+// Bit-exactness: every step is an exactly specified fp32 operation (products
+// and quotients with __fmul_rn/__fdiv_rn, adds in a fixed butterfly order) or
+// an integer decision, so the codes and scale bytes are a pure function of the
+// input, independent of launch shape.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+
+#include "mx_internal.cuh"
+#include "mx_ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kElemE4M3 = 0, kElemE2M1 = 1;
+
+__host__ __device__ constexpr int elem_of(int fmt)
+{
+    return (fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MOSS_FP8) ? kElemE4M3 : kElemE2M1;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ------------------------------------------------------------ scale rules
+// b > 0 finite as (1 + mant * 2^-23) * 2^fb, exactly (subnormals normalised).
+struct Norm {
+    int fb;
+    uint32_t mant;
+};
+
+__device__ __forceinline__ Norm normalize_pos(float b)
+{
+    const uint32_t u = __float_as_uint(b);
+    const int E = static_cast<int>((u >> 23) & 0xFFu);
+    const uint32_t m = u & 0x7FFFFFu;
+    if (E != 0)
+        return {E - 127, m};
+    const int msb = 31 - __clz(m);  // b = m * 2^-149
+    return {msb - 149, (m << (23 - msb)) & 0x7FFFFFu};
+}
+
+// Power-of-two exponent e of a block with max |y| = b: the block is scaled by
+// 2^-e and its E8M0 byte is e + 127.  Q = 448 = 1.75 * 2^8 (E4M3) or
+// 6 = 1.5 * 2^2 (E2M1).  All decisions are made on the exact significand.
+template <int ELEM>
+__device__ __forceinline__ int pow2_exponent(float b, int rule)
+{
+    if (b == 0.0f)
+        return 0;
+    constexpr int fq = ELEM == kElemE4M3 ? 8 : 2;              // floor(log2 Q) (= emax)
+    constexpr uint32_t mq = ELEM == kElemE4M3 ? 0x600000u : 0x400000u;  // Q significand bits
+    const Norm n = normalize_pos(b);
+    int e;
+    if (rule == MX_SCALE_FLOOR) {
+        e = n.fb - fq;  // floor(log2 b) - emax
+    } else if (rule == MX_SCALE_CEIL) {
+        e = n.fb - fq + (n.mant > mq ? 1 : 0);  // smallest e with b * 2^-e <= Q
+    } else {  // NEAREST: round(log2(b / Q)) decided on squared significands
+        const uint64_t MB = (1ull << 23) | n.mant, MQ = (1ull << 23) | mq;
+        if (n.mant >= mq)
+            e = n.fb - fq + ((MB * MB >= 2 * MQ * MQ) ? 1 : 0);
+        else
+            e = n.fb - fq - 1 + ((2 * MB * MB >= MQ * MQ) ? 1 : 0);
+    }
+    return max(-127, min(127, e));
+}
+
+// 2^-e as an fp32 value, e in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float exp2_neg(int e)
+{
+    const int x = 127 - e;
+    return x > 0 ? __uint_as_float(static_cast<uint32_t>(x) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ------------------------------------------------------------------ casts
+// Round-to-nearest-even, saturating; `lo` lands in the low byte/nibble.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float dec_e4m3_pos(uint32_t c)
+{
+    const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
+    return e == 0 ? static_cast<float>(m) * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Stochastic rounding onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}: up iff
+// u16 < p * 2^16, p = (|s| - lo) / (hi - lo); every step below is exact.
+__device__ __forceinline__ uint32_t e2m1_sr(float s, uint32_t u16)
+{
+    const uint32_t sign = (__float_as_uint(s) >> 31) << 3;
+    const float a = fabsf(s);
+    if (a >= 6.0f)
+        return sign | 7u;
+    float lo, inv_step;
+    uint32_t code;
+    if (a < 2.0f) {
+        lo = floorf(a * 2.0f) * 0.5f;
+        inv_step = 2.0f;
+        code = static_cast<uint32_t>(lo * 2.0f);
+    } else if (a < 4.0f) {
+        lo = floorf(a);
+        inv_step = 1.0f;
+        code = static_cast<uint32_t>(lo) + 2u;
+    } else {
+        lo = 4.0f;
+        inv_step = 0.5f;
+        code = 6u;
+    }
+    if (a == lo)
+        return sign | code;
+    const float p16 = __fmul_rn(__fsub_rn(a, lo), inv_step * 65536.0f);
+    return sign | (static_cast<float>(u16) < p16 ? code + 1u : code);
+}
+
+// ------------------------------------------------------------- Philox4x32-10
+// Salmon et al., SC'11: two 32x32 -> 64 multiplies per round, ten rounds, the
+// key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The 8 random 16-bit draws of the 8 elements with linear index L8*8 .. L8*8+7.
+__device__ __forceinline__ void sr_bits8(uint64_t seed, uint32_t sid, uint64_t L8, uint32_t (&u)[8])
+{
+    const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(L8), static_cast<uint32_t>(L8 >> 32), sid, 0u),
+                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+    u[0] = w.x & 0xFFFFu; u[1] = w.x >> 16;
+    u[2] = w.y & 0xFFFFu; u[3] = w.y >> 16;
+    u[4] = w.z & 0xFFFFu; u[5] = w.z >> 16;
+    u[6] = w.w & 0xFFFFu; u[7] = w.w >> 16;
+}
+
+// In-register butterflies of the fixed-sign Sylvester transform over N values
+// (stages h = 1, 2, 4, ... < N): (x_j, x_j+h) <- (x_j + x_j+h, x_j - x_j+h).
+template <int N>
+__device__ __forceinline__ void fwht_local(float* v)
+{
+#pragma unroll
+    for (int h = 1; h < N; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if ((j & h) == 0) {
+                const float a = v[j], b = v[j + h];
+                v[j] = __fadd_rn(a, b);
+                v[j + h] = __fsub_rn(a, b);
+            }
+}
+
+// Butterfly stage across lanes: partner lane = lane ^ mask; the lower lane
+// keeps x_lo + x_hi, the upper one x_lo - x_hi.
+__device__ __forceinline__ void fwht_lanes(float (&v)[8], int mask, bool upper)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float p = __shfl_xor_sync(0xFFFFFFFFu, v[i], mask);
+        v[i] = upper ? __fsub_rn(p, v[i]) : __fadd_rn(v[i], p);
+    }
+}
+
+__device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
+{
+    if (fmt == MX_FMT_MOSS_FP8 || fmt == MX_FMT_NVFP4) {
+        const float am = *amax;
+        return am == 0.0f ? 1.0f : __fdiv_rn(am, fmt == MX_FMT_MOSS_FP8 ? 448.0f : 2688.0f);
+    }
+    return 1.0f;
+}
+
+// ---------------------------------------------------------- block encoding
+// Encodes one scale block held as N consecutive values in registers (the
+// block's max |v| is `bmax`).  Produces the scale byte and N codes packed
+// little-endian into `out` (E4M3: N bytes; E2M1: N/2 bytes).  `L8` is the
+// Philox counter of the first 8 elements (used only for SR).
+template <int FMT, bool SR, int N>
+__device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, float ts, float nv_denom,
+                                                 int rule, uint64_t seed, uint32_t sid, uint64_t L8,
+                                                 uint32_t* out)
+{
+    constexpr int ELEM = elem_of(FMT);
+    uint32_t sfbyte;
+    bool zero = false;
+    if constexpr (FMT == MX_FMT_NVFP4) {
+        const uint32_t sb = cvt_e4m3x2(__fdiv_rn(bmax, nv_denom), 0.0f) & 0x7Fu;
+        const float d = __fmul_rn(dec_e4m3_pos(sb), ts);
+        sfbyte = sb;
+        if (d == 0.0f)
+            zero = true;
+        else
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                v[i] = __fdiv_rn(v[i], d);
+    } else {
+        const int e = pow2_exponent<ELEM>(bmax, rule);
+        const float s2 = exp2_neg(e);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            v[i] = __fmul_rn(v[i], s2);
+        sfbyte = static_cast<uint32_t>(e + 127);
+    }
+    if constexpr (ELEM == kElemE4M3) {
+#pragma unroll
+        for (int w = 0; w < N / 4; ++w)
+            out[w] = cvt_e4m3x2(v[4 * w], v[4 * w + 1]) | (cvt_e4m3x2(v[4 * w + 2], v[4 * w + 3]) << 16);
+    } else {
+#pragma unroll
+        for (int w = 0; w < N / 8; ++w) {
+            uint32_t word = 0;
+            if (zero) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    word |= ((__float_as_uint(v[8 * w + i]) >> 31) << 3) << (4 * i);
+            } else if constexpr (SR) {
+                uint32_t u[8];
+                sr_bits8(seed, sid, L8 + w, u);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    word |= e2m1_sr(v[8 * w + i], u[i]) << (4 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    word |= cvt_e2m1x2(v[8 * w + 2 * i], v[8 * w + 2 * i + 1]) << (8 * i);
+            }
+            out[w] = word;
+        }
+    }
+    return sfbyte;
+}
+
+// ---------------------------------------------------------------- kernels
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restrict__ x, int64_t R,
+                                                        int64_t C, int64_t ld, unsigned* __restrict__ out)
+{
+    const int64_t cpr = C / 8;
+    uint32_t m2 = 0;  // two packed |bf16| maxima
+    auto fold = [&](const uint4& w) {
+        m2 = __vmaxu2(m2, w.x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w.y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w.z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, w.w & 0x7FFF7FFFu);
+    };
+    const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (ld == C) {  // contiguous: one flat stream of 16-byte chunks, two loads in flight
+        const uint4* p = reinterpret_cast<const uint4*>(x);
+        const int64_t total = R * cpr;
+        int64_t t = tid;
+        for (; t + nthr < total; t += 2 * nthr) {
+            const uint4 a = __ldg(p + t), b = __ldg(p + t + nthr);
+            fold(a);
+            fold(b);
+        }
+        if (t < total)
+            fold(__ldg(p + t));
+    } else {
+        for (int64_t r = blockIdx.y; r < R; r += gridDim.y)
+            for (int64_t c8 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c8 < cpr;
+                 c8 += static_cast<int64_t>(gridDim.x) * blockDim.x)
+                fold(__ldg(reinterpret_cast<const uint4*>(x + r * ld + c8 * 8)));
+    }
+    unsigned m = max(m2 & 0xFFFFu, m2 >> 16) << 16;  // bf16 bits -> fp32 bits of |x|
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    __shared__ unsigned wmax[kThreads / 32];
+    if ((threadIdx.x & 31) == 0)
+        wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        m = threadIdx.x < kThreads / 32 ? wmax[threadIdx.x] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (threadIdx.x == 0)
+            atomicMax(out, m);
+    }
+}
+
+// Rowwise producer.  One work item = one row and 256*U consecutive 8-element
+// chunks of it; a thread handles U chunks (U loads in flight).
+template <int FMT, bool SR, bool HAD>
+__global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
+{
+    constexpr int BLOCK = fmt_block(FMT);
+    constexpr int LPB = BLOCK / 8;  // lanes per scale block
+    constexpr int U = 2;
+    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
+    const int lane = threadIdx.x & 31;
+    const int64_t C = a.C, cpr = C / 8;
+    const int64_t kgroups = sf_kgroups(C / BLOCK);
+    const int64_t items_per_row = (cpr + kThreads * U - 1) / (kThreads * U);
+    const int64_t items = a.R * items_per_row;
+    const float ts = tensor_scale_of(FMT, a.amax);
+    const float nv_denom = __fmul_rn(6.0f, ts);
+    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
+        *a.tensor_scale = ts;
+
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int64_t r = item / items_per_row;
+        const int64_t cbase = (item - r * items_per_row) * (kThreads * U) + threadIdx.x;
+        const uint16_t* xr = a.x + r * a.ld;
+        uint4 w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c8 = cbase + u * kThreads;
+            w[u] = c8 < cpr ? __ldg(reinterpret_cast<const uint4*>(xr + c8 * 8)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c8 = cbase + u * kThreads;
+            // Whole scale blocks are either all in range or all out of range
+            // (C % BLOCK == 0), so the shuffles below stay within valid groups.
+            if (cbase - threadIdx.x + u * kThreads >= cpr)
+                break;  // warp-uniform: the whole CTA slice is past the row end
+            float v[8] = {bf16_lo(w[u].x), bf16_hi(w[u].x), bf16_lo(w[u].y), bf16_hi(w[u].y),
+                          bf16_lo(w[u].z), bf16_hi(w[u].z), bf16_lo(w[u].w), bf16_hi(w[u].w)};
+            if constexpr (HAD) {
+                fwht_local<8>(v);
+                fwht_lanes(v, 1, (lane & 1) != 0);
+                fwht_lanes(v, 2, (lane & 2) != 0);
+            }
+            if constexpr (FMT == MX_FMT_MOSS_FP8) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = __fdiv_rn(v[i], ts);
+            }
+            float bmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                bmax = fmaxf(bmax, fabsf(v[i]));
+#pragma unroll
+            for (int m = 1; m < LPB; m <<= 1)
+                bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, m));
+            if (c8 < cpr) {
+                uint32_t out[2];
+                const uint32_t sfb = encode_block<FMT, SR, 8>(v, bmax, ts, nv_denom, a.rule, a.seed,
+                                                              a.stream_id, r * cpr + c8, out);
+                if constexpr (FP4)
+                    *reinterpret_cast<uint32_t*>(a.codes + r * (C / 2) + c8 * 4) = out[0];
+                else
+                    *reinterpret_cast<uint2*>(a.codes + r * C + c8 * 8) = make_uint2(out[0], out[1]);
+                if ((lane & (LPB - 1)) == 0)
+                    a.sf[sf_offset(r, (c8 * 8) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
+            }
+        }
+    }
+}
+
+// Colwise producer: operand row c (= input column c), K = R.  A thread owns
+// one column and SEG consecutive input rows (32 bytes of output codes).
+template <int FMT, bool SR, bool HAD>
+__global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
+{
+    constexpr int BLOCK = fmt_block(FMT);
+    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
+    constexpr int SEG = FP4 ? 64 : 32;
+    const int64_t c = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    const int64_t R = a.R, C = a.C;
+    const float ts = tensor_scale_of(FMT, a.amax);
+    const float nv_denom = __fmul_rn(6.0f, ts);
+    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        *a.tensor_scale = ts;
+    if (c >= C)
+        return;
+    const int64_t kgroups = sf_kgroups(R / BLOCK);
+    const int64_t nsegs = (R + SEG - 1) / SEG;
+    const int64_t row_bytes = FP4 ? R / 2 : R;
+    for (int64_t seg = blockIdx.y; seg < nsegs; seg += gridDim.y) {
+        const int64_t k0 = seg * SEG;
+        const int nk = static_cast<int>(R - k0 < SEG ? R - k0 : SEG);  // multiple of 32
+        const uint16_t* xc = a.x + k0 * a.ld + c;
+        uint32_t out[8];
+#pragma unroll
+        for (int b = 0; b < SEG / BLOCK; ++b) {
+            float blk[BLOCK];
+            const bool in = b * BLOCK < nk;  // whole blocks only: nk is a multiple of 32
+#pragma unroll
+            for (int i = 0; i < BLOCK; ++i)
+                blk[i] = in ? __uint_as_float(static_cast<uint32_t>(__ldg(xc + (b * BLOCK + i) * a.ld)) << 16) : 0.0f;
+            if constexpr (HAD)
+                fwht_local<BLOCK>(blk);
+            if constexpr (FMT == MX_FMT_MOSS_FP8) {
+#pragma unroll
+                for (int i = 0; i < BLOCK; ++i)
+                    blk[i] = __fdiv_rn(blk[i], ts);
+            }
+            float bmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BLOCK; ++i)
+                bmax = fmaxf(bmax, fabsf(blk[i]));
+            constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
+            const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
+            const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, ts, nv_denom, a.rule, a.seed,
+                                                              a.stream_id, L8, out + b * WPB);
+            if (b * BLOCK < nk)
+                a.sf[sf_offset(c, (k0 + b * BLOCK) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
+        }
+        uint8_t* dst = a.codes + c * row_bytes + (FP4 ? k0 / 2 : k0);
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        if (nk == SEG)
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ sf,
+                                                           const float* __restrict__ ts, int64_t rows,
+                                                           int64_t k, int fmt, float* __restrict__ out)
+{
+    const int block = fmt_block(fmt);
+    const int64_t kgroups = sf_kgroups(k / block);
+    const float t = (fmt_has_tensor_scale(fmt) && ts) ? *ts : 1.0f;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * k;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / k, j = i - r * k;
+        float cv;
+        if (fmt_is_fp4(fmt)) {
+            const uint32_t byte = codes[r * (k / 2) + j / 2];
+            const uint32_t n = (j & 1) ? (byte >> 4) : (byte & 0xFu);
+            const float mags[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+            cv = (n & 8u) ? -mags[n & 7u] : mags[n & 7u];
+        } else {
+            const uint32_t byte = codes[r * k + j];
+            const float mag = dec_e4m3_pos(byte & 0x7Fu);
+            cv = (byte & 0x80u) ? -mag : mag;
+        }
+        const uint32_t s = sf[sf_offset(r, j / block, kgroups)];
+        const float sv = fmt == MX_FMT_NVFP4 ? dec_e4m3_pos(s) : exp2_neg(127 - static_cast<int>(s));
+        out[i] = __fmul_rn(__fmul_rn(cv, sv), t);
+    }
+}
+
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int* status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+        // Nothing ever arrives on `bar`: the wait must give up.
+        if (!mbar_wait_bounded(b, 0, limit_ns))
+            atomicExch(status, MX_ERR_TIMEOUT);
+    }
+}
+
+template <int FMT, bool SR, bool HAD>
+int launch_q(const QuantArgs& q, const Device& d, cudaStream_t s)
+{
+    if (q.dir == MX_ROWWISE) {
+        const int64_t cpr = q.C / 8;
+        const int64_t items = q.R * ((cpr + kThreads * 2 - 1) / (kThreads * 2));
+        const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(d.sms) * 8));
+        quant_row_kernel<FMT, SR, HAD><<<grid, kThreads, 0, s>>>(q);
+    } else {
+        constexpr int SEG = elem_of(FMT) == kElemE2M1 ? 64 : 32;
+        const int64_t gx = (q.C + kThreads - 1) / kThreads;
+        const int64_t nsegs = (q.R + SEG - 1) / SEG;
+        const int64_t want_y = std::max<int64_t>(1, (static_cast<int64_t>(d.sms) * 8 + gx - 1) / gx);
+        const int gy = static_cast<int>(std::min<int64_t>(std::min<int64_t>(nsegs, want_y * 4), 65535));
+        quant_col_kernel<FMT, SR, HAD><<<dim3(static_cast<unsigned>(gx), gy), kThreads, 0, s>>>(q);
+    }
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d, cudaStream_t s)
+{
+    if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (R == 0 || C == 0)
+        return MX_OK;
+    const int64_t chunks = R * (C / 8);
+    dim3 grid;
+    if (ld == C) {
+        grid.x = static_cast<unsigned>(std::max<int64_t>(
+            1, std::min<int64_t>((chunks + kThreads - 1) / kThreads, static_cast<int64_t>(d.sms) * 8)));
+    } else {
+        grid.x = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((C / 8 + kThreads - 1) / kThreads, 64)));
+        grid.y = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(R, (static_cast<int64_t>(d.sms) * 8 + grid.x - 1) / grid.x)));
+    }
+    amax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld, reinterpret_cast<unsigned*>(amax));
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s)
+{
+    const bool sr = q.rounding == MX_ROUND_SR;
+    const bool had = q.hadamard != 0;
+    switch (q.fmt) {
+    case MX_FMT_MXFP8_E4M3:
+        return had ? launch_q<MX_FMT_MXFP8_E4M3, false, true>(q, d, s)
+                   : launch_q<MX_FMT_MXFP8_E4M3, false, false>(q, d, s);
+    case MX_FMT_MXFP4_E2M1:
+        if (sr)
+            return had ? launch_q<MX_FMT_MXFP4_E2M1, true, true>(q, d, s)
+                       : launch_q<MX_FMT_MXFP4_E2M1, true, false>(q, d, s);
+        return had ? launch_q<MX_FMT_MXFP4_E2M1, false, true>(q, d, s)
+                   : launch_q<MX_FMT_MXFP4_E2M1, false, false>(q, d, s);
+    case MX_FMT_NVFP4:
+        return sr ? launch_q<MX_FMT_NVFP4, true, false>(q, d, s) : launch_q<MX_FMT_NVFP4, false, false>(q, d, s);
+    case MX_FMT_MOSS_FP8:
+        return launch_q<MX_FMT_MOSS_FP8, false, false>(q, d, s);
+    default:
+        return MX_ERR_INVALID_ARG;
+    }
+}
+
+int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStream_t s)
+{
+    const int64_t n = A->rows * A->k;
+    if (n == 0)
+        return MX_OK;
+    const int grid = static_cast<int>(std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(d.sms) * 8));
+    dequant_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(A->codes), A->sf, A->tensor_scale, A->rows,
+                                             A->k, A->fmt, out);
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_wait_selftest(uint64_t limit_ns, const Device& d, cudaStream_t s)
+{
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, d.status);
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+}  // namespace mx

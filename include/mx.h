@@ -1,0 +1,221 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) block-scaled low-precision linear layer.
+ *
+ * The library quantizes bf16 tensors into block-scaled FP8/FP4 operands laid
+ * out for the 5th-generation tensor core, multiplies them with tcgen05
+ * block-scaled MMA, and composes the two into a linear layer's forward,
+ * data-gradient and weight-gradient passes.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [MOSS] "MOSS: 用微缩放和自动缩放实现无损 FP8 训练，OLMo-7B 加速 34%":
+ *          创新 1 (two-level scaling), Power-of-Two 的关键优势, 两级缩放实现,
+ *          GEMM Kernel 优化 (main loop on the tensor core, dequantise once in
+ *          the epilogue).
+ *   [COAT] "COAT: Compressing Optimizer States and Activation for memory
+ *          efficient FP8 Training" (article): FP8 量化最佳化器狀態的難點
+ *          (E4M3 range 448 .. 0.00195).
+ *   [FAF]  "格式感知融合:让FP4预训练提速两倍的工程实践":
+ *          FP4加速为何常常"纸上富贵" (E2M1; nvfp block scaling; MX mxfp),
+ *          格式感知融合的设计思路 (producer writes the consumer layout),
+ *          两个关键的数值技巧 (stochastic rounding of gradients, fixed-sign
+ *          32-point Hadamard on the weight gradient).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named x, X, W, dY, codes, sf, amax, tensor_scale, C, Y, dX,
+ *     dW and workspace are DEVICE pointers; the mx_tensor and mx_bwd_opts
+ *     structs themselves live in host memory.
+ *   - The caller owns all memory.  The library allocates no device memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     enqueues its work on that stream and returns without synchronising.
+ *   - Return value: MX_OK or an mx_status error code.  Argument errors are
+ *     found on the host before anything is launched.  A device-side bounded
+ *     wait that gives up records MX_ERR_TIMEOUT in a per-device status word
+ *     that mx_last_device_status() reads.
+ *   - bf16 inputs must be finite; NaN/Inf inputs give unspecified codes.
+ *   - Only sm_103 devices are supported (MX_ERR_UNSUPPORTED otherwise);
+ *     without a CUDA device calls return MX_ERR_NO_DEVICE.
+ */
+#ifndef MX_GB300_H
+#define MX_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mx_status {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = 1,  /* null pointer, bad enum, inconsistent shapes */
+    MX_ERR_UNSUPPORTED = 2,  /* format/option combination or device not supported */
+    MX_ERR_ALIGNMENT = 3,    /* pointer/leading-dimension/K alignment rule broken */
+    MX_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MX_ERR_TIMEOUT = 5,      /* a device-side bounded wait gave up */
+    MX_ERR_NO_DEVICE = 6,    /* no usable CUDA device */
+    MX_ERR_WORKSPACE = 7     /* workspace missing or smaller than required */
+} mx_status;
+
+/* Block-scaled formats.
+ * MXFP8_E4M3: E4M3 codes, one E8M0 (power-of-two) scale per 32 elements along
+ *             K ([FAF] mxfp, the MX standard).  No tensor scale.
+ * MXFP4_E2M1: E2M1 codes, one E8M0 scale per 32 elements.  No tensor scale.
+ * NVFP4:      E2M1 codes, one UE4M3 scale per 16 elements and an FP32 tensor
+ *             scale amax / (448 * 6) ([FAF] nvfp, block scaling under a
+ *             global scale).
+ * MOSS_FP8:   E4M3 codes, FP32 tensor scale amax / 448 times a power-of-two
+ *             micro scale per 32 elements ([MOSS] 创新 1, 两级缩放实现). */
+typedef enum mx_format {
+    MX_FMT_MXFP8_E4M3 = 0,
+    MX_FMT_MXFP4_E2M1 = 1,
+    MX_FMT_NVFP4 = 2,
+    MX_FMT_MOSS_FP8 = 3
+} mx_format;
+
+/* RNE: round to nearest, ties to even, saturating at the largest finite
+ * value.  SR: stochastic rounding ([FAF] 两个关键的数值技巧), E2M1 formats
+ * only: element L = r*K + k of the K-major operand rounds up iff u16 < p*2^16,
+ * p its distance fraction between the two neighbouring grid points and u16
+ * the 16-bit half (L odd: high, even: low) of word (L&7)>>1 of
+ * Philox4x32-10(counter = {L>>3, L>>35, stream_id, 0}, key = {seed, seed>>32}). */
+typedef enum mx_rounding { MX_ROUND_RNE = 0, MX_ROUND_SR = 1 } mx_rounding;
+
+/* Power-of-two scale rule for a block with max |y| = b (Q = 448, emax = 8 for
+ * E4M3; Q = 6, emax = 2 for E2M1).  DEFAULT = FLOOR for the MX formats and
+ * CEIL for MOSS; NVFP4 accepts DEFAULT only.
+ * FLOOR: e = floor(log2 b) - emax.  CEIL: smallest e with b*2^-e <= Q.
+ * NEAREST: e = round(log2(b/Q)) ([MOSS] 两级缩放实现's rounding to the
+ * nearest power of two).  e is clamped to [-127, 127]; b = 0 gives e = 0. */
+typedef enum mx_scale_rule {
+    MX_SCALE_DEFAULT = 0,
+    MX_SCALE_FLOOR = 1,
+    MX_SCALE_CEIL = 2,
+    MX_SCALE_NEAREST = 3
+} mx_scale_rule;
+
+/* ROWWISE quantizes x[R, C] along C (operand rows = R, K = C).
+ * COLWISE quantizes along R and writes the transposed operand
+ * (operand rows = C, K = R): the transpose is fused into the producer. */
+typedef enum mx_dir { MX_ROWWISE = 0, MX_COLWISE = 1 } mx_dir;
+
+typedef enum mx_out_dtype { MX_OUT_F32 = 0, MX_OUT_BF16 = 1 } mx_out_dtype;
+
+/* A quantized K-major operand.  Device buffers are caller-allocated:
+ *   codes        mx_codes_bytes(fmt, rows, k) bytes: row-major [rows, K];
+ *                E4M3 one byte per element; E2M1 two per byte, the even k in
+ *                the low nibble.  Row stride = K or K/2 bytes.
+ *   sf           mx_sf_bytes(fmt, rows, k) bytes: block scales in the tensor
+ *                core's scale-factor layout: 512-byte tiles of 128 rows x 4
+ *                K-blocks, ordered by row tile then K-block group; row r,
+ *                block kb at (r%32)*16 + ((r%128)/32)*4 + kb%4 inside its
+ *                tile ([FAF] 格式感知融合的设计思路: the producer writes the
+ *                consumer's layout).  Padding bytes are left unwritten.
+ *   amax         1 float: max |x| over the tensor (written for NVFP4, MOSS).
+ *   tensor_scale 1 float: the FP32 tensor scale (NVFP4, MOSS), else unused.
+ * mx_quantize fills rows, k, fmt, block and hadamard. */
+typedef struct mx_tensor {
+    void* codes;
+    uint8_t* sf;
+    float* amax;
+    float* tensor_scale;
+    int64_t rows;
+    int64_t k;
+    int32_t fmt;
+    int32_t block;
+    int32_t hadamard;
+    int32_t reserved;
+} mx_tensor;
+
+/* Byte sizes of an operand's buffers (0 for invalid arguments). */
+size_t mx_codes_bytes(int fmt, int64_t rows, int64_t k);
+size_t mx_sf_bytes(int fmt, int64_t rows, int64_t k);
+
+/* amax[0] = max |x| over a bf16 matrix x[R, C] with row stride ld elements
+ * (ld >= C, ld % 8 == 0, x 16-byte aligned).  [MOSS] 两级缩放实现, level 1. */
+int mx_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, void* stream);
+
+/* The fused quantize producer: bf16 x[R, C] (row stride ld elements) ->
+ * codes + block scales (+ amax and tensor scale) in *out.
+ *   block      32 for MXFP8/MXFP4/MOSS, 16 for NVFP4 (MX_ERR_UNSUPPORTED else).
+ *   rounding   MX_ROUND_SR only with E2M1 formats.
+ *   hadamard   1: multiply every 32-element K-block by the fixed-sign
+ *              Sylvester H32 (unnormalised, five fp32 butterfly stages in
+ *              the order h = 1, 2, 4, 8, 16) before scaling; MX formats only
+ *              ([FAF] 两个关键的数值技巧).
+ *   amax_in    optional device float holding max |x| (skips the amax pass of
+ *              NVFP4/MOSS; it is copied to out->amax); NULL = compute it.
+ *   seed, stream_id  the SR Philox key and third counter word.
+ * Alignment: x 16-byte aligned, ld % 8 == 0, K % block == 0; for COLWISE also
+ * R % 32 == 0.  out->codes 16-byte aligned. */
+int mx_quantize(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fmt, int block,
+                int rounding, int scale_rule, uint64_t seed, uint32_t stream_id, int hadamard,
+                const float* amax_in, mx_tensor* out, void* stream);
+
+/* out[r, k] (fp32, row-major [rows, K]) = dec(code) * dec(block scale) *
+ * tensor scale (if the format has one).  The inverse map of [MOSS]
+ * 两级缩放实现's dequantize; a test aid, not on the hot path. */
+int mx_dequantize(const mx_tensor* A, float* out, void* stream);
+
+/* The block-scaled GEMM: C[M, N] = alpha * dq(A) dq(B)^T with M = A->rows,
+ * N = B->rows, K = A->k = B->k, both operands K-major and of the same format.
+ * Block scales are applied inside the tcgen05 MMA; the epilogue multiplies the
+ * fp32 accumulator once by alpha = fl32(fl32(tsA * tsB) * e), tsX the tensor
+ * scales (1 when the format has none) and e = extra_alpha, times 1/32 when
+ * both operands carry the Hadamard transform ((H a)^T (H b) = 32 a^T b)
+ * ([MOSS] GEMM Kernel 优化: dequantise once in the epilogue).
+ * C is fp32 or bf16 (RNE), row stride ldc elements (ldc >= N, ldc % 8 == 0,
+ * C 16-byte aligned).  K % 128 == 0 for FP8 formats, K % 256 == 0 for FP4.
+ * A->hadamard must equal B->hadamard. */
+int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
+            int out_dtype, void* stream);
+
+/* Workspace bytes for mx_linear_fwd (pass 0) and mx_linear_bwd (pass 1). */
+size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass);
+
+/* Forward of a linear layer: Y[T, Nout] = X[T, Kin] W[Nout, Kin]^T, both
+ * operands quantized rowwise with RNE and the format's default rule, Y in
+ * out_dtype with row stride Nout.  workspace: device, >= the size above. */
+int mx_linear_fwd(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt,
+                  void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward options ([FAF] 两个关键的数值技巧: stochastic rounding of the
+ * gradient and a fixed-sign Hadamard-32 preconditioning of the weight
+ * gradient, both on the mxfp route). */
+typedef struct mx_bwd_opts {
+    int32_t wgrad_hadamard;   /* 1: H32 along tokens on both wgrad operands (MX formats) */
+    int32_t wgrad_dy_rounding;/* mx_rounding for dY^T in wgrad (SR: E2M1 formats) */
+    uint64_t seed;            /* SR Philox key */
+    uint32_t stream_id;       /* SR Philox counter word 2 */
+    int32_t reserved;
+} mx_bwd_opts;
+
+/* Backward of the same layer (opts NULL = RNE, no Hadamard):
+ *   dgrad dX[T, Kin]  = dY[T, Nout] W[Nout, Kin]   (dY rowwise, W colwise)
+ *   wgrad dW[Nout, Kin] = dY^T X                    (dY, X colwise)
+ * dX or dW may be NULL to skip that GEMM.  Outputs are row-major with row
+ * strides Kin, in dx_dtype / dw_dtype. */
+int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64_t Kin,
+                  int64_t Nout, int fmt, const mx_bwd_opts* opts, void* dX, int dx_dtype,
+                  void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/* Human-readable text of an mx_status. */
+const char* mx_strerror(int status);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device (MX_OK or MX_ERR_TIMEOUT). */
+int mx_last_device_status(void* stream);
+
+/* Self-test of the bounded-wait path: launches one block that waits on an
+ * mbarrier nothing ever arrives at, giving up after limit_ns nanoseconds.
+ * Synchronises the stream and returns MX_ERR_TIMEOUT when the wait gave up as
+ * designed (and the status word then reads MX_ERR_TIMEOUT), MX_OK never. */
+int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream);
+
+/* Test hook: force the GEMM's CTA tile width N to 128 or 256 (0 restores the
+ * automatic choice).  Affects later mx_gemm / mx_linear_* calls process-wide. */
+void mx_debug_set_gemm_tile_n(int bn);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MX_GB300_H */

@@ -83,23 +83,41 @@ double orc_decode_e8m0(unsigned code)
     return ldexp(1.0, (int)(code & 0xffu) - 127);
 }
 
-/* Nearest point of a monotone non-negative grid dec(0) = 0 < dec(1) < ... <
- * dec(maxcode); values at or above the largest point saturate to it; an exact
- * tie goes to the code whose mantissa LSB (= code LSB) is 0. */
-static unsigned nearest_grid_code(double a, double (*dec)(unsigned), unsigned maxcode)
+/* The non-negative value grids, decoded once from the bit patterns above:
+ * E4M3 codes 0x00..0x7E and E2M1 codes 0..7, strictly increasing. */
+static double g_e4m3_grid[0x7f];
+static double g_e2m1_grid[8];
+
+__attribute__((constructor)) static void init_grids(void)
 {
-    if (a >= dec(maxcode))
+    for (unsigned c = 0; c <= 0x7eu; ++c)
+        g_e4m3_grid[c] = orc_decode_e4m3(c);
+    for (unsigned c = 0; c <= 7u; ++c)
+        g_e2m1_grid[c] = orc_decode_e2m1(c);
+}
+
+/* Nearest point of an increasing non-negative grid g[0] = 0 < ... < g[maxcode]
+ * to a >= 0.  Values at or above the largest point saturate to it.  The
+ * nearest point is one of the two grid neighbours of a; an exact tie goes to
+ * the code whose mantissa LSB (= code LSB) is 0. */
+static unsigned nearest_grid_code(double a, const double* g, unsigned maxcode)
+{
+    if (a >= g[maxcode])
         return maxcode;
-    unsigned best = 0u;
-    double bestd = a;
-    for (unsigned c = 1u; c <= maxcode; ++c) {
-        double d = fabs(dec(c) - a);
-        if (d < bestd || (d == bestd && (c & 1u) == 0u)) {
-            best = c;
-            bestd = d;
-        }
+    unsigned lo = 0u, hi = maxcode; /* invariant: g[lo] <= a < g[hi] */
+    while (hi - lo > 1u) {
+        unsigned mid = (lo + hi) / 2u;
+        if (g[mid] <= a)
+            lo = mid;
+        else
+            hi = mid;
     }
-    return best;
+    double dlo = a - g[lo], dhi = g[hi] - a;
+    if (dlo < dhi)
+        return lo;
+    if (dhi < dlo)
+        return hi;
+    return (lo & 1u) ? hi : lo;
 }
 
 /* Round-to-nearest-even with saturation to the largest finite value (the
@@ -108,13 +126,13 @@ static unsigned nearest_grid_code(double a, double (*dec)(unsigned), unsigned ma
 unsigned orc_encode_e4m3_rne(float v)
 {
     unsigned s = signbit(v) ? 0x80u : 0u;
-    return s | nearest_grid_code(fabs((double)v), orc_decode_e4m3, 0x7eu);
+    return s | nearest_grid_code(fabs((double)v), g_e4m3_grid, 0x7eu);
 }
 
 unsigned orc_encode_e2m1_rne(float v)
 {
     unsigned s = signbit(v) ? 0x8u : 0u;
-    return s | nearest_grid_code(fabs((double)v), orc_decode_e2m1, 0x7u);
+    return s | nearest_grid_code(fabs((double)v), g_e2m1_grid, 0x7u);
 }
 
 /* Stochastic rounding onto the E2M1 grid ([FAF] 两个关键的数值技巧: round up

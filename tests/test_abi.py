@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads, and exports every function include/mx.h declares.
+
+These run without a GPU: only size queries, error strings and the no-device /
+argument-error paths are called (nothing is launched).
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+import fp4_precision_gemms_gb300 as mx
+from conftest import gpu_available
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(mx_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mx.build()
+    return mx.lib()
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(mx.EXPORTED)
+
+
+def test_size_queries(lib):
+    f = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3}
+    assert lib.mx_codes_bytes(f["mxfp8"], 256, 256) == 65536
+    assert lib.mx_codes_bytes(f["mxfp4"], 256, 256) == 32768
+    assert lib.mx_codes_bytes(f["nvfp4"], 3, 33) == 0  # odd K cannot be packed
+    # scale tiles: 128 rows x 4 blocks per 512 bytes, padded
+    assert lib.mx_sf_bytes(f["mxfp8"], 256, 256) == 2 * 2 * 512
+    assert lib.mx_sf_bytes(f["nvfp4"], 130, 64) == 2 * 1 * 512
+    assert lib.mx_sf_bytes(f["moss"], 11008, 4096) == 86 * 32 * 512
+    assert lib.mx_sf_bytes(f["mxfp8"], 8, 48) == 0  # K not a multiple of the block
+    assert lib.mx_sf_bytes(9, 8, 64) == 0
+    assert lib.mx_linear_workspace_bytes(8192, 4096, 6144, f["nvfp4"], 0) > 8192 * 2048 + 6144 * 2048
+
+
+def test_strerror(lib):
+    for code in range(8):
+        s = lib.mx_strerror(code).decode()
+        assert s and s != "unknown status"
+    assert lib.mx_strerror(99).decode() == "unknown status"
+
+
+@pytest.mark.skipif(gpu_available(), reason="checks the no-GPU error path")
+def test_calls_without_a_gpu_fail_loudly(lib):
+    t = mx._CTensor()
+    rc = lib.mx_quantize(None, 0, 0, 0, 0, 0, 32, 0, 0, 0, 0, 0, None, C.byref(t), None)
+    assert rc == mx.MX_ERR_NO_DEVICE
+    assert lib.mx_gemm(C.byref(t), C.byref(t), 1.0, None, 0, 0, None) == mx.MX_ERR_NO_DEVICE
+    assert lib.mx_last_device_status(None) == mx.MX_ERR_NO_DEVICE
+    with pytest.raises(mx.MXError):
+        mx.quantize(torch.zeros(32, 32, dtype=torch.bfloat16), "mxfp8")

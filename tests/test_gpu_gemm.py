@@ -1,0 +1,121 @@
+"""Parity of the tcgen05 block-scaled GEMM with the oracle's fp64 GEMM over the
+dequantised operands (and bit-exact where fp32 accumulation is exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads
+from parity import assert_gemm_close, bits
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import fp4_precision_gemms_gb300 as m
+    m.build()
+    yield m
+    m.set_gemm_tile_n(0)
+
+
+def quant_pair(mx, a, b, fmt, **kw):
+    qa, qb = mx.quantize(a.cuda(), fmt, **kw), mx.quantize(b.cuda(), fmt, **kw)
+    ra, rb = orc.quantize(bits(a), fmt, **kw), orc.quantize(bits(b), fmt, **kw)
+    return qa, qb, ra, rb
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_exact_small_integers(mx, fmt, bn):
+    """Small-integer codes with power-of-two scales: every partial sum is exact in
+    fp32, so the tensor core must reproduce the fp64 oracle bit for bit."""
+    mx.set_gemm_tile_n(bn)
+    rng = np.random.default_rng(1)
+    vals = np.array([-6, -4, -3, -2, -1, 0, 1, 2, 3, 4, 6])
+    a = torch.tensor(rng.choice(vals, (256, 512)), dtype=torch.float32).to(torch.bfloat16)
+    b = torch.tensor(rng.choice(vals, (384, 512)), dtype=torch.float32).to(torch.bfloat16)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt, rule="ceil")
+    c = mx.gemm(qa, qb)
+    ref, _ = orc.gemm(ra, rb)
+    assert np.array_equal(c.cpu().numpy().astype(np.float64), ref)
+    assert np.array_equal(ref, (a.double() @ b.double().t()).numpy())
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("bn", [128, 256])
+def test_scale_factor_layout_one_hot(mx, fmt, bn):
+    """Pins the swizzled scale layout against the hardware: with all-ones inputs,
+    raise single scale bytes of A and of B in the GPU buffers (at the offsets the
+    layout definition gives) and check every output against the oracle GEMM
+    computed with the same raised logical scales."""
+    mx.set_gemm_tile_n(bn)
+    M, N, K = 256, 384, 1024 if fmt in ("mxfp4", "nvfp4") else 512
+    a = torch.ones(M, K, dtype=torch.bfloat16)
+    b = torch.ones(N, K, dtype=torch.bfloat16)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    rng = np.random.default_rng(3)
+    for q, r in ((qa, ra), (qb, rb)):
+        kb = r.sf_logical.shape[1]
+        sf = q.sf.cpu().numpy()
+        for row in range(r.rows):
+            blk = int(rng.integers(0, kb))
+            # E8M0: +1 doubles the scale; UE4M3 (0x7E here): -8 halves it
+            new = int(r.sf_logical[row, blk]) + (1 if fmt != "nvfp4" else -8)
+            r.sf_logical[row, blk] = new
+            sf[orc.sf_index(row, blk, kb)] = new
+        q.sf.copy_(torch.from_numpy(sf))
+    c = mx.gemm(qa, qb)
+    ref, cabs = orc.gemm(ra, rb)
+    assert_gemm_close(c, ref, cabs, f"one-hot {fmt}", tol=1e-6)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mnk", [(256, 256, 256), (200, 136, 512), (384, 640, 1024), (130, 520, 256)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_random_gemm(mx, fmt, mnk, out_dtype):
+    M, N, K = mnk
+    if fmt in ("mxfp4", "nvfp4") and K % 256:
+        K = 256 * ((K + 255) // 256)
+    a = workloads.draw("student_t3", (M, K), 40 + M)
+    b = workloads.draw("normal", (N, K), 41 + N, 0.02)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    for bn in (128, 256):
+        mx.set_gemm_tile_n(bn)
+        c = mx.gemm(qa, qb, out_dtype=out_dtype)
+        ref, cabs = orc.gemm(ra, rb)
+        assert_gemm_close(c, ref, cabs, f"{fmt} {mnk} bn={bn}")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_hadamard_alpha(mx, fmt):
+    """Both operands transformed: the epilogue applies the 1/32 of (Ha)^T(Hb) = 32 a^T b."""
+    dy = workloads.draw("student_t3", (512, 256), 51, 1e-3)
+    x = workloads.draw("normal", (512, 384), 52)
+    qa = mx.quantize(dy.cuda(), fmt, "col", hadamard=True)
+    qb = mx.quantize(x.cuda(), fmt, "col", hadamard=True)
+    ra = orc.quantize(bits(dy), fmt, "col", hadamard=True)
+    rb = orc.quantize(bits(x), fmt, "col", hadamard=True)
+    c = mx.gemm(qa, qb, extra_alpha=0.5)
+    ref, cabs = orc.gemm(ra, rb, extra_alpha=0.5 / 32)
+    assert_gemm_close(c, ref, cabs, f"H32 {fmt}")
+
+
+def test_mixed_hadamard_rejected(mx):
+    x = workloads.draw("normal", (256, 256), 1).cuda()
+    qa = mx.quantize(x, "mxfp8", "col", hadamard=True)
+    qb = mx.quantize(x, "mxfp8", "col")
+    with pytest.raises(mx.MXError) as e:
+        mx.gemm(qa, qb)
+    assert e.value.code == mx.MX_ERR_INVALID_ARG
+
+
+def test_gemm_k_alignment_rejected(mx):
+    x = workloads.draw("normal", (128, 96), 1).cuda()
+    q = mx.quantize(x, "mxfp8")
+    with pytest.raises(mx.MXError) as e:
+        mx.gemm(q, q)
+    assert e.value.code == mx.MX_ERR_ALIGNMENT
+    assert mx.last_device_status() == mx.MX_OK

@@ -1,0 +1,162 @@
+"""Parity of the CUDA quantize producer with the oracle: bit-exact codes, scale
+bytes (in the tensor core's layout), amax and tensor scale."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads
+from parity import assert_quant_equal, bits
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import fp4_precision_gemms_gb300 as m
+    m.build()
+    assert torch.cuda.is_available()
+    return m
+
+
+def run_both(mx, x, fmt, direction="row", **kw):
+    q = mx.quantize(x.cuda(), fmt, direction, **kw)
+    torch.cuda.synchronize()
+    ref = orc.quantize(bits(x), fmt, direction, **kw)
+    return q, ref
+
+
+def test_status_word_starts_clear(mx):
+    assert mx.last_device_status() == mx.MX_OK
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_every_bf16_pattern(mx, fmt, direction):
+    """All 65280 finite bf16 values, seeded-shuffled so every block mixes binades."""
+    pats = workloads.all_bf16_patterns()
+    g = torch.Generator().manual_seed(0)
+    pats = pats[torch.randperm(pats.numel(), generator=g)]
+    x = torch.zeros(512 * 128, dtype=torch.bfloat16)
+    x[:pats.numel()] = pats
+    x = x.view(512, 128)
+    q, ref = run_both(mx, x, fmt, direction)
+    assert_quant_equal(q, ref, f"{fmt}/{direction}")
+
+
+@pytest.mark.parametrize("fmt,rule", [(f, r) for f in ("mxfp8", "mxfp4", "moss")
+                                      for r in ("floor", "ceil", "nearest")])
+def test_scale_rules(mx, fmt, rule):
+    x = workloads.draw("outliers", (256, 256), 11)
+    for direction in ("row", "col"):
+        q, ref = run_both(mx, x, fmt, direction, rule=rule)
+        assert_quant_equal(q, ref, f"{fmt}/{rule}/{direction}")
+
+
+SHAPES = [(416, 544), (128, 4096), (32, 32), (4096, 64)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("kind", ["student_t3", "lognormal_cols", "outliers"])
+def test_random_tensors(mx, fmt, shape, kind):
+    x = workloads.draw(kind, shape, 100 + shape[0])
+    for direction in ("row", "col"):
+        q, ref = run_both(mx, x, fmt, direction)
+        assert_quant_equal(q, ref, f"{fmt}/{kind}/{shape}/{direction}")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+@pytest.mark.parametrize("direction", ["row", "col"])
+@pytest.mark.parametrize("seed,stream_id", [(42, 0), (7, 3), (2**40 + 5, 9)])
+def test_stochastic_rounding(mx, fmt, direction, seed, stream_id):
+    x = workloads.draw("student_t3", (416, 544), 5, 1e-3)
+    q, ref = run_both(mx, x, fmt, direction, rounding="sr", seed=seed, stream_id=stream_id)
+    assert_quant_equal(q, ref, f"SR {fmt}/{direction}/{seed}")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_hadamard(mx, fmt, direction):
+    x = workloads.draw("outliers", (416, 544), 6)
+    q, ref = run_both(mx, x, fmt, direction, hadamard=True)
+    assert_quant_equal(q, ref, f"H32 {fmt}/{direction}")
+    if fmt == "mxfp4":
+        q, ref = run_both(mx, x, fmt, direction, hadamard=True, rounding="sr", seed=42)
+        assert_quant_equal(q, ref, f"H32+SR {fmt}/{direction}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "moss"])
+def test_amax_kernel_and_precomputed_amax(mx, fmt):
+    x = workloads.draw("student_t3", (416, 544), 8)
+    xg = x.cuda()
+    a = mx.amax(xg)
+    torch.cuda.synchronize()
+    assert np.float32(a.item()) == np.float32(orc.amax_bf16(bits(x)))
+    # a caller-supplied amax (here twice the true one) replaces the amax pass
+    a2 = a * 2
+    q = mx.quantize(xg, fmt, "col", amax_in=a2)
+    ref = orc.quantize(bits(x), fmt, "col", amax_in=float(a2.item()))
+    torch.cuda.synchronize()
+    assert_quant_equal(q, ref, f"amax_in {fmt}")
+
+
+def test_strided_rows(mx):
+    big = workloads.draw("student_t3", (256, 640), 9)
+    view = big.cuda()[:, :576]
+    for fmt in FMTS:
+        for direction in ("row", "col"):
+            q = mx.quantize(view, fmt, direction)
+            ref = orc.quantize(bits(big[:, :576]), fmt, direction)
+            torch.cuda.synchronize()
+            assert_quant_equal(q, ref, f"strided {fmt}/{direction}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_dequantize(mx, fmt):
+    x = workloads.draw("student_t3", (128, 256), 12)
+    q, ref = run_both(mx, x, fmt)
+    d = mx.dequantize(q).cpu().numpy().astype(np.float64)
+    want = ref.dequantize() * (ref.tensor_scale if ref.tensor_scale is not None else 1.0)
+    assert np.array_equal(d.astype(np.float32), want.astype(np.float32))
+
+
+def test_zero_tensor_and_empty(mx):
+    x = torch.zeros(128, 64, dtype=torch.bfloat16)
+    for fmt in FMTS:
+        q, ref = run_both(mx, x, fmt)
+        assert_quant_equal(q, ref, f"zeros {fmt}")
+        assert (q.codes.cpu() == 0).all()
+    e = mx.quantize(torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"), "nvfp4")
+    torch.cuda.synchronize()
+    assert e.rows == 0 and float(e.scalars[1]) == 1.0
+
+
+def test_argument_errors(mx):
+    x = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mx.MXError) as e:
+        mx.quantize(x, "mxfp8", rounding="sr")
+    assert e.value.code == mx.MX_ERR_UNSUPPORTED
+    with pytest.raises(mx.MXError) as e:
+        mx.quantize(x, "nvfp4", hadamard=True)
+    assert e.value.code == mx.MX_ERR_UNSUPPORTED
+    with pytest.raises(mx.MXError) as e:
+        mx.quantize(torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda"), "mxfp8", "col")
+    assert e.value.code in (mx.MX_ERR_ALIGNMENT, mx.MX_ERR_INVALID_ARG)
+    with pytest.raises(mx.MXError) as e:
+        mx.quantize(torch.zeros(64, 48, dtype=torch.bfloat16, device="cuda"), "mxfp8")
+    assert e.value.code in (mx.MX_ERR_ALIGNMENT, mx.MX_ERR_INVALID_ARG)
+
+
+def test_bounded_wait_gives_up_and_reports(mx):
+    assert mx.last_device_status() == mx.MX_OK
+    rc = mx.selftest_bounded_wait(2_000_000)  # 2 ms
+    assert rc == mx.MX_ERR_TIMEOUT
+    assert mx.last_device_status() == mx.MX_ERR_TIMEOUT  # read and cleared
+    assert mx.last_device_status() == mx.MX_OK
+    # the context is still usable afterwards
+    x = workloads.draw("normal", (64, 64), 1)
+    q, ref = run_both(mx, x, "mxfp8")
+    assert_quant_equal(q, ref, "after timeout")
