@@ -30,7 +30,8 @@ MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_dequantize", "mx_gemm",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_bwd", "mx_strerror",
-            "mx_last_device_status", "mx_selftest_bounded_wait", "mx_debug_set_gemm_tile_n")
+            "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
+            "mx_debug_set_gemm_tile_n")
 
 
 class MXError(RuntimeError):
@@ -96,6 +97,8 @@ def lib():
             L.mx_last_device_status.argtypes = [p]
             L.mx_selftest_bounded_wait.restype = i32
             L.mx_selftest_bounded_wait.argtypes = [u64, p]
+            L.mx_launch_count.restype = u64
+            L.mx_launch_count.argtypes = []
             L.mx_debug_set_gemm_tile_n.restype = None
             L.mx_debug_set_gemm_tile_n.argtypes = [i32]
             _lib = L
@@ -266,6 +269,11 @@ def last_device_status(stream=None) -> int:
 
 def selftest_bounded_wait(limit_ns: int, stream=None) -> int:
     return int(lib().mx_selftest_bounded_wait(int(limit_ns), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched so far in this process."""
+    return int(lib().mx_launch_count())
 
 
 def set_gemm_tile_n(bn: int) -> None:

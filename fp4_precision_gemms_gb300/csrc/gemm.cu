@@ -344,6 +344,7 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.wait_ns = kWaitLimitNs;
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + G::BM - 1) / G::BM));
     bs_gemm_kernel<KIND, BN, STAGES><<<grid, 192, G::SMEM_ALLOC, s>>>(ta, tb, p);
+    count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 

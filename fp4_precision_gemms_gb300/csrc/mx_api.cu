@@ -12,6 +12,8 @@ namespace mx {
 // Per-device status word written by kernels whose bounded waits give up.
 __device__ int g_status_word;
 
+std::atomic<uint64_t> g_kernel_launches{0};
+
 void set_gemm_tile_n(int bn);
 
 int current_device(Device* d)
@@ -410,6 +412,8 @@ int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream)
         return MX_ERR_CUDA;
     return v;
 }
+
+uint64_t mx_launch_count(void) { return g_kernel_launches.load(); }
 
 // Test hook: force the GEMM tile width (128 or 256; 0 = automatic).
 void mx_debug_set_gemm_tile_n(int bn) { set_gemm_tile_n(bn); }

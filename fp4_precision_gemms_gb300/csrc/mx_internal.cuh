@@ -1,5 +1,6 @@
 // mx_internal.cuh -- declarations shared by the library's translation units.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -46,6 +47,10 @@ struct QuantArgs {
     uint8_t* codes;
     uint8_t* sf;
 };
+
+// Number of kernels this library has launched in the process.
+extern std::atomic<uint64_t> g_kernel_launches;
+inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d,
                 cudaStream_t s);

@@ -488,6 +488,7 @@ int launch_q(const QuantArgs& q, const Device& d, cudaStream_t s)
         const int64_t items = q.R * ((cpr + kThreads * 2 - 1) / (kThreads * 2));
         const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(d.sms) * 8));
         quant_row_kernel<FMT, SR, HAD><<<grid, kThreads, 0, s>>>(q);
+        count_launch();
     } else {
         constexpr int SEG = elem_of(FMT) == kElemE2M1 ? 64 : 32;
         const int64_t gx = (q.C + kThreads - 1) / kThreads;
@@ -495,6 +496,7 @@ int launch_q(const QuantArgs& q, const Device& d, cudaStream_t s)
         const int64_t want_y = std::max<int64_t>(1, (static_cast<int64_t>(d.sms) * 8 + gx - 1) / gx);
         const int gy = static_cast<int>(std::min<int64_t>(std::min<int64_t>(nsegs, want_y * 4), 65535));
         quant_col_kernel<FMT, SR, HAD><<<dim3(static_cast<unsigned>(gx), gy), kThreads, 0, s>>>(q);
+        count_launch();
     }
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
@@ -517,6 +519,7 @@ int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, co
         grid.y = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(R, (static_cast<int64_t>(d.sms) * 8 + grid.x - 1) / grid.x)));
     }
     amax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld, reinterpret_cast<unsigned*>(amax));
+    count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
@@ -551,12 +554,14 @@ int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStrea
     const int grid = static_cast<int>(std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(d.sms) * 8));
     dequant_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(A->codes), A->sf, A->tensor_scale, A->rows,
                                              A->k, A->fmt, out);
+    count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
 int launch_wait_selftest(uint64_t limit_ns, const Device& d, cudaStream_t s)
 {
     wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, d.status);
+    count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 

@@ -211,6 +211,10 @@ int mx_last_device_status(void* stream);
  * designed (and the status word then reads MX_ERR_TIMEOUT), MX_OK never. */
 int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream);
 
+/* Number of CUDA kernels this library has launched in the calling process
+ * (memset/memcpy nodes not counted).  Lets a caller count device work. */
+uint64_t mx_launch_count(void);
+
 /* Test hook: force the GEMM's CTA tile width N to 128 or 256 (0 restores the
  * automatic choice).  Affects later mx_gemm / mx_linear_* calls process-wide. */
 void mx_debug_set_gemm_tile_n(int bn);

@@ -1,0 +1,74 @@
+"""The linear layer's forward, data-gradient and weight-gradient passes through the
+C ABI (mx_linear_fwd / mx_linear_bwd) against the oracle's composition of the
+same quantizations and GEMMs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import workloads
+from parity import assert_gemm_close, assert_quant_equal, bits
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import fp4_precision_gemms_gb300 as m
+    m.build()
+    return m
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("tkn", [(256, 512, 384), (384, 1024, 256)])
+def test_forward(mx, fmt, tkn):
+    T, Kin, Nout = tkn
+    X = workloads.draw("student_t3", (T, Kin), 61)
+    W = workloads.draw("normal", (Nout, Kin), 62, 0.02)
+    for out_dtype in (torch.bfloat16, torch.float32):
+        Y = mx.linear_fwd(X.cuda(), W.cuda(), fmt, out_dtype=out_dtype)
+        ref, cabs = orc.gemm(orc.quantize(bits(X), fmt), orc.quantize(bits(W), fmt))
+        assert_gemm_close(Y, ref, cabs, f"fwd {fmt}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_backward(mx, fmt):
+    T, Kin, Nout = 512, 256, 768
+    X = workloads.draw("student_t3", (T, Kin), 71)
+    W = workloads.draw("normal", (Nout, Kin), 72, 0.02)
+    dY = workloads.draw("student_t3", (T, Nout), 73, 1e-3)
+    dX, dW = mx.linear_bwd(dY.cuda(), X.cuda(), W.cuda(), fmt, dx_dtype=torch.float32)
+    ref, cabs = orc.gemm(orc.quantize(bits(dY), fmt), orc.quantize(bits(W), fmt, "col"))
+    assert_gemm_close(dX, ref, cabs, f"dgrad {fmt}")
+    ref, cabs = orc.gemm(orc.quantize(bits(dY), fmt, "col"), orc.quantize(bits(X), fmt, "col"))
+    assert_gemm_close(dW, ref, cabs, f"wgrad {fmt}")
+
+
+@pytest.mark.parametrize("seed,sid", [(42, 0), (1234, 5)])
+def test_mxfp4_wgrad_hadamard_sr(mx, seed, sid):
+    """The mxfp route's weight gradient: H32 on both operands along tokens, SR on dY."""
+    T, Kin, Nout = 512, 256, 384
+    X = workloads.draw("normal", (T, Kin), 81)
+    W = workloads.draw("normal", (Nout, Kin), 82, 0.02)
+    dY = workloads.draw("student_t3", (T, Nout), 83, 1e-3)
+    _, dW = mx.linear_bwd(dY.cuda(), X.cuda(), W.cuda(), "mxfp4", wgrad_hadamard=True,
+                          wgrad_dy_rounding="sr", seed=seed, stream_id=sid, need_dx=False)
+    ra = orc.quantize(bits(dY), "mxfp4", "col", rounding="sr", seed=seed, stream_id=sid, hadamard=True)
+    rb = orc.quantize(bits(X), "mxfp4", "col", hadamard=True)
+    ref, cabs = orc.gemm(ra, rb, extra_alpha=1.0 / 32)
+    assert_gemm_close(dW, ref, cabs, "wgrad mxfp4 H32+SR")
+    # and the result estimates the exact dY^T X
+    exact = (dY.double().t() @ X.double()).numpy()
+    rel = np.linalg.norm(dW.cpu().double().numpy() - exact) / np.linalg.norm(exact)
+    assert rel < 0.25
+
+
+def test_workspace_too_small(mx):
+    X = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mx.MXError) as e:
+        mx.linear_fwd(X, W, "mxfp8", workspace=ws)
+    assert e.value.code == mx.MX_ERR_WORKSPACE
