@@ -29,7 +29,7 @@ MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
 MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_dequantize", "mx_gemm",
-            "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_bwd", "mx_strerror",
+            "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
             "mx_debug_set_gemm_tile_n")
 
@@ -88,6 +88,8 @@ def lib():
             L.mx_linear_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
             L.mx_linear_fwd.restype = i32
             L.mx_linear_fwd.argtypes = [p, p, i64, i64, i64, i32, p, i32, p, sz, p]
+            L.mx_linear_fwd_noalloc.restype = i32
+            L.mx_linear_fwd_noalloc.argtypes = [p, p, i64, i64, i64, i32, p, i32, p]
             L.mx_linear_bwd.restype = i32
             L.mx_linear_bwd.argtypes = [p, p, p, i64, i64, i64, i32, C.POINTER(_CBwdOpts), p, i32, p,
                                         i32, p, sz, p]
@@ -236,6 +238,20 @@ def linear_fwd(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloa
     rc = lib().mx_linear_fwd(_ptr(X), _ptr(W), T, Kin, Nout, FORMATS[fmt], _ptr(Y), OUT[Y.dtype],
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mx_linear_fwd")
+    return Y
+
+
+def linear_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloat16,
+                       out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """linear_fwd without a workspace: the library's fixed device array holds the
+    quantized operands (for callers that cannot allocate; up to 32 MiB)."""
+    _on_gpu(X, W)
+    T, Kin = X.shape
+    Nout = W.shape[0]
+    Y = out if out is not None else torch.empty((T, Nout), dtype=out_dtype, device=X.device)
+    rc = lib().mx_linear_fwd_noalloc(_ptr(X), _ptr(W), T, Kin, Nout, FORMATS[fmt], _ptr(Y),
+                                     OUT[Y.dtype], _stream(stream))
+    _check(rc, "mx_linear_fwd_noalloc")
     return Y
 
 

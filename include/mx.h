@@ -178,6 +178,23 @@ size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, 
 int mx_linear_fwd(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt,
                   void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* mx_linear_fwd for callers that cannot allocate device memory (code running
+ * inside an allocator or memory-pool callback, processes whose device memory
+ * is reserved up front, plugin interfaces that pass only input and output
+ * pointers).  The pages have no counterpart to this entry point.
+ * Same arguments and result as mx_linear_fwd minus the workspace: the
+ * quantized operands go to a fixed 32 MiB array in the library's device
+ * memory (held by every GPU that loads the library until the process exits).
+ * Returns MX_ERR_WORKSPACE, launching nothing, when
+ * mx_linear_workspace_bytes(T, Kin, Nout, fmt, 0) exceeds 32 MiB.
+ * It calls no allocator.  The first call on a device looks up the array's
+ * device address for that device (make that first call before any stream
+ * capture).  All calls share the one array: calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on it and must be ordered by
+ * the caller. */
+int mx_linear_fwd_noalloc(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout,
+                          int fmt, void* Y, int out_dtype, void* stream);
+
 /* Backward options ([FAF] 两个关键的数值技巧: stochastic rounding of the
  * gradient and a fixed-sign Hadamard-32 preconditioning of the weight
  * gradient, both on the mxfp route). */
