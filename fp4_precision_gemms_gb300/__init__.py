@@ -31,7 +31,7 @@ MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_dequantize", "mx_gemm",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
-            "mx_debug_set_gemm_tile_n")
+            "mx_debug_divide", "mx_debug_set_gemm_tile_n")
 
 
 class MXError(RuntimeError):
@@ -101,6 +101,8 @@ def lib():
             L.mx_selftest_bounded_wait.argtypes = [u64, p]
             L.mx_launch_count.restype = u64
             L.mx_launch_count.argtypes = []
+            L.mx_debug_divide.restype = i32
+            L.mx_debug_divide.argtypes = [p, p, i64, p, p, p]
             L.mx_debug_set_gemm_tile_n.restype = None
             L.mx_debug_set_gemm_tile_n.argtypes = [i32]
             _lib = L
@@ -290,6 +292,15 @@ def selftest_bounded_wait(limit_ns: int, stream=None) -> int:
 def launch_count() -> int:
     """Kernels the library has launched so far in this process."""
     return int(lib().mx_launch_count())
+
+
+def debug_divide(v: torch.Tensor, d: torch.Tensor):
+    """(fast, ieee) quotients of the quantizer's shared-divisor division."""
+    _on_gpu(v, d)
+    fast, ieee = torch.empty_like(v), torch.empty_like(v)
+    _check(lib().mx_debug_divide(_ptr(v), _ptr(d), v.numel(), _ptr(fast), _ptr(ieee), _stream()),
+           "mx_debug_divide")
+    return fast, ieee
 
 
 def set_gemm_tile_n(bn: int) -> None:

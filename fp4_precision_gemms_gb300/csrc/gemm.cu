@@ -85,6 +85,7 @@ struct GemmParams {
     int M, N, K;
     int out_bf16;
     int64_t kgroups;  // 4-block SF groups along K (same for A and B)
+    int m_tiles, n_tiles, group_m;  // tile grid and the M-extent of a raster group
     int* status;
     uint64_t wait_ns;
 };
@@ -112,7 +113,20 @@ __global__ void __launch_bounds__(192, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.y, n_tile = blockIdx.x;
+    // Grouped tile order: consecutive CTAs sweep the N tiles of a group of
+    // group_m M tiles, so a wave of resident CTAs shares a few A row tiles and
+    // B column tiles in L2 instead of streaming all of B once per M tile.
+    int m_tile, n_tile;
+    {
+        const int tile = blockIdx.x;
+        const int per_group = p.group_m * p.n_tiles;
+        const int g = tile / per_group;
+        const int first_m = g * p.group_m;
+        const int gm = min(p.group_m, p.m_tiles - first_m);
+        const int r = tile - g * per_group;
+        m_tile = first_m + r % gm;
+        n_tile = r / gm;
+    }
     const int num_kt = p.K / G::BK;
 
     if (threadIdx.x == 0) {
@@ -342,7 +356,12 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.status = d.status;
     p.wait_ns = kWaitLimitNs;
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + G::BM - 1) / G::BM));
+    p.m_tiles = static_cast<int>((M + G::BM - 1) / G::BM);
+    p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+    // A group keeps about 16 MiB of A row tiles resident in L2.
+    const int64_t a_tile_bytes = static_cast<int64_t>(G::BM) * kbytes;
+    p.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+    const dim3 grid(static_cast<unsigned>(p.m_tiles) * static_cast<unsigned>(p.n_tiles));
     bs_gemm_kernel<KIND, BN, STAGES><<<grid, 192, G::SMEM_ALLOC, s>>>(ta, tb, p);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;

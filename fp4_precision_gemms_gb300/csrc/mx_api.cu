@@ -415,6 +415,17 @@ int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream)
 
 uint64_t mx_launch_count(void) { return g_kernel_launches.load(); }
 
+int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, float* q_ieee, void* stream)
+{
+    if (n < 0 || (n > 0 && (!v || !d || !q_fast || !q_ieee)))
+        return MX_ERR_INVALID_ARG;
+    Device dev;
+    const int rc = current_device(&dev);
+    if (rc != MX_OK)
+        return rc;
+    return launch_divide_check(v, d, n, q_fast, q_ieee, dev, static_cast<cudaStream_t>(stream));
+}
+
 // Test hook: force the GEMM tile width (128 or 256; 0 = automatic).
 void mx_debug_set_gemm_tile_n(int bn) { set_gemm_tile_n(bn); }
 

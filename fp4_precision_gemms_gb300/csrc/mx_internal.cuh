@@ -59,5 +59,7 @@ int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStrea
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
                 int out_dtype, const Device& d, cudaStream_t s);
 int launch_wait_selftest(uint64_t limit_ns, const Device& d, cudaStream_t s);
+int launch_divide_check(const float* v, const float* dv, int64_t n, float* fast, float* ieee, const Device& d,
+                        cudaStream_t s);
 
 }  // namespace mx

@@ -8,8 +8,9 @@
 //                      threads of a scale block combine their maxima with warp
 //                      shuffles; codes leave as one coalesced 8- or 4-byte store.
 //   quant_col_kernel   bf16 [R, C] -> transposed operand [C, R] (quantized along
-//                      R): each thread owns one input column and 32 bytes of
-//                      output codes, so the transpose costs no shared memory.
+//                      R): a CTA stages SEG x 256 of the input in shared memory
+//                      with 16-byte loads, then each thread encodes one column's
+//                      SEG values into 32 bytes of output codes.
 // Both write the block scales straight into the tensor core's scale-factor
 // layout ("格式感知融合:让FP4预训练提速两倍的工程实践", section
 // 格式感知融合的设计思路: the producer writes the consumer's layout), and both
@@ -17,7 +18,7 @@
 // rounding (same page, section 两个关键的数值技巧).
 //
 // Bit-exactness: every step is an exactly specified fp32 operation (products
-// and quotients with __fmul_rn/__fdiv_rn, adds in a fixed butterfly order) or
+// with __fmul_rn, correctly rounded quotients, adds in a fixed butterfly order) or
 // an integer decision, so the codes and scale bytes are a pure function of the
 // input, independent of launch shape.
 #include <algorithm>
@@ -199,6 +200,33 @@ __device__ __forceinline__ void fwht_lanes(float (&v)[8], int mask, bool upper)
     }
 }
 
+// Quotient v / d, rounded to nearest as an IEEE division would, for a
+// divisor d that many elements share.  From the correctly rounded reciprocal
+// r = RN(1/d) (one __frcp_rn per block), q0 = RN(v r) is within 1.5 ulp of v/d;
+// one residual correction q1 = RN(q0 + (v - q0 d) r) (the residual is exact
+// with one FMA) brings it within 1 ulp, and a second one rounds correctly by
+// Markstein's theorem (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  The
+// theorem assumes no underflow or overflow, so the fast path is taken only
+// when the divisor (r == 0 marks one outside [2^-100, 2^100]), the quotient
+// and the numerator are all at least 2^-100 in magnitude, which keeps both
+// residuals exactly representable; everything else takes the IEEE division.
+__device__ __forceinline__ float recip_for_div(float d)
+{
+    return (d >= 0x1p-100f && d <= 0x1p100f) ? __frcp_rn(d) : 0.0f;
+}
+
+__device__ __forceinline__ float div_shared(float v, float d, float r)
+{
+    const float q0 = __fmul_rn(v, r);
+    const float a = fabsf(q0);
+    if (a >= 0x1p-100f && a <= 0x1p100f && fabsf(v) >= 0x1p-100f) {
+        const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, v), r, q0);
+        return __fmaf_rn(__fmaf_rn(-q1, d, v), r, q1);
+    }
+    return (v == 0.0f && r != 0.0f) ? q0 : __fdiv_rn(v, d);
+}
+
 __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
 {
     if (fmt == MX_FMT_MOSS_FP8 || fmt == MX_FMT_NVFP4) {
@@ -225,12 +253,14 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, floa
         const uint32_t sb = cvt_e4m3x2(__fdiv_rn(bmax, nv_denom), 0.0f) & 0x7Fu;
         const float d = __fmul_rn(dec_e4m3_pos(sb), ts);
         sfbyte = sb;
-        if (d == 0.0f)
+        if (d == 0.0f) {
             zero = true;
-        else
+        } else {
+            const float rd = recip_for_div(d);
 #pragma unroll
             for (int i = 0; i < N; ++i)
-                v[i] = __fdiv_rn(v[i], d);
+                v[i] = div_shared(v[i], d, rd);
+        }
     } else {
         const int e = pow2_exponent<ELEM>(bmax, rule);
         const float s2 = exp2_neg(e);
@@ -320,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
 {
     constexpr int BLOCK = fmt_block(FMT);
     constexpr int LPB = BLOCK / 8;  // lanes per scale block
-    constexpr int U = 2;
+    constexpr int U = 4;
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     const int lane = threadIdx.x & 31;
     const int64_t C = a.C, cpr = C / 8;
@@ -328,6 +358,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
     const int64_t items_per_row = (cpr + kThreads * U - 1) / (kThreads * U);
     const int64_t items = a.R * items_per_row;
     const float ts = tensor_scale_of(FMT, a.amax);
+    const float rts = recip_for_div(ts);
     const float nv_denom = __fmul_rn(6.0f, ts);
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
@@ -359,7 +390,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
             if constexpr (FMT == MX_FMT_MOSS_FP8) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    v[i] = __fdiv_rn(v[i], ts);
+                    v[i] = div_shared(v[i], ts, rts);
             }
             float bmax = 0.0f;
 #pragma unroll
@@ -383,59 +414,86 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
     }
 }
 
-// Colwise producer: operand row c (= input column c), K = R.  A thread owns
-// one column and SEG consecutive input rows (32 bytes of output codes).
+// Colwise producer: operand row c (= input column c), K = R.  A CTA stages a
+// tile of SEG input rows x 256 input columns in shared memory with coalesced
+// 16-byte loads; then each thread encodes one column's SEG values (32 bytes of
+// output codes) and writes them as two 16-byte stores.
 template <int FMT, bool SR, bool HAD>
 __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
 {
     constexpr int BLOCK = fmt_block(FMT);
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
-    constexpr int SEG = FP4 ? 64 : 32;
-    const int64_t c = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    constexpr int SEG = FP4 ? 64 : 32;   // K elements per thread
+    constexpr int TC = kThreads;         // input columns per tile
+    constexpr int CPR = TC / 8;          // 16-byte chunks per tile row
+    __shared__ __align__(16) uint16_t tile[SEG][TC];
     const int64_t R = a.R, C = a.C;
     const float ts = tensor_scale_of(FMT, a.amax);
+    const float rts = recip_for_div(ts);
     const float nv_denom = __fmul_rn(6.0f, ts);
-    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
-    if (c >= C)
-        return;
     const int64_t kgroups = sf_kgroups(R / BLOCK);
-    const int64_t nsegs = (R + SEG - 1) / SEG;
     const int64_t row_bytes = FP4 ? R / 2 : R;
-    for (int64_t seg = blockIdx.y; seg < nsegs; seg += gridDim.y) {
-        const int64_t k0 = seg * SEG;
+    const int64_t ctiles = (C + TC - 1) / TC, ktiles = (R + SEG - 1) / SEG;
+    for (int64_t t = blockIdx.x; t < ctiles * ktiles; t += gridDim.x) {
+        const int64_t kt = t / ctiles, ct = t - kt * ctiles;
+        const int64_t k0 = kt * SEG, c0 = ct * TC;
         const int nk = static_cast<int>(R - k0 < SEG ? R - k0 : SEG);  // multiple of 32
-        const uint16_t* xc = a.x + k0 * a.ld + c;
-        uint32_t out[8];
 #pragma unroll
-        for (int b = 0; b < SEG / BLOCK; ++b) {
-            float blk[BLOCK];
-            const bool in = b * BLOCK < nk;  // whole blocks only: nk is a multiple of 32
+        for (int j = 0; j < SEG * CPR / kThreads; ++j) {
+            const int i = j * kThreads + threadIdx.x;
+            const int r = i / CPR, cc = (i % CPR) * 8;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            const int64_t col = c0 + cc;
+            if (r < nk && col < C) {
+                const uint16_t* src = a.x + (k0 + r) * a.ld + col;
+                if (col + 8 <= C) {
+                    w = __ldg(reinterpret_cast<const uint4*>(src));
+                } else {
+                    uint16_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                    for (int e = 0; e < 8 && col + e < C; ++e)
+                        h[e] = src[e];
+                    w = make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                                   h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
+                }
+            }
+            *reinterpret_cast<uint4*>(&tile[r][cc]) = w;
+        }
+        __syncthreads();
+        const int64_t c = c0 + threadIdx.x;
+        if (c < C) {
+            uint32_t out[8];
 #pragma unroll
-            for (int i = 0; i < BLOCK; ++i)
-                blk[i] = in ? __uint_as_float(static_cast<uint32_t>(__ldg(xc + (b * BLOCK + i) * a.ld)) << 16) : 0.0f;
-            if constexpr (HAD)
-                fwht_local<BLOCK>(blk);
-            if constexpr (FMT == MX_FMT_MOSS_FP8) {
+            for (int b = 0; b < SEG / BLOCK; ++b) {
+                float blk[BLOCK];
 #pragma unroll
                 for (int i = 0; i < BLOCK; ++i)
-                    blk[i] = __fdiv_rn(blk[i], ts);
-            }
-            float bmax = 0.0f;
+                    blk[i] = __uint_as_float(static_cast<uint32_t>(tile[b * BLOCK + i][threadIdx.x]) << 16);
+                if constexpr (HAD)
+                    fwht_local<BLOCK>(blk);
+                if constexpr (FMT == MX_FMT_MOSS_FP8) {
 #pragma unroll
-            for (int i = 0; i < BLOCK; ++i)
-                bmax = fmaxf(bmax, fabsf(blk[i]));
-            constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
-            const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
-            const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, ts, nv_denom, a.rule, a.seed,
-                                                              a.stream_id, L8, out + b * WPB);
-            if (b * BLOCK < nk)
-                a.sf[sf_offset(c, (k0 + b * BLOCK) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
+                    for (int i = 0; i < BLOCK; ++i)
+                        blk[i] = div_shared(blk[i], ts, rts);
+                }
+                float bmax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < BLOCK; ++i)
+                    bmax = fmaxf(bmax, fabsf(blk[i]));
+                constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
+                const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
+                const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, ts, nv_denom, a.rule, a.seed,
+                                                                  a.stream_id, L8, out + b * WPB);
+                if (b * BLOCK < nk)
+                    a.sf[sf_offset(c, (k0 + b * BLOCK) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
+            }
+            uint8_t* dst = a.codes + c * row_bytes + (FP4 ? k0 / 2 : k0);
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            if (nk == SEG)
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
         }
-        uint8_t* dst = a.codes + c * row_bytes + (FP4 ? k0 / 2 : k0);
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        if (nk == SEG)
-            reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        __syncthreads();
     }
 }
 
@@ -467,6 +525,18 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __rest
     }
 }
 
+__global__ void __launch_bounds__(kThreads) divide_check_kernel(const float* __restrict__ v, const float* __restrict__ d,
+                                                                int64_t n, float* __restrict__ fast,
+                                                                float* __restrict__ ieee)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float dv = d[i];
+        fast[i] = div_shared(v[i], dv, recip_for_div(dv));
+        ieee[i] = __fdiv_rn(v[i], dv);
+    }
+}
+
 __global__ void wait_selftest_kernel(uint64_t limit_ns, int* status)
 {
     __shared__ __align__(8) uint64_t bar;
@@ -485,17 +555,15 @@ int launch_q(const QuantArgs& q, const Device& d, cudaStream_t s)
 {
     if (q.dir == MX_ROWWISE) {
         const int64_t cpr = q.C / 8;
-        const int64_t items = q.R * ((cpr + kThreads * 2 - 1) / (kThreads * 2));
+        const int64_t items = q.R * ((cpr + kThreads * 4 - 1) / (kThreads * 4));
         const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(d.sms) * 8));
         quant_row_kernel<FMT, SR, HAD><<<grid, kThreads, 0, s>>>(q);
         count_launch();
     } else {
         constexpr int SEG = elem_of(FMT) == kElemE2M1 ? 64 : 32;
-        const int64_t gx = (q.C + kThreads - 1) / kThreads;
-        const int64_t nsegs = (q.R + SEG - 1) / SEG;
-        const int64_t want_y = std::max<int64_t>(1, (static_cast<int64_t>(d.sms) * 8 + gx - 1) / gx);
-        const int gy = static_cast<int>(std::min<int64_t>(std::min<int64_t>(nsegs, want_y * 4), 65535));
-        quant_col_kernel<FMT, SR, HAD><<<dim3(static_cast<unsigned>(gx), gy), kThreads, 0, s>>>(q);
+        const int64_t tiles = ((q.C + kThreads - 1) / kThreads) * ((q.R + SEG - 1) / SEG);
+        const int grid = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(d.sms) * 8));
+        quant_col_kernel<FMT, SR, HAD><<<grid, kThreads, 0, s>>>(q);
         count_launch();
     }
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
@@ -554,6 +622,17 @@ int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStrea
     const int grid = static_cast<int>(std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(d.sms) * 8));
     dequant_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(A->codes), A->sf, A->tensor_scale, A->rows,
                                              A->k, A->fmt, out);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_divide_check(const float* v, const float* dv, int64_t n, float* fast, float* ieee, const Device& d,
+                        cudaStream_t s)
+{
+    if (n == 0)
+        return MX_OK;
+    const int grid = static_cast<int>(std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(d.sms) * 8));
+    divide_check_kernel<<<grid, kThreads, 0, s>>>(v, dv, n, fast, ieee);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }

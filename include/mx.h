@@ -232,6 +232,11 @@ int mx_selftest_bounded_wait(uint64_t limit_ns, void* stream);
  * (memset/memcpy nodes not counted).  Lets a caller count device work. */
 uint64_t mx_launch_count(void);
 
+/* Test hook: the quantizer's division by a shared divisor (q_fast, computed
+ * from the divisor's correctly rounded reciprocal plus residual corrections)
+ * next to CUDA's IEEE division (q_ieee), for n device pairs v[i] / d[i]. */
+int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, float* q_ieee, void* stream);
+
 /* Test hook: force the GEMM's CTA tile width N to 128 or 256 (0 restores the
  * automatic choice).  Affects later mx_gemm / mx_linear_* calls process-wide. */
 void mx_debug_set_gemm_tile_n(int bn);
