@@ -411,6 +411,7 @@ def run_case(args):
     gemm:<fmt>:MxNxK  or  quant:<fmt>:<row|col>:RxC  (bf16 Student-t inputs)."""
     import fp4_precision_gemms_gb300 as mx
     mx.build()
+    mx.set_gemm_variant(args.gemm_variant)
     parts = args.case.split(":")
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
@@ -463,9 +464,10 @@ def main():
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=512)
+    ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=256)
     ap.add_argument("--case", default=None, help="time one kernel: gemm:fmt:MxNxK or quant:fmt:dir:RxC")
+    ap.add_argument("--gemm-variant", default="auto", help="force a GEMM kernel variant (tuning aid)")
     args = ap.parse_args()
     if args.case:
         run_case(args)

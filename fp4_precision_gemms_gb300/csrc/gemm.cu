@@ -367,6 +367,404 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair kernel.  A cluster of two CTAs computes 256 x 256 output tiles with
+// tcgen05.mma.cta_group::2: each CTA stages 128 rows of A and 128 rows of B
+// (its half of the tile's N) per K-stage, so per SM the operand and
+// scale-factor traffic per flop is two thirds of the single-CTA 128 x 256 tile.
+// The kernel is persistent: cluster c walks tiles c, c + clusters, ... in the
+// grouped order.  Roles per CTA:
+//   warp 0        TMA producer (both CTAs): code and scale tiles, completing on
+//                 the rank-0 CTA's stage barrier (two arrivals per stage).
+//   warp 1        TMEM allocation (both CTAs, jointly); in rank 0 one thread
+//                 issues the scale copies and MMAs for the pair and frees
+//                 stages and the accumulator with multicast commits.
+//   warps 2-9     epilogue (both CTAs): pull this CTA's 128 x 256 accumulator
+//                 rows from TMEM into registers, release the accumulator to the
+//                 next tile's MMAs, then scale and store.
+// Scale factors live in one TMEM slot per pipeline stage.
+template <int KIND, int STAGES_>
+struct CfgPair {
+    static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
+    static constexpr int BN = 256;  // pair tile N; each CTA stages BN / 2 rows of B
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BKB = 128;
+    static constexpr int EPB = KIND == 0 ? 1 : 2;
+    static constexpr int BK = BKB * EPB;
+    static constexpr int BLOCK = KIND == 2 ? 16 : 32;
+    static constexpr int MMA_K_BYTES = 32;
+    static constexpr int MMAS = BKB / MMA_K_BYTES;
+    static constexpr int BPM = MMA_K_BYTES * EPB / BLOCK;
+    static constexpr int NCHUNK = MMAS * BPM / 4;
+    // The pair MMA reads B's scales for all 256 rows of the tile from each
+    // CTA's TMEM, so each CTA stages both 128-row scale tiles of B.
+    static constexpr int SFB_RT = 2;
+    static constexpr int A_BYTES = BM * BKB;
+    static constexpr int B_BYTES = (BN / 2) * BKB;
+    static constexpr int SFA_BYTES = NCHUNK * 512;
+    static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int SMEM_BYTES = OFF_BAR + (2 * STAGES + 3) * 8 + 16;
+    static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+    static constexpr int SFT = STAGES;  // one scale slot per pipeline stage
+    static constexpr int SFA_COLS = 4 * NCHUNK;
+    static constexpr int SFB_COLS = 8 * NCHUNK;
+    static constexpr int TM_SFA = BN;
+    static constexpr int TM_SFB = TM_SFA + SFT * SFA_COLS;
+    static constexpr int TM_USED = TM_SFB + SFT * SFB_COLS;
+    static constexpr int TM_ALLOC = 512;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;
+    static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
+    static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // per CTA per stage
+    static_assert(TM_USED <= TM_ALLOC, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
+struct PairParams {
+    const float* tsa;
+    const float* tsb;
+    float extra;
+    void* c;
+    int64_t ldc;
+    int M, N, K;
+    int out_bf16;
+    int64_t kgroups;
+    int m_tiles, n_tiles, group_m;  // 256 x 256 tiles
+    int* status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void grouped_tile(int tile, int m_tiles, int n_tiles, int group_m, int& mt, int& nt)
+{
+    const int per_group = group_m * n_tiles;
+    const int g = tile / per_group;
+    const int first_m = g * group_m;
+    const int gm = min(group_m, m_tiles - first_m);
+    const int r = tile - g * per_group;
+    mt = first_m + r % gm;
+    nt = r / gm;
+}
+
+template <int KIND, int STAGES>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
+    bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                        const PairParams p)
+{
+    using G = CfgPair<KIND, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t bar0 = s0 + G::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t accf = bar0 + 8u * (2 * STAGES);
+    const uint32_t acce = accf + 8u;
+    const uint32_t tdone = acce + 8u;  // this CTA's epilogue warps have read the accumulator
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_BAR + 8 * (2 * STAGES + 3));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_ctarank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int num_kt = p.K / G::BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 2);   // one arrive.expect_tx from each CTA's producer
+            mbar_init(empty(s), 1);  // rank 0's multicast commit
+        }
+        mbar_init(accf, 1);
+        mbar_init(acce, 2);  // one arrival from each CTA's epilogue
+        mbar_init(tdone, G::EPI_WARPS);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmSFA);
+        prefetch_tmap(&tmSFB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), G::TM_ALLOC);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // barrier initialisation and the joint TMEM allocation seen by both CTAs
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t full0_r0 = mapa_shared(full(0), 0);
+            int it = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
+                int mt, nt;
+                grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                const int arow = mt * 256 + static_cast<int>(rank) * 128;
+                const int brow = nt * 256 + static_cast<int>(rank) * 128;
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
+                    if (it >= STAGES && !mbar_wait_bounded(empty(s), (round - 1) & 1u, p.wait_ns)) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = full0_r0 + 8u * s;
+                    mbar_arrive_expect_tx_cluster(fb, G::TX);
+                    tma_load_2d_pair(s0 + G::OFF_A + s * G::A_BYTES, &tmA, fb, kt * G::BKB, arow);
+                    tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES, &tmB, fb, kt * G::BKB, brow);
+                    tma_load_2d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0,
+                                     static_cast<int>(((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK) * 4));
+#pragma unroll
+                    for (int r = 0; r < G::SFB_RT; ++r) {
+                        const int rt = nt * 2 + r;
+                        tma_load_2d_pair(s0 + G::OFF_SFB + s * G::SFB_BYTES + r * G::NCHUNK * 512, &tmSFB, fb, 0,
+                                         static_cast<int>((rt * p.kgroups + kt * G::NCHUNK) * 4));
+                    }
+                }
+            }
+            if (stop) {  // give copies already issued time to land before the CTA can exit
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int it = 0, titer = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters, ++titer) {
+                if (titer > 0 && !mbar_wait_bounded(acce, static_cast<uint32_t>(titer - 1) & 1u, p.wait_ns)) {
+                    atomicExch(p.status, MX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
+                    // A full stage implies both producers saw this stage's previous MMAs
+                    // complete, so the stage's scale slot is free to overwrite.
+                    const bool ok = mbar_wait_bounded(full(s), round & 1u, p.wait_ns);
+                    const int slot = s;
+                    if (!ok) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + G::TM_SFA + slot * G::SFA_COLS;
+                    const uint32_t sfb_t = tmem + G::TM_SFB + slot * G::SFB_COLS;
+#pragma unroll
+                    for (int c = 0; c < G::NCHUNK; ++c)
+                        tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(s0 + G::OFF_SFA + s * G::SFA_BYTES + c * 512));
+#pragma unroll
+                    for (int r = 0; r < G::SFB_RT; ++r)
+#pragma unroll
+                        for (int c = 0; c < G::NCHUNK; ++c)
+                            tc_cp_sf_pair(sfb_t + 8 * c + 4 * r,
+                                          sdesc_sf(s0 + G::OFF_SFB + s * G::SFB_BYTES + (r * G::NCHUNK + c) * 512));
+                    const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES);
+                    const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES);
+#pragma unroll
+                    for (int i = 0; i < G::MMAS; ++i) {
+                        const int fb = i * G::BPM;
+                        const int chunk = fb / 4;
+                        const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
+                        const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, 256, G::BN, sf_id, sf_id);
+                        const uint64_t koff = static_cast<uint64_t>((i * G::MMA_K_BYTES) >> 4);
+                        mma_bs_pair<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk, sfb_t + 8 * chunk,
+                                          (kt > 0 || i > 0) ? 1u : 0u);
+                    }
+                    tc_commit_pair(empty(s), 0x3);
+                }
+                tc_commit_pair(accf, 0x3);  // this tile's accumulator is complete in both CTAs
+            }
+        }
+        __syncwarp();
+    } else {
+        const int ew = warp - 2;        // 0 .. 7
+        const int q = warp & 3;         // TMEM lane quarter this warp may read
+        const int half = ew >> 2;       // accumulator columns half*128 .. +127
+        const uint32_t acce_r0 = mapa_shared(acce, 0);
+        const float ta = p.tsa ? *p.tsa : 1.0f, tb = p.tsb ? *p.tsb : 1.0f;
+        const float alpha = __fmul_rn(__fmul_rn(ta, tb), p.extra);
+        int titer = 0;
+        for (int tile = cluster_id; tile < tiles; tile += nclusters, ++titer) {
+            int mt, nt;
+            grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+            if (!mbar_wait_bounded(accf, static_cast<uint32_t>(titer) & 1u, p.wait_ns)) {
+                atomicExch(p.status, MX_ERR_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 128 + j * 32, r[j]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tdone);
+            if (ew == 0 && lane == 0) {
+                // once all eight warps have their columns, the accumulator is free
+                if (mbar_wait_bounded(tdone, static_cast<uint32_t>(titer) & 1u, p.wait_ns))
+                    mbar_arrive_cluster(acce_r0);
+                else
+                    atomicExch(p.status, MX_ERR_TIMEOUT);
+            }
+            const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+            if (row < p.M) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col0 = nt * 256 + half * 128 + j * 32;
+                    if (col0 >= p.N)
+                        break;
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), alpha);
+                    const bool full_chunk = col0 + 32 <= p.N;
+                    if (p.out_bf16) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
+                        if (full_chunk) {
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * w + 2 * h], v[8 * w + 2 * h + 1]);
+                                    pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    dst[i] = __float2bfloat16_rn(v[i]);
+                        }
+                    } else {
+                        float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
+                        if (full_chunk) {
+#pragma unroll
+                            for (int w = 0; w < 8; ++w)
+                                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < p.N)
+                                    dst[i] = v[i];
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // remote arrivals and the peer's TMEM reads are finished
+    if (warp == 1) {
+        if (*abort_flag && lane == 0 && rank == 0)
+            (void)mbar_wait_bounded(accf, 0, kWaitLimitNs);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, G::TM_ALLOC);
+    }
+}
+
+// 2-D map over a scale-factor buffer viewed as rows of 128 bytes; one box is
+// `chunks` consecutive 512-byte chunks.  Boxes past the end read zeros.
+bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(bytes / 128)};
+    const cuuint64_t strides[1] = {128u};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(4 * chunks)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int STAGES>
+int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
+                const Device& d, cudaStream_t s)
+{
+    using G = CfgPair<KIND, STAGES>;
+    auto kernel = bs_gemm_pair_kernel<KIND, STAGES>;
+    static int configured_device = -1;
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(G::THREADS);
+    cfg.dynamicSmemBytes = G::SMEM_ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (configured_device != d.id) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_ALLOC) != cudaSuccess)
+            return MX_ERR_CUDA;
+        cfg.gridDim = dim3(2 * (d.sms / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1)
+            return MX_ERR_CUDA;
+        max_clusters = n;
+        configured_device = d.id;
+    }
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    const int64_t kbytes = K / G::EPB;
+    CUtensorMap ta, tb, tsa, tsb;
+    const int64_t sfa_bytes = sf_layout_bytes(M, K / G::BLOCK), sfb_bytes = sf_layout_bytes(N, K / G::BLOCK);
+    if (!make_code_map(&ta, A->codes, M, kbytes, 128) || !make_code_map(&tb, B->codes, N, kbytes, 128) ||
+        !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
+        return MX_ERR_CUDA;
+    PairParams p;
+    p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
+    p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
+    p.extra = extra;
+    p.c = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.out_bf16 = out_dtype == MX_OUT_BF16;
+    p.kgroups = sf_kgroups(K / G::BLOCK);
+    p.m_tiles = static_cast<int>((M + 255) / 256);
+    p.n_tiles = static_cast<int>((N + 255) / 256);
+    const int64_t a_tile_bytes = 256 * kbytes;
+    p.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+    p.status = d.status;
+    p.wait_ns = kWaitLimitNs;
+    const int tiles = p.m_tiles * p.n_tiles;
+    cfg.gridDim = dim3(2 * std::min(tiles, max_clusters));
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, p) != cudaSuccess)
+        return MX_ERR_CUDA;
+    count_launch();
+    return MX_OK;
+}
+
 template <int KIND>
 int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
                 const Device& d, cudaStream_t s, int bn)
@@ -378,28 +776,43 @@ int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 
 }  // namespace
 
-// Tile width override for tests (0 = automatic).
-static int g_force_bn = 0;
+// Kernel override for tests: 0 = automatic, 1 = single CTA with N = 128,
+// 2 = single CTA with N = 256, 3 = CTA pair (256 x 256 tiles).
+static int g_variant = 0;
 
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
                 const Device& d, cudaStream_t s)
 {
     if (A->rows == 0 || B->rows == 0)
         return MX_OK;
-    const int bn = g_force_bn ? g_force_bn : (B->rows > 128 ? 256 : 128);
-    switch (A->fmt) {
-    case MX_FMT_MXFP8_E4M3:
-    case MX_FMT_MOSS_FP8:
-        return launch_kind<0>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
-    case MX_FMT_MXFP4_E2M1:
-        return launch_kind<1>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
-    case MX_FMT_NVFP4:
-        return launch_kind<2>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
-    default:
+    int v = g_variant;
+    if (v == 0) {
+        // CTA pairs once there are enough 256 x 256 tiles to fill the GPU;
+        // single-CTA tiles for small problems, where more, smaller tiles win.
+        const int64_t pair_tiles = ((A->rows + 255) / 256) * ((B->rows + 255) / 256);
+        v = pair_tiles >= d.sms / 2 ? 3 : (B->rows > 128 ? 2 : 1);
+    }
+    const int kind = (A->fmt == MX_FMT_MXFP8_E4M3 || A->fmt == MX_FMT_MOSS_FP8) ? 0
+                   : A->fmt == MX_FMT_MXFP4_E2M1                                ? 1
+                   : A->fmt == MX_FMT_NVFP4                                     ? 2
+                                                                                : -1;
+    if (kind < 0)
         return MX_ERR_INVALID_ARG;
+    if (v == 3) {
+        switch (kind) {
+        case 0: return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
+        case 1: return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
+        default: return launch_pair<2, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
+        }
+    }
+    const int bn = v == 1 ? 128 : 256;
+    switch (kind) {
+    case 0: return launch_kind<0>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    case 1: return launch_kind<1>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    default: return launch_kind<2>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
     }
 }
 
-void set_gemm_tile_n(int bn) { g_force_bn = (bn == 128 || bn == 256) ? bn : 0; }
+void set_gemm_variant(int v) { g_variant = (v >= 0 && v <= 3) ? v : 0; }
 
 }  // namespace mx

@@ -14,7 +14,7 @@ __device__ int g_status_word;
 
 std::atomic<uint64_t> g_kernel_launches{0};
 
-void set_gemm_tile_n(int bn);
+void set_gemm_variant(int v);
 
 int current_device(Device* d)
 {
@@ -426,7 +426,7 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
     return launch_divide_check(v, d, n, q_fast, q_ieee, dev, static_cast<cudaStream_t>(stream));
 }
 
-// Test hook: force the GEMM tile width (128 or 256; 0 = automatic).
-void mx_debug_set_gemm_tile_n(int bn) { set_gemm_tile_n(bn); }
+// Test hook: force one GEMM kernel variant (0 = automatic).
+void mx_debug_set_gemm_variant(int variant) { set_gemm_variant(variant); }
 
 }  // extern "C"

@@ -237,9 +237,10 @@ uint64_t mx_launch_count(void);
  * next to CUDA's IEEE division (q_ieee), for n device pairs v[i] / d[i]. */
 int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, float* q_ieee, void* stream);
 
-/* Test hook: force the GEMM's CTA tile width N to 128 or 256 (0 restores the
- * automatic choice).  Affects later mx_gemm / mx_linear_* calls process-wide. */
-void mx_debug_set_gemm_tile_n(int bn);
+/* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
+ * calls, process-wide: 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA
+ * 128 x 256 tiles, 3 CTA-pair (cluster of two) 256 x 256 tiles. */
+void mx_debug_set_gemm_variant(int variant);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,7 @@ def mx():
     import fp4_precision_gemms_gb300 as m
     m.build()
     yield m
-    m.set_gemm_tile_n(0)
+    m.set_gemm_variant("auto")
 
 
 def quant_pair(mx, a, b, fmt, **kw):
@@ -28,11 +28,11 @@ def quant_pair(mx, a, b, fmt, **kw):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
-@pytest.mark.parametrize("bn", [128, 256])
-def test_exact_small_integers(mx, fmt, bn):
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+def test_exact_small_integers(mx, fmt, variant):
     """Small-integer codes with power-of-two scales: every partial sum is exact in
     fp32, so the tensor core must reproduce the fp64 oracle bit for bit."""
-    mx.set_gemm_tile_n(bn)
+    mx.set_gemm_variant(variant)
     rng = np.random.default_rng(1)
     vals = np.array([-6, -4, -3, -2, -1, 0, 1, 2, 3, 4, 6])
     a = torch.tensor(rng.choice(vals, (256, 512)), dtype=torch.float32).to(torch.bfloat16)
@@ -45,13 +45,13 @@ def test_exact_small_integers(mx, fmt, bn):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("bn", [128, 256])
-def test_scale_factor_layout_one_hot(mx, fmt, bn):
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+def test_scale_factor_layout_one_hot(mx, fmt, variant):
     """Pins the swizzled scale layout against the hardware: with all-ones inputs,
     raise single scale bytes of A and of B in the GPU buffers (at the offsets the
     layout definition gives) and check every output against the oracle GEMM
     computed with the same raised logical scales."""
-    mx.set_gemm_tile_n(bn)
+    mx.set_gemm_variant(variant)
     M, N, K = 256, 384, 1024 if fmt in ("mxfp4", "nvfp4") else 512
     a = torch.ones(M, K, dtype=torch.bfloat16)
     b = torch.ones(N, K, dtype=torch.bfloat16)
@@ -82,15 +82,16 @@ def test_random_gemm(mx, fmt, mnk, out_dtype):
     a = workloads.draw("student_t3", (M, K), 40 + M)
     b = workloads.draw("normal", (N, K), 41 + N, 0.02)
     qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
-    for bn in (128, 256):
-        mx.set_gemm_tile_n(bn)
+    for variant in ("cta_n128", "cta_n256", "pair"):
+        mx.set_gemm_variant(variant)
         c = mx.gemm(qa, qb, out_dtype=out_dtype)
         ref, cabs = orc.gemm(ra, rb)
-        assert_gemm_close(c, ref, cabs, f"{fmt} {mnk} bn={bn}")
+        assert_gemm_close(c, ref, cabs, f"{fmt} {mnk} {variant}")
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
 def test_hadamard_alpha(mx, fmt):
+    mx.set_gemm_variant("auto")
     """Both operands transformed: the epilogue applies the 1/32 of (Ha)^T(Hb) = 32 a^T b."""
     dy = workloads.draw("student_t3", (512, 256), 51, 1e-3)
     x = workloads.draw("normal", (512, 384), 52)
@@ -119,3 +120,20 @@ def test_gemm_k_alignment_rejected(mx):
         mx.gemm(q, q)
     assert e.value.code == mx.MX_ERR_ALIGNMENT
     assert mx.last_device_status() == mx.MX_OK
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_pair_kernel_many_tiles_and_tails(mx, fmt):
+    """Enough 256 x 256 tiles that every cluster runs several (persistent
+    loop, accumulator hand-off between tiles), with ragged M and N tails."""
+    mx.set_gemm_variant("pair")
+    M, N, K = 1280 + 72, 1536 + 40, 512
+    a = workloads.draw("student_t3", (M, K), 77)
+    b = workloads.draw("normal", (N, K), 78, 0.02)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    rows = np.r_[0:40, M - 80:M]
+    for out_dtype in (torch.float32, torch.bfloat16):
+        c = mx.gemm(qa, qb, out_dtype=out_dtype)
+        ref, cabs = orc.gemm(ra, rb, rows=rows)
+        assert_gemm_close(c[torch.as_tensor(rows, device=c.device)], ref, cabs, f"pair {fmt}")
+    mx.set_gemm_variant("auto")
