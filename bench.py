@@ -140,6 +140,12 @@ def quant_bytes(fmt: str, elems: int, amax_pass: bool) -> float:
     return elems * (2.0 + (2.0 if amax_pass else 0.0) + CODE_BYTES[fmt] + 1.0 / BLOCK[fmt])
 
 
+def dual_bytes(fmt: str, elems: int, amax_pass: bool) -> float:
+    """Algorithmic HBM bytes of one dual-direction producer call: one bf16 read
+    (+ the amax pass's read) and two sets of codes and scale bytes."""
+    return elems * (2.0 + (2.0 if amax_pass else 0.0) + 2.0 * (CODE_BYTES[fmt] + 1.0 / BLOCK[fmt]))
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_precision_gemms_gb300", "csrc")
@@ -187,24 +193,23 @@ class Plan:
         self.has_ts = fmt in ("nvfp4", "moss")
 
     def calls(self, inputs):
-        """The step as a list of (kind, fn, flops_or_bytes) in issue order."""
+        """The step as a list of (kind, fn, flops_or_bytes) in issue order.  Each of
+        X, W and dY is read once by the dual-direction producer, which emits the
+        rowwise operand and the transposed operand the other pass needs."""
         mx, fmt, out = self.mx, self.fmt, []
         for e in self.gemms:
             g = e["g"]
             X, W, dY = inputs[g.x.name], inputs[g.w.name], inputs[g.dy.name]
             T, Kin, Nout = e["T"], e["Kin"], e["Nout"]
             ts = self.has_ts
-            out.append(("quant", lambda X=X, e=e: mx.quantize(X, fmt, "row", out=e["xq"]), quant_bytes(fmt, T * Kin, ts)))
-            out.append(("quant", lambda W=W, e=e: mx.quantize(W, fmt, "row", out=e["wq"]), quant_bytes(fmt, Nout * Kin, ts)))
+            out.append(("quant", lambda X=X, e=e: mx.quantize_dual(X, fmt, row_out=e["xq"], col_out=e["xtq"]),
+                        dual_bytes(fmt, T * Kin, ts)))
+            out.append(("quant", lambda W=W, e=e: mx.quantize_dual(W, fmt, row_out=e["wq"], col_out=e["wtq"]),
+                        dual_bytes(fmt, Nout * Kin, ts)))
             out.append(("gemm", lambda e=e: mx.gemm(e["xq"], e["wq"], out=e["Y"]), 2.0 * T * Kin * Nout))
-            out.append(("quant", lambda dY=dY, e=e: mx.quantize(dY, fmt, "row", out=e["dyq"]), quant_bytes(fmt, T * Nout, ts)))
-            out.append(("quant", lambda W=W, e=e: mx.quantize(W, fmt, "col", out=e["wtq"], amax_in=e["wq"].amax if ts else None),
-                        quant_bytes(fmt, Nout * Kin, False)))
+            out.append(("quant", lambda dY=dY, e=e: mx.quantize_dual(dY, fmt, row_out=e["dyq"], col_out=e["dytq"]),
+                        dual_bytes(fmt, T * Nout, ts)))
             out.append(("gemm", lambda e=e: mx.gemm(e["dyq"], e["wtq"], out=e["dX"]), 2.0 * T * Kin * Nout))
-            out.append(("quant", lambda dY=dY, e=e: mx.quantize(dY, fmt, "col", out=e["dytq"], amax_in=e["dyq"].amax if ts else None),
-                        quant_bytes(fmt, T * Nout, False)))
-            out.append(("quant", lambda X=X, e=e: mx.quantize(X, fmt, "col", out=e["xtq"], amax_in=e["xq"].amax if ts else None),
-                        quant_bytes(fmt, T * Kin, False)))
             out.append(("gemm", lambda e=e: mx.gemm(e["dytq"], e["xtq"], out=e["dW"]), 2.0 * T * Kin * Nout))
         return out
 
@@ -412,6 +417,7 @@ def run_case(args):
     import fp4_precision_gemms_gb300 as mx
     mx.build()
     mx.set_gemm_variant(args.gemm_variant)
+    mx.set_quant_impl(args.quant_impl)
     parts = args.case.split(":")
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
@@ -430,8 +436,16 @@ def run_case(args):
         x = workloads.draw("student_t3", (R, Cc), 1, device=dev)
         rows, k = (R, Cc) if direction == "row" else (Cc, R)
         q = mx.MXTensor(fmt, rows, k, dev)
-        fn = lambda: mx.quantize(x, fmt, direction, out=q)  # noqa: E731
-        work, unit = quant_bytes(fmt, R * Cc, fmt in ("nvfp4", "moss")), "GB/s"
+        amax_in = mx.amax(x) if fmt in ("nvfp4", "moss") else None  # time the producer pass alone
+        if direction == "dual":
+            qc = mx.MXTensor(fmt, Cc, R, dev)
+            q = mx.MXTensor(fmt, R, Cc, dev)
+            fn = lambda: mx.quantize_dual(x, fmt, row_out=q, col_out=qc, amax_in=amax_in)  # noqa: E731
+            work = dual_bytes(fmt, R * Cc, False)
+        else:
+            fn = lambda: mx.quantize(x, fmt, direction, out=q, amax_in=amax_in)  # noqa: E731
+            work = quant_bytes(fmt, R * Cc, False)
+        unit = "GB/s"
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
@@ -468,6 +482,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=256)
     ap.add_argument("--case", default=None, help="time one kernel: gemm:fmt:MxNxK or quant:fmt:dir:RxC")
     ap.add_argument("--gemm-variant", default="auto", help="force a GEMM kernel variant (tuning aid)")
+    ap.add_argument("--quant-impl", default="auto", help="force a producer implementation (tuning aid)")
     args = ap.parse_args()
     if args.case:
         run_case(args)

@@ -28,10 +28,10 @@ OUT = {torch.float32: 0, torch.bfloat16: 1}
 MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
 MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
-EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_dequantize", "mx_gemm",
+EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
-            "mx_debug_divide", "mx_debug_set_gemm_variant")
+            "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_gemm_variant")
 
 
 class MXError(RuntimeError):
@@ -80,6 +80,11 @@ def lib():
             L.mx_quantize.restype = i32
             L.mx_quantize.argtypes = [p, i64, i64, i64, i32, i32, i32, i32, i32, u64, u32, i32, p,
                                       C.POINTER(_CTensor), p]
+            L.mx_quantize_dual.restype = i32
+            L.mx_quantize_dual.argtypes = [p, i64, i64, i64, i32, i32, i32, u64, u32, i32, i32, i32, i32, p,
+                                           C.POINTER(_CTensor), C.POINTER(_CTensor), p]
+            L.mx_debug_set_quant_impl.restype = None
+            L.mx_debug_set_quant_impl.argtypes = [i32]
             L.mx_dequantize.restype = i32
             L.mx_dequantize.argtypes = [C.POINTER(_CTensor), p, p]
             L.mx_gemm.restype = i32
@@ -202,6 +207,35 @@ def quantize(x: torch.Tensor, fmt: str, direction: str = "row", rounding: str = 
     _check(rc, "mx_quantize")
     q.rows, q.k, q.hadamard = ct.rows, ct.k, bool(ct.hadamard)
     return q
+
+
+def quantize_dual(x: torch.Tensor, fmt: str, rule: str = "default", seed: int = 0, stream_id: int = 0,
+                  row_rounding: str = "rne", row_hadamard: bool = False, col_rounding: str = "rne",
+                  col_hadamard: bool = False, amax_in: torch.Tensor | None = None,
+                  row_out: MXTensor | None = None, col_out: MXTensor | None = None, stream=None):
+    """One read of bf16 x [R, C] -> (rowwise operand [R, C], colwise operand [C, R])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    _on_gpu(x, amax_in)
+    R, Cc = x.shape
+    qr = row_out if row_out is not None else MXTensor(fmt, R, Cc, x.device)
+    qc = col_out if col_out is not None else MXTensor(fmt, Cc, R, x.device)
+    cr, cc = qr._c(), qc._c()
+    rc = lib().mx_quantize_dual(_ptr(x), R, Cc, x.stride(0), FORMATS[fmt], BLOCK[fmt], RULES[rule], seed,
+                                stream_id, ROUNDING[row_rounding], int(bool(row_hadamard)),
+                                ROUNDING[col_rounding], int(bool(col_hadamard)), _ptr(amax_in),
+                                C.byref(cr), C.byref(cc), _stream(stream))
+    _check(rc, "mx_quantize_dual")
+    qr.rows, qr.k, qr.hadamard = cr.rows, cr.k, bool(cr.hadamard)
+    qc.rows, qc.k, qc.hadamard = cc.rows, cc.k, bool(cc.hadamard)
+    return qr, qc
+
+
+QUANT_IMPLS = {"auto": 0, "direct": 1, "tile": 2}
+
+
+def set_quant_impl(impl: str) -> None:
+    """Choose the producer implementation (tests and tuning)."""
+    lib().mx_debug_set_quant_impl(QUANT_IMPLS[impl])
 
 
 def dequantize(q: MXTensor, stream=None) -> torch.Tensor:

@@ -102,58 +102,133 @@ size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
     return off;
 }
 
-int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fmt, int block, int rounding,
-                  int rule, uint64_t seed, uint32_t stream_id, int hadamard, const float* amax_in, mx_tensor* out,
-                  const Device& d, cudaStream_t s)
+// Producer implementation for tests and tuning: 0 automatic (direct loads
+// rowwise, tile producer colwise), 1 direct loads, 2 tile producer.
+int g_quant_impl = 0;
+
+// Shared argument checks of the single and dual producers.
+int check_quantize_args(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int rule)
 {
-    if (!out || !valid_fmt(fmt) || (dir != MX_ROWWISE && dir != MX_COLWISE) || R < 0 || C < 0 || ld < C)
-        return MX_ERR_INVALID_ARG;
-    if (rounding != MX_ROUND_RNE && rounding != MX_ROUND_SR)
+    if (!valid_fmt(fmt) || R < 0 || C < 0 || ld < C)
         return MX_ERR_INVALID_ARG;
     if (rule < MX_SCALE_DEFAULT || rule > MX_SCALE_NEAREST)
         return MX_ERR_INVALID_ARG;
     if (block != fmt_block(fmt))
         return MX_ERR_UNSUPPORTED;
+    if (fmt == MX_FMT_NVFP4 && rule != MX_SCALE_DEFAULT)
+        return MX_ERR_UNSUPPORTED;
+    if (ld % 8 != 0 || !aligned16(x))
+        return MX_ERR_ALIGNMENT;
+    if (R > 0 && C > 0 && !x)
+        return MX_ERR_INVALID_ARG;
+    return MX_OK;
+}
+
+int check_direction(int fmt, int rounding, int hadamard)
+{
+    if (rounding != MX_ROUND_RNE && rounding != MX_ROUND_SR)
+        return MX_ERR_INVALID_ARG;
     if (rounding == MX_ROUND_SR && !fmt_is_fp4(fmt))
         return MX_ERR_UNSUPPORTED;
     if (hadamard && !(fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MXFP4_E2M1))
         return MX_ERR_UNSUPPORTED;
-    if (fmt == MX_FMT_NVFP4 && rule != MX_SCALE_DEFAULT)
-        return MX_ERR_UNSUPPORTED;
+    return MX_OK;
+}
+
+int check_output(const mx_tensor* out, int fmt, int64_t R, int64_t C)
+{
+    if (!out)
+        return MX_ERR_INVALID_ARG;
+    if (!aligned16(out->codes))
+        return MX_ERR_ALIGNMENT;
+    if (R > 0 && C > 0 && (!out->codes || !out->sf))
+        return MX_ERR_INVALID_ARG;
+    if (fmt_has_tensor_scale(fmt) && (!out->amax || !out->tensor_scale))
+        return MX_ERR_INVALID_ARG;
+    return MX_OK;
+}
+
+void fill_meta(mx_tensor* out, int64_t rows, int64_t k, int fmt, int hadamard)
+{
+    out->rows = rows;
+    out->k = k;
+    out->fmt = fmt;
+    out->block = fmt_block(fmt);
+    out->hadamard = hadamard ? 1 : 0;
+}
+
+// Makes out->amax hold max|x| (copied from amax_in or reduced from x).
+int prepare_amax(const void* x, int64_t R, int64_t C, int64_t ld, const float* amax_in, mx_tensor* out,
+                 const Device& d, cudaStream_t s)
+{
+    if (amax_in) {
+        if (amax_in != out->amax &&
+            cudaMemcpyAsync(out->amax, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+        return MX_OK;
+    }
+    return launch_amax(x, R, C, ld, out->amax, d, s);
+}
+
+int set_unit_scale(mx_tensor* out, cudaStream_t s)
+{
+    static const float one = 1.0f;  // the tensor scale of an empty tensor
+    return cudaMemcpyAsync(out->tensor_scale, &one, sizeof one, cudaMemcpyHostToDevice, s) == cudaSuccess ? MX_OK
+                                                                                                        : MX_ERR_CUDA;
+}
+
+int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fmt, int block, int rounding,
+                  int rule, uint64_t seed, uint32_t stream_id, int hadamard, const float* amax_in, mx_tensor* out,
+                  const Device& d, cudaStream_t s)
+{
+    if (dir != MX_ROWWISE && dir != MX_COLWISE)
+        return MX_ERR_INVALID_ARG;
+    int rc = check_quantize_args(x, R, C, ld, fmt, block, rule);
+    if (rc == MX_OK)
+        rc = check_direction(fmt, rounding, hadamard);
+    if (rc == MX_OK)
+        rc = check_output(out, fmt, R, C);
+    if (rc != MX_OK)
+        return rc;
     const int64_t rows = dir == MX_ROWWISE ? R : C;
     const int64_t k = dir == MX_ROWWISE ? C : R;
     if (k % block != 0 || (dir == MX_COLWISE && R % 32 != 0))
         return MX_ERR_ALIGNMENT;
-    if (ld % 8 != 0 || !aligned16(x) || !aligned16(out->codes))
-        return MX_ERR_ALIGNMENT;
-    if (R > 0 && C > 0 && (!x || !out->codes || !out->sf))
-        return MX_ERR_INVALID_ARG;
-    const bool ts = fmt_has_tensor_scale(fmt);
-    if (ts && (!out->amax || !out->tensor_scale))
-        return MX_ERR_INVALID_ARG;
     if (rule == MX_SCALE_DEFAULT)
         rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
-    out->rows = rows;
-    out->k = k;
-    out->fmt = fmt;
-    out->block = block;
-    out->hadamard = hadamard ? 1 : 0;
-    if (ts) {
-        if (amax_in) {
-            if (amax_in != out->amax &&
-                cudaMemcpyAsync(out->amax, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-                return MX_ERR_CUDA;
+    fill_meta(out, rows, k, fmt, hadamard);
+    const bool ts = fmt_has_tensor_scale(fmt);
+    if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, out, d, s)) != MX_OK)
+        return rc;
+    if (R == 0 || C == 0)
+        return ts ? set_unit_scale(out, s) : MX_OK;
+    const bool tile = g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE);
+    if (tile) {
+        TileArgs t = {};
+        t.x = x;
+        t.R = R;
+        t.C = C;
+        t.fmt = fmt;
+        t.rule = rule;
+        t.seed = seed;
+        t.stream_id = stream_id;
+        t.amax = out->amax;
+        t.tensor_scale = out->tensor_scale;
+        uint8_t* codes = static_cast<uint8_t*>(out->codes);
+        if (dir == MX_ROWWISE) {
+            t.row_codes = codes;
+            t.row_sf = out->sf;
+            t.row_sr = rounding == MX_ROUND_SR;
+            t.row_had = hadamard ? 1 : 0;
         } else {
-            const int rc = launch_amax(x, R, C, ld, out->amax, d, s);
-            if (rc != MX_OK)
-                return rc;
+            t.col_codes = codes;
+            t.col_sf = out->sf;
+            t.col_sr = rounding == MX_ROUND_SR;
+            t.col_had = hadamard ? 1 : 0;
         }
-    }
-    if (R == 0 || C == 0) {  // nothing to encode; the tensor scale of an all-zero tensor is 1
-        static const float one = 1.0f;
-        if (ts && cudaMemcpyAsync(out->tensor_scale, &one, sizeof one, cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return MX_ERR_CUDA;
-        return MX_OK;
+        t.status = d.status;
+        t.wait_ns = kWaitLimitNs;
+        return launch_quantize_tile(t, ld, d, s);
     }
     QuantArgs q;
     q.x = static_cast<const uint16_t*>(x);
@@ -172,6 +247,67 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
     q.codes = static_cast<uint8_t*>(out->codes);
     q.sf = out->sf;
     return launch_quantize(q, d, s);
+}
+
+int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int rule,
+                       uint64_t seed, uint32_t stream_id, int row_rounding, int row_hadamard, int col_rounding,
+                       int col_hadamard, const float* amax_in, mx_tensor* row_out, mx_tensor* col_out,
+                       const Device& d, cudaStream_t s)
+{
+    int rc = check_quantize_args(x, R, C, ld, fmt, block, rule);
+    if (rc == MX_OK)
+        rc = check_direction(fmt, row_rounding, row_hadamard);
+    if (rc == MX_OK)
+        rc = check_direction(fmt, col_rounding, col_hadamard);
+    if (rc == MX_OK)
+        rc = check_output(row_out, fmt, R, C);
+    if (rc == MX_OK)
+        rc = check_output(col_out, fmt, R, C);
+    if (rc != MX_OK)
+        return rc;
+    if (C % block != 0 || R % 32 != 0)
+        return MX_ERR_ALIGNMENT;
+    if (rule == MX_SCALE_DEFAULT)
+        rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
+    fill_meta(row_out, R, C, fmt, row_hadamard);
+    fill_meta(col_out, C, R, fmt, col_hadamard);
+    const bool ts = fmt_has_tensor_scale(fmt);
+    if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, row_out, d, s)) != MX_OK)
+        return rc;
+    if (R == 0 || C == 0) {
+        if (!ts)
+            return MX_OK;
+        if ((rc = set_unit_scale(row_out, s)) != MX_OK)
+            return rc;
+        if (cudaMemcpyAsync(col_out->amax, row_out->amax, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return MX_ERR_CUDA;
+        return set_unit_scale(col_out, s);
+    }
+    TileArgs t = {};
+    t.x = x;
+    t.R = R;
+    t.C = C;
+    t.fmt = fmt;
+    t.rule = rule;
+    t.seed = seed;
+    t.stream_id = stream_id;
+    t.amax = row_out->amax;
+    t.tensor_scale = row_out->tensor_scale;
+    if (ts) {
+        t.amax_copy = col_out->amax;
+        t.tensor_scale_copy = col_out->tensor_scale;
+    }
+    t.row_codes = static_cast<uint8_t*>(row_out->codes);
+    t.row_sf = row_out->sf;
+    t.row_sr = row_rounding == MX_ROUND_SR;
+    t.row_had = row_hadamard ? 1 : 0;
+    t.col_codes = static_cast<uint8_t*>(col_out->codes);
+    t.col_sf = col_out->sf;
+    t.col_sr = col_rounding == MX_ROUND_SR;
+    t.col_had = col_hadamard ? 1 : 0;
+    t.status = d.status;
+    t.wait_ns = kWaitLimitNs;
+    return launch_quantize_tile(t, ld, d, s);
 }
 
 int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
@@ -244,6 +380,19 @@ int mx_quantize(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fm
         return rc;
     return quantize_impl(x, R, C, ld, dir, fmt, block, rounding, scale_rule, seed, stream_id, hadamard, amax_in, out,
                          d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_quantize_dual(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int scale_rule,
+                     uint64_t seed, uint32_t stream_id, int row_rounding, int row_hadamard, int col_rounding,
+                     int col_hadamard, const float* amax_in, mx_tensor* row_out, mx_tensor* col_out, void* stream)
+{
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return quantize_dual_impl(x, R, C, ld, fmt, block, scale_rule, seed, stream_id, row_rounding, row_hadamard,
+                              col_rounding, col_hadamard, amax_in, row_out, col_out, d,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int mx_dequantize(const mx_tensor* A, float* out, void* stream)
@@ -333,12 +482,20 @@ int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64
     off += carve(ws + off, fmt, Nout, T, &dyt);
     carve(ws + off, fmt, Kin, T, &xt);
     const int block = fmt_block(fmt);
-    const bool ts = fmt_has_tensor_scale(fmt);
-    if (dX) {
-        rc = quantize_impl(dY, T, Nout, Nout, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
-                           nullptr, &dyr, d, s);
+    if (dX && dW) {
+        // one pass over dY emits both its dgrad (rowwise) and wgrad (colwise) operands
+        rc = quantize_dual_impl(dY, T, Nout, Nout, fmt, block, MX_SCALE_DEFAULT, o.seed, o.stream_id, MX_ROUND_RNE, 0,
+                                o.wgrad_dy_rounding, o.wgrad_hadamard, nullptr, &dyr, &dyt, d, s);
         if (rc != MX_OK)
             return rc;
+    }
+    if (dX) {
+        if (!dW) {
+            rc = quantize_impl(dY, T, Nout, Nout, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
+                               nullptr, &dyr, d, s);
+            if (rc != MX_OK)
+                return rc;
+        }
         rc = quantize_impl(W, Nout, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
                            nullptr, &wt, d, s);
         if (rc != MX_OK)
@@ -348,12 +505,12 @@ int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64
             return rc;
     }
     if (dW) {
-        // dY's tensor amax is shared by its rowwise and colwise quantizations.
-        const float* dy_amax = (dX && ts) ? dyr.amax : nullptr;
-        rc = quantize_impl(dY, T, Nout, Nout, MX_COLWISE, fmt, block, o.wgrad_dy_rounding, MX_SCALE_DEFAULT, o.seed,
-                           o.stream_id, o.wgrad_hadamard, dy_amax, &dyt, d, s);
-        if (rc != MX_OK)
-            return rc;
+        if (!dX) {
+            rc = quantize_impl(dY, T, Nout, Nout, MX_COLWISE, fmt, block, o.wgrad_dy_rounding, MX_SCALE_DEFAULT,
+                               o.seed, o.stream_id, o.wgrad_hadamard, nullptr, &dyt, d, s);
+            if (rc != MX_OK)
+                return rc;
+        }
         rc = quantize_impl(X, T, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0,
                            o.wgrad_hadamard, nullptr, &xt, d, s);
         if (rc != MX_OK)
@@ -425,6 +582,9 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
         return rc;
     return launch_divide_check(v, d, n, q_fast, q_ieee, dev, static_cast<cudaStream_t>(stream));
 }
+
+// Test hook: producer implementation (0 automatic, 1 direct loads, 2 tile producer).
+void mx_debug_set_quant_impl(int impl) { g_quant_impl = (impl >= 0 && impl <= 2) ? impl : 0; }
 
 // Test hook: force one GEMM kernel variant (0 = automatic).
 void mx_debug_set_gemm_variant(int variant) { set_gemm_variant(variant); }

@@ -48,6 +48,28 @@ struct QuantArgs {
     uint8_t* sf;
 };
 
+// One producer pass over x emitting the rowwise operand, the colwise operand or
+// both (a null codes pointer skips that direction).
+struct TileArgs {
+    const void* x;
+    int64_t R, C;
+    int fmt, rule;
+    uint64_t seed;
+    uint32_t stream_id;
+    const float* amax;
+    float* tensor_scale;
+    float* amax_copy;          // optional second amax / tensor-scale destination
+    float* tensor_scale_copy;  // (the colwise operand of a dual pass)
+    uint8_t* row_codes;
+    uint8_t* row_sf;
+    int row_sr, row_had;
+    uint8_t* col_codes;
+    uint8_t* col_sf;
+    int col_sr, col_had;
+    int* status;
+    uint64_t wait_ns;
+};
+
 // Number of kernels this library has launched in the process.
 extern std::atomic<uint64_t> g_kernel_launches;
 inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -55,6 +77,7 @@ inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_re
 int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d,
                 cudaStream_t s);
 int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s);
+int launch_quantize_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s);
 int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStream_t s);
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
                 int out_dtype, const Device& d, cudaStream_t s);

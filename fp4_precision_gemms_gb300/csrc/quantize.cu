@@ -11,6 +11,8 @@
 //                      R): a CTA stages SEG x 256 of the input in shared memory
 //                      with 16-byte loads, then each thread encodes one column's
 //                      SEG values into 32 bytes of output codes.
+//   quant_tile_kernel  TMA-pipelined 64 x 256 tiles; rowwise, colwise or both
+//                      operands from one read of x (the dual-direction pass).
 // Both write the block scales straight into the tensor core's scale-factor
 // layout ("格式感知融合:让FP4预训练提速两倍的工程实践", section
 // 格式感知融合的设计思路: the producer writes the consumer's layout), and both
@@ -23,6 +25,7 @@
 // input, independent of launch shape.
 #include <algorithm>
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "mx_internal.cuh"
@@ -216,6 +219,10 @@ __device__ __forceinline__ float recip_for_div(float d)
     return (d >= 0x1p-100f && d <= 0x1p100f) ? __frcp_rn(d) : 0.0f;
 }
 
+// The rare IEEE fallback of div_shared, out of line so that the many inlined
+// copies of the fast path stay small.
+__device__ __noinline__ float div_ieee(float v, float d) { return __fdiv_rn(v, d); }
+
 __device__ __forceinline__ float div_shared(float v, float d, float r)
 {
     const float q0 = __fmul_rn(v, r);
@@ -224,7 +231,7 @@ __device__ __forceinline__ float div_shared(float v, float d, float r)
         const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, v), r, q0);
         return __fmaf_rn(__fmaf_rn(-q1, d, v), r, q1);
     }
-    return (v == 0.0f && r != 0.0f) ? q0 : __fdiv_rn(v, d);
+    return (v == 0.0f && r != 0.0f) ? q0 : div_ieee(v, d);
 }
 
 __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
@@ -237,29 +244,82 @@ __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
 }
 
 // ---------------------------------------------------------- block encoding
+// Tensor-level constants of one producer pass.  For NVFP4 a block's divisor
+// d = fl32(dec(s_b) * s_t) takes one of 128 values (one per UE4M3 scale byte
+// s_b), so each CTA tabulates d and its correctly rounded reciprocal once.
+struct ScaleCtx {
+    float ts;              // tensor scale (1 for the MX formats)
+    float rts;             // recip_for_div(ts) (MOSS)
+    float nv_denom;        // fl32(6 * ts) (NVFP4)
+    float rden;            // recip_for_div(nv_denom)
+    const float2* nv_tab;  // [128] {d, recip_for_div(d)} per scale byte (NVFP4)
+};
+
+// Every thread calls this; the caller synchronises before the table is read.
+template <int FMT>
+__device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* tab_smem)
+{
+    ScaleCtx c;
+    c.ts = tensor_scale_of(FMT, amax);
+    c.rts = recip_for_div(c.ts);
+    c.nv_denom = __fmul_rn(6.0f, c.ts);
+    c.rden = recip_for_div(c.nv_denom);
+    c.nv_tab = tab_smem;
+    if constexpr (FMT == MX_FMT_NVFP4) {
+        for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
+            const float d = __fmul_rn(dec_e4m3_pos(static_cast<uint32_t>(sb)), c.ts);
+            tab_smem[sb] = make_float2(d, recip_for_div(d));
+        }
+    }
+    return c;
+}
+
 // Encodes one scale block held as N consecutive values in registers (the
 // block's max |v| is `bmax`).  Produces the scale byte and N codes packed
 // little-endian into `out` (E4M3: N bytes; E2M1: N/2 bytes).  `L8` is the
 // Philox counter of the first 8 elements (used only for SR).
 template <int FMT, bool SR, int N>
-__device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, float ts, float nv_denom,
-                                                 int rule, uint64_t seed, uint32_t sid, uint64_t L8,
-                                                 uint32_t* out)
+__device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, const ScaleCtx& sc, int rule,
+                                                 uint64_t seed, uint32_t sid, uint64_t L8, uint32_t* out)
 {
     constexpr int ELEM = elem_of(FMT);
     uint32_t sfbyte;
     bool zero = false;
     if constexpr (FMT == MX_FMT_NVFP4) {
-        const uint32_t sb = cvt_e4m3x2(__fdiv_rn(bmax, nv_denom), 0.0f) & 0x7Fu;
-        const float d = __fmul_rn(dec_e4m3_pos(sb), ts);
+        const uint32_t sb = cvt_e4m3x2(div_shared(bmax, sc.nv_denom, sc.rden), 0.0f) & 0x7Fu;
+        const float2 drd = sc.nv_tab[sb];  // {fl32(dec(sb) * ts), its reciprocal}
         sfbyte = sb;
-        if (d == 0.0f) {
+        if (drd.x == 0.0f) {
             zero = true;
         } else {
-            const float rd = recip_for_div(d);
+            if constexpr (!SR) {
+                if (drd.y != 0.0f) {
+                    // RNE needs only the E2M1 code of fl32(v / d), a monotone step
+                    // function of the quotient.  q0 = fl32(v * RN(1/d)) lies within
+                    // 2 ulp of fl32(v / d), so the codes of q0 (1 -+ 2^-20) bracket
+                    // the exact code; when they agree they are the exact code.
+                    constexpr float lo_f = 1.0f - 0x1p-20f, hi_f = 1.0f + 0x1p-20f;
+                    uint32_t agree = 1u;
+#pragma unroll
+                    for (int w = 0; w < N / 8; ++w) {
+                        uint32_t wlo = 0, whi = 0;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float qa = __fmul_rn(v[8 * w + 2 * i], drd.y);
+                            const float qb = __fmul_rn(v[8 * w + 2 * i + 1], drd.y);
+                            wlo |= cvt_e2m1x2(__fmul_rn(qa, lo_f), __fmul_rn(qb, lo_f)) << (8 * i);
+                            whi |= cvt_e2m1x2(__fmul_rn(qa, hi_f), __fmul_rn(qb, hi_f)) << (8 * i);
+                        }
+                        out[w] = wlo;
+                        agree &= (wlo == whi) ? 1u : 0u;
+                    }
+                    if (agree)
+                        return sfbyte;
+                }
+            }
 #pragma unroll
             for (int i = 0; i < N; ++i)
-                v[i] = div_shared(v[i], d, rd);
+                v[i] = div_shared(v[i], drd.x, drd.y);
         }
     } else {
         const int e = pow2_exponent<ELEM>(bmax, rule);
@@ -357,11 +417,12 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
     const int64_t kgroups = sf_kgroups(C / BLOCK);
     const int64_t items_per_row = (cpr + kThreads * U - 1) / (kThreads * U);
     const int64_t items = a.R * items_per_row;
-    const float ts = tensor_scale_of(FMT, a.amax);
-    const float rts = recip_for_div(ts);
-    const float nv_denom = __fmul_rn(6.0f, ts);
+    __shared__ float2 nv_tab[128];
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
+    const float ts = sc.ts, rts = sc.rts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
+    __syncthreads();
 
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
         const int64_t r = item / items_per_row;
@@ -401,7 +462,7 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
                 bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, m));
             if (c8 < cpr) {
                 uint32_t out[2];
-                const uint32_t sfb = encode_block<FMT, SR, 8>(v, bmax, ts, nv_denom, a.rule, a.seed,
+                const uint32_t sfb = encode_block<FMT, SR, 8>(v, bmax, sc, a.rule, a.seed,
                                                               a.stream_id, r * cpr + c8, out);
                 if constexpr (FP4)
                     *reinterpret_cast<uint32_t*>(a.codes + r * (C / 2) + c8 * 4) = out[0];
@@ -427,10 +488,10 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
     constexpr int TC = kThreads;         // input columns per tile
     constexpr int CPR = TC / 8;          // 16-byte chunks per tile row
     __shared__ __align__(16) uint16_t tile[SEG][TC];
+    __shared__ float2 nv_tab[128];
     const int64_t R = a.R, C = a.C;
-    const float ts = tensor_scale_of(FMT, a.amax);
-    const float rts = recip_for_div(ts);
-    const float nv_denom = __fmul_rn(6.0f, ts);
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
+    const float ts = sc.ts, rts = sc.rts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
     const int64_t kgroups = sf_kgroups(R / BLOCK);
@@ -483,7 +544,7 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
                     bmax = fmaxf(bmax, fabsf(blk[i]));
                 constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
                 const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
-                const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, ts, nv_denom, a.rule, a.seed,
+                const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, sc, a.rule, a.seed,
                                                                   a.stream_id, L8, out + b * WPB);
                 if (b * BLOCK < nk)
                     a.sf[sf_offset(c, (k0 + b * BLOCK) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
@@ -494,6 +555,180 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
                 reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
         }
         __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------ tile producer
+// Persistent producer over 64 x 256 tiles of x staged in shared memory by TMA
+// through a three-stage mbarrier pipeline.  From each staged tile it can emit
+// the rowwise operand (blocks along the 256 columns: each warp encodes whole
+// rows, 8 elements per lane, block maxima combined with shuffles), the colwise
+// operand (blocks along the 64 rows: each thread encodes one column into 32
+// bytes of codes), or both: one read of x then serves the forward operand and
+// the transposed operand a backward pass needs ("格式感知融合:让FP4预训练提速两倍的
+// 工程实践", section FP4加速为何常常"纸上富贵": operand packing, layout
+// construction and saving backward state are the costs around the GEMM).
+// Rounding is a compile-time choice per direction and the Hadamard transform
+// is compiled only for the MX formats, so a kernel holds only the code it runs.
+constexpr int kTR = 64, kTC = 256, kTStages = 3;
+constexpr int kTileBytes = kTR * kTC * 2;
+
+template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
+__global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileArgs a)
+{
+    constexpr int BLOCK = fmt_block(FMT);
+    constexpr int LPB = BLOCK / 8;
+    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
+    constexpr bool HAD_OK = FMT == MX_FMT_MXFP8_E4M3 || FMT == MX_FMT_MXFP4_E2M1;
+    constexpr int SEG = FP4 ? 64 : 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const uint32_t sbase = smem_u32(base);
+    const uint32_t bar0 = sbase + kTStages * kTileBytes;
+    __shared__ float2 nv_tab[128];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t R = a.R, C = a.C;
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
+    const float ts = sc.ts, rts = sc.rts;
+    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && tid == 0) {
+        *a.tensor_scale = ts;
+        if (a.tensor_scale_copy) {
+            *a.tensor_scale_copy = ts;
+            *a.amax_copy = *a.amax;
+        }
+    }
+    const bool row_had = HAD_OK && a.row_had, col_had = HAD_OK && a.col_had;
+    const int64_t ctiles = (C + kTC - 1) / kTC, tiles = ((R + kTR - 1) / kTR) * ctiles;
+    const int64_t my_n = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t kg_row = sf_kgroups(C / BLOCK), kg_col = sf_kgroups(R / BLOCK);
+    const int64_t col_row_bytes = FP4 ? R / 2 : R;
+
+    auto issue = [&](int64_t i) {
+        const int st = static_cast<int>(i % kTStages);
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        const int64_t rt = t / ctiles, ct = t - rt * ctiles;
+        mbar_arrive_expect_tx(bar0 + 8u * st, kTileBytes);
+        tma_load_2d(sbase + st * kTileBytes, &tmx, bar0 + 8u * st, static_cast<int32_t>(ct * kTC),
+                    static_cast<int32_t>(rt * kTR));
+    };
+    if (tid == 0) {
+        for (int st = 0; st < kTStages; ++st)
+            mbar_init(bar0 + 8u * st, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmx);
+        for (int64_t i = 0; i < my_n && i < kTStages; ++i)
+            issue(i);
+    }
+    __syncthreads();
+    int64_t i = 0;
+    for (; i < my_n; ++i) {
+        const int st = static_cast<int>(i % kTStages);
+        const bool ok = mbar_wait_bounded(bar0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns);
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0)
+                atomicExch(a.status, MX_ERR_TIMEOUT);
+            break;
+        }
+        const uint16_t* tile = reinterpret_cast<const uint16_t*>(base + st * kTileBytes);  // [kTR][kTC]
+        const int64_t t = blockIdx.x + i * gridDim.x;
+        const int64_t rt = t / ctiles, ct = t - rt * ctiles;
+        const int64_t r0 = rt * kTR, c0 = ct * kTC;
+        if constexpr (DO_ROW) {
+            // warp w encodes tile rows w, w + 8, ...; lane l owns columns 8l .. 8l + 7
+            const int64_t col = c0 + lane * 8;
+            for (int rr = warp; rr < kTR; rr += kThreads / 32) {
+                const int64_t row = r0 + rr;
+                if (row >= R)
+                    break;  // warp-uniform
+                const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * kTC + lane * 8);
+                float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+                if constexpr (HAD_OK) {
+                    if (row_had) {
+                        fwht_local<8>(v);
+                        fwht_lanes(v, 1, (lane & 1) != 0);
+                        fwht_lanes(v, 2, (lane & 2) != 0);
+                    }
+                }
+                if constexpr (FMT == MX_FMT_MOSS_FP8) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = div_shared(v[e], ts, rts);
+                }
+                float bmax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    bmax = fmaxf(bmax, fabsf(v[e]));
+#pragma unroll
+                for (int m = 1; m < LPB; m <<= 1)
+                    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, m));
+                if (col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
+                    uint32_t out[2];
+                    const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
+                    const uint32_t sfb = encode_block<FMT, ROW_SR, 8>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
+                    if constexpr (FP4)
+                        *reinterpret_cast<uint32_t*>(a.row_codes + row * (C / 2) + col / 2) = out[0];
+                    else
+                        *reinterpret_cast<uint2*>(a.row_codes + row * C + col) = make_uint2(out[0], out[1]);
+                    if ((lane & (LPB - 1)) == 0)
+                        a.row_sf[sf_offset(row, col / BLOCK, kg_row)] = static_cast<uint8_t>(sfb);
+                }
+            }
+        }
+        if constexpr (DO_COL) {
+            const int64_t c = c0 + tid;
+            const int nk = static_cast<int>(R - r0 < kTR ? R - r0 : kTR);  // valid rows, a multiple of 32
+            if (c < C) {
+#pragma unroll
+                for (int k0 = 0; k0 < kTR; k0 += SEG) {
+                    if (k0 >= nk)
+                        break;
+                    uint32_t out[8];
+#pragma unroll
+                    for (int b = 0; b < SEG / BLOCK; ++b) {
+                        const bool in = k0 + b * BLOCK < nk;
+                        float blk[BLOCK];
+#pragma unroll
+                        for (int e = 0; e < BLOCK; ++e)
+                            blk[e] = __uint_as_float(static_cast<uint32_t>(tile[(k0 + b * BLOCK + e) * kTC + tid]) << 16);
+                        if constexpr (HAD_OK) {
+                            if (col_had)
+                                fwht_local<BLOCK>(blk);
+                        }
+                        if constexpr (FMT == MX_FMT_MOSS_FP8) {
+#pragma unroll
+                            for (int e = 0; e < BLOCK; ++e)
+                                blk[e] = div_shared(blk[e], ts, rts);
+                        }
+                        float bmax = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < BLOCK; ++e)
+                            bmax = fmaxf(bmax, fabsf(blk[e]));
+                        constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;
+                        const int64_t kabs = r0 + k0 + b * BLOCK;
+                        const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + kabs / 8;
+                        const uint32_t sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8,
+                                                                              out + b * WPB);
+                        if (in)
+                            a.col_sf[sf_offset(c, kabs / BLOCK, kg_col)] = static_cast<uint8_t>(sfb);
+                    }
+                    uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? (r0 + k0) / 2 : r0 + k0);
+                    reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                    if (k0 + SEG <= nk)
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with this stage
+        if (tid == 0 && i + kTStages < my_n) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(i + kTStages);
+        }
+    }
+    if (i < my_n && tid == 0) {  // gave up: let the copies already issued land before exiting
+        for (int64_t j = i; j < my_n && j < i + kTStages; ++j)
+            (void)mbar_wait_bounded(bar0 + 8u * static_cast<int>(j % kTStages), static_cast<uint32_t>(j / kTStages) & 1u,
+                                    kWaitLimitNs);
     }
 }
 
@@ -569,6 +804,85 @@ int launch_q(const QuantArgs& q, const Device& d, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+using EncodeTiledFnQ = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFnQ encode_fn_q()
+{
+    static EncodeTiledFnQ fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFnQ>(p);
+    }();
+    return fn;
+}
+
+template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
+int launch_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
+{
+    auto kernel = quant_tile_kernel<FMT, DO_ROW, DO_COL, ROW_SR, COL_SR>;
+    constexpr int smem = kTStages * kTileBytes + kTStages * 8 + 128;
+    static int configured_device = -1;
+    if (configured_device != d.id) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return MX_ERR_CUDA;
+        configured_device = d.id;
+    }
+    EncodeTiledFnQ enc = encode_fn_q();
+    if (!enc)
+        return MX_ERR_CUDA;
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(t.C), static_cast<cuuint64_t>(t.R)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {kTC, kTR};
+    const cuuint32_t estr[2] = {1u, 1u};
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(t.x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MX_ERR_CUDA;
+    const int64_t tiles = ((t.R + kTR - 1) / kTR) * ((t.C + kTC - 1) / kTC);
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(d.sms) * 2));
+    kernel<<<grid, kThreads, smem, s>>>(m, t);
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+// Stochastic rounding exists only for the E2M1 formats; the host rejects it
+// for the others, so only those instantiations are built.
+template <int FMT, bool DO_ROW, bool DO_COL>
+int launch_tile_sr(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
+{
+    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
+    const bool rsr = DO_ROW && t.row_sr, csr = DO_COL && t.col_sr;
+    if constexpr (FP4) {
+        if (rsr && csr)
+            return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, DO_COL>(t, ld, d, s);
+        if (rsr)
+            return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, false>(t, ld, d, s);
+        if (csr)
+            return launch_tile<FMT, DO_ROW, DO_COL, false, DO_COL>(t, ld, d, s);
+    }
+    if (rsr || csr)
+        return MX_ERR_UNSUPPORTED;
+    return launch_tile<FMT, DO_ROW, DO_COL, false, false>(t, ld, d, s);
+}
+
+template <bool DO_ROW, bool DO_COL>
+int launch_tile_fmt(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
+{
+    switch (t.fmt) {
+    case MX_FMT_MXFP8_E4M3: return launch_tile_sr<MX_FMT_MXFP8_E4M3, DO_ROW, DO_COL>(t, ld, d, s);
+    case MX_FMT_MXFP4_E2M1: return launch_tile_sr<MX_FMT_MXFP4_E2M1, DO_ROW, DO_COL>(t, ld, d, s);
+    case MX_FMT_NVFP4: return launch_tile_sr<MX_FMT_NVFP4, DO_ROW, DO_COL>(t, ld, d, s);
+    case MX_FMT_MOSS_FP8: return launch_tile_sr<MX_FMT_MOSS_FP8, DO_ROW, DO_COL>(t, ld, d, s);
+    default: return MX_ERR_INVALID_ARG;
+    }
+}
+
 }  // namespace
 
 int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d, cudaStream_t s)
@@ -612,6 +926,20 @@ int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s)
     default:
         return MX_ERR_INVALID_ARG;
     }
+}
+
+int launch_quantize_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
+{
+    if (t.R == 0 || t.C == 0)
+        return MX_OK;
+    const bool row = t.row_codes != nullptr, col = t.col_codes != nullptr;
+    if (row && col)
+        return launch_tile_fmt<true, true>(t, ld, d, s);
+    if (row)
+        return launch_tile_fmt<true, false>(t, ld, d, s);
+    if (col)
+        return launch_tile_fmt<false, true>(t, ld, d, s);
+    return MX_ERR_INVALID_ARG;
 }
 
 int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStream_t s)

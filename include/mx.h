@@ -151,6 +151,20 @@ int mx_quantize(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fm
                 int rounding, int scale_rule, uint64_t seed, uint32_t stream_id, int hadamard,
                 const float* amax_in, mx_tensor* out, void* stream);
 
+/* The dual-direction producer: one read of bf16 x[R, C] emits both the
+ * rowwise operand (row_out: rows R, K = C) and the colwise operand (col_out:
+ * rows C, K = R), exactly as two mx_quantize calls would, each direction with
+ * its own rounding and Hadamard options.  A layer's forward operand and the
+ * transposed operand its backward pass needs come from one pass over memory
+ * ([FAF] FP4加速为何常常"纸上富贵": operand packing, layout construction and
+ * saving backward state are the costs around the GEMM).  Both outputs share
+ * the tensor amax and tensor scale (written to both).  Requires
+ * C % block == 0 and R % 32 == 0; other rules as mx_quantize. */
+int mx_quantize_dual(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block,
+                     int scale_rule, uint64_t seed, uint32_t stream_id, int row_rounding,
+                     int row_hadamard, int col_rounding, int col_hadamard, const float* amax_in,
+                     mx_tensor* row_out, mx_tensor* col_out, void* stream);
+
 /* out[r, k] (fp32, row-major [rows, K]) = dec(code) * dec(block scale) *
  * tensor scale (if the format has one).  The inverse map of [MOSS]
  * 两级缩放实现's dequantize; a test aid, not on the hot path. */
@@ -236,6 +250,11 @@ uint64_t mx_launch_count(void);
  * from the divisor's correctly rounded reciprocal plus residual corrections)
  * next to CUDA's IEEE division (q_ieee), for n device pairs v[i] / d[i]. */
 int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, float* q_ieee, void* stream);
+
+/* Test hook: choose the producer implementation for later calls, process-wide:
+ * 0 automatic, 1 direct-load row/col kernels, 2 the shared-memory tile producer
+ * for both directions.  Outputs are identical; only the speed differs. */
+void mx_debug_set_quant_impl(int impl);
 
 /* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
  * calls, process-wide: 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA

@@ -13,12 +13,15 @@ pytestmark = pytest.mark.gpu
 FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
 
 
-@pytest.fixture(scope="module")
-def mx():
+@pytest.fixture(scope="module", params=["auto", "direct", "tile"])
+def mx(request):
+    """The library, once per producer implementation (outputs must not depend on it)."""
     import fp4_precision_gemms_gb300 as m
     m.build()
     assert torch.cuda.is_available()
-    return m
+    m.set_quant_impl(request.param)
+    yield m
+    m.set_quant_impl("auto")
 
 
 def run_both(mx, x, fmt, direction="row", **kw):
@@ -160,3 +163,41 @@ def test_bounded_wait_gives_up_and_reports(mx):
     x = workloads.draw("normal", (64, 64), 1)
     q, ref = run_both(mx, x, "mxfp8")
     assert_quant_equal(q, ref, "after timeout")
+
+
+# ------------------------------------------------------------ dual producer
+DUAL_SHAPES = [(416, 544), (256, 4096), (4096, 96), (96, 288)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", DUAL_SHAPES)
+def test_dual_producer_matches_two_single_passes(mx, fmt, shape):
+    x = workloads.draw("outliers" if fmt == "mxfp8" else "student_t3", shape, 300 + shape[1])
+    qr, qc = mx.quantize_dual(x.cuda(), fmt)
+    torch.cuda.synchronize()
+    assert_quant_equal(qr, orc.quantize(bits(x), fmt, "row"), f"dual row {fmt} {shape}")
+    assert_quant_equal(qc, orc.quantize(bits(x), fmt, "col"), f"dual col {fmt} {shape}")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8", "nvfp4"])
+def test_dual_producer_direction_options(mx, fmt):
+    """The weight-gradient pattern: dY rowwise with RNE for dgrad and colwise
+    with SR (+ Hadamard on the mxfp route) for wgrad, from one pass."""
+    x = workloads.draw("student_t3", (512, 384), 31, 1e-3)
+    sr = "sr" if fmt != "mxfp8" else "rne"
+    had = fmt != "nvfp4"
+    qr, qc = mx.quantize_dual(x.cuda(), fmt, seed=42, stream_id=1, col_rounding=sr, col_hadamard=had)
+    torch.cuda.synchronize()
+    assert_quant_equal(qr, orc.quantize(bits(x), fmt, "row"), f"dual row {fmt}")
+    ref = orc.quantize(bits(x), fmt, "col", rounding=sr, seed=42, stream_id=1, hadamard=had)
+    assert_quant_equal(qc, ref, f"dual col {fmt}")
+    qr2, qc2 = mx.quantize_dual(x.cuda(), fmt, row_hadamard=had, row_rounding=sr, seed=7)
+    torch.cuda.synchronize()
+    assert_quant_equal(qr2, orc.quantize(bits(x), fmt, "row", hadamard=had, rounding=sr, seed=7), f"dual row opts {fmt}")
+    assert_quant_equal(qc2, orc.quantize(bits(x), fmt, "col"), f"dual col plain {fmt}")
+
+
+def test_dual_producer_rejects_ragged_rows(mx):
+    with pytest.raises(mx.MXError) as e:
+        mx.quantize_dual(torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda"), "mxfp8")
+    assert e.value.code in (mx.MX_ERR_ALIGNMENT, mx.MX_ERR_INVALID_ARG)
