@@ -21,6 +21,7 @@ scaling, no collective on the data path); the step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -80,8 +81,10 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle samples every 50 ms.  Started before the warm-up
+    (nvidia-smi takes a moment to start); only the samples whose timestamps fall
+    inside the window marked by start_window()/end_window() are summarised."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -89,6 +92,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.window = [None, None]
 
     def __enter__(self):
         try:
@@ -96,14 +100,21 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
 
+    def start_window(self):
+        self.window[0] = datetime.datetime.now()
+
+    def end_window(self):
+        self.window[1] = datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)  # let the sample that straddles the window's end land
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -114,24 +125,41 @@ class ClockSampler:
     def summary(self):
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lo, hi = self.window
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    mhz, mx_mhz = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                if lo is not None and ts < lo - datetime.timedelta(milliseconds=25):
+                    continue
+                if hi is not None and ts > hi + datetime.timedelta(milliseconds=25):
+                    continue
+                sm.append(mhz)
+                smax = mx_mhz
+                try:
+                    power.append(float(parts[4]))
+                except ValueError:
+                    pass
+                for n, v in zip(names, parts[6:10]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
         os.unlink(self.path)
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons) if sm else ["unsampled"], "samples": len(sm),
+                "power_w_median": float(np.median(power)) if power else None}
+
+
+GEMM_KERNEL_NAME = {"cta_n128": "bs_gemm_kernel<{fmt}, 128x128 tiles>",
+                    "cta_n256": "bs_gemm_kernel<{fmt}, 128x256 tiles>",
+                    "pair": "bs_gemm_pair_kernel<{fmt}, 256x256 tiles, CTA pair>"}
 
 
 def quant_bytes(fmt: str, elems: int, amax_pass: bool) -> float:
@@ -146,28 +174,33 @@ def dual_bytes(fmt: str, elems: int, amax_pass: bool) -> float:
     return elems * (2.0 + (2.0 if amax_pass else 0.0) + 2.0 * (CODE_BYTES[fmt] + 1.0 / BLOCK[fmt]))
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "mx_ptx.cuh"), "quant": ("quantize.cu", "mx_ptx.cuh")}
+
+
+def source_hash(kind: str) -> str:
+    """Hash of the sources one kernel class is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_precision_gemms_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
-    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if the
-    summary was taken on the current kernel sources."""
+def ncu_traffic(kind: str, fmt: str):
+    """Mean DRAM bytes (read + write) per launch of one kernel class over one
+    step, from the committed ncu summary, if it was taken on the current
+    sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except Exception:
         return None
-    if t.get("source_hash") != source_hash():
+    e = t.get("kernels", {}).get(f"{kind}_{fmt}")
+    if e is None or e.get("source_hash") != source_hash(kind):
         return None
-    e = t.get("kernels", {}).get(kernel_key)
-    return None if e is None else e.get("dram_bytes_per_launch")
+    return e.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------ our library
@@ -236,23 +269,32 @@ def run_ours(args, world, rank, local):
             if events is not None:
                 events[i][1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert mx.last_device_status() == mx.MX_OK
+    # which GEMM kernel each scheme's launches use (named in the roofline)
+    variants = {}
+    for fmt, kind, fn, _ in calls:
+        fn()
+        if kind == "gemm":
+            variants.setdefault(fmt, set()).add(mx.last_gemm_variant())
+    gemm_kernels = {f: " + ".join(GEMM_KERNEL_NAME[v].format(fmt=f) for v in sorted(vs)) for f, vs in variants.items()}
     # per-call events for every timed step
     ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = mx.launch_count()
-    barrier(world)
-    torch.cuda.synchronize()
     with ClockSampler(device.index) as clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        assert mx.last_device_status() == mx.MX_OK
+        launches0 = mx.launch_count()
+        barrier(world)
+        torch.cuda.synchronize()
+        clk.start_window()
         t0.record(stream)
         for s in range(args.steps):
             step(ev[s])
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.end_window()
     barrier(world)
     launches = mx.launch_count() - launches0
     status = mx.last_device_status()
@@ -268,6 +310,7 @@ def run_ours(args, world, rank, local):
         a["work"] += work
         a["calls"] += 1
     result = dict(ms=ms, gemm_flops=gemm_flops, per=per, launches=launches, clocks=clk.summary(),
+                  gemm_kernels=gemm_kernels,
                   status=status, calls_per_step=len(calls))
     if not args.no_e2e:
         result["e2e"] = run_e2e(mx, wl, inputs, device, args, world)
@@ -472,7 +515,7 @@ def config_of(wl, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=5)
@@ -511,15 +554,15 @@ def main():
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
         peak = pk["bf16_tflops_sustained"] * NOMINAL_RATIO[fmt]
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "kernel": f"bs_gemm_kernel<{fmt}>",
+                "frac": round(achieved / peak, 4), "kernel": r["gemm_kernels"][fmt],
                 "peak_source": f"{src}: bf16_tflops_sustained x {NOMINAL_RATIO[fmt]:g} (nominal {fmt} / bf16 ratio)",
-                "traffic": ncu_traffic(f"gemm_{fmt}")}
+                "traffic": ncu_traffic("gemm", fmt)}
     else:
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "kernel": f"quantize<{fmt}>", "peak_source": f"{src}: hbm_gbs",
-                "traffic": ncu_traffic(f"quant_{fmt}")}
+                "traffic": ncu_traffic("quant", fmt)}
     kernels = {}
     for (f, k), a in sorted(r["per"].items()):
         if k == "gemm":

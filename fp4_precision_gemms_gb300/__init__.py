@@ -31,7 +31,8 @@ MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
-            "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_gemm_variant")
+            "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_gemm_variant",
+            "mx_debug_last_gemm_variant")
 
 
 class MXError(RuntimeError):
@@ -110,6 +111,8 @@ def lib():
             L.mx_debug_divide.argtypes = [p, p, i64, p, p, p]
             L.mx_debug_set_gemm_variant.restype = None
             L.mx_debug_set_gemm_variant.argtypes = [i32]
+            L.mx_debug_last_gemm_variant.restype = i32
+            L.mx_debug_last_gemm_variant.argtypes = []
             _lib = L
     return _lib
 
@@ -343,3 +346,9 @@ GEMM_VARIANTS = {"auto": 0, "cta_n128": 1, "cta_n256": 2, "pair": 3}
 def set_gemm_variant(variant: str) -> None:
     """Force one GEMM kernel variant (tests and tuning); "auto" restores the default."""
     lib().mx_debug_set_gemm_variant(GEMM_VARIANTS[variant])
+
+
+def last_gemm_variant() -> str:
+    """The GEMM variant the most recent GEMM launch used (a GEMM_VARIANTS key)."""
+    v = lib().mx_debug_last_gemm_variant()
+    return {i: k for k, i in GEMM_VARIANTS.items()}.get(v, "none")

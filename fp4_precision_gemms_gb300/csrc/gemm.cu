@@ -779,6 +779,7 @@ int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 // Kernel override for tests: 0 = automatic, 1 = single CTA with N = 128,
 // 2 = single CTA with N = 256, 3 = CTA pair (256 x 256 tiles).
 static int g_variant = 0;
+static int g_last_variant = 0;  // the variant the last launch_gemm chose
 
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
                 const Device& d, cudaStream_t s)
@@ -792,6 +793,7 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         const int64_t pair_tiles = ((A->rows + 255) / 256) * ((B->rows + 255) / 256);
         v = pair_tiles >= d.sms / 2 ? 3 : (B->rows > 128 ? 2 : 1);
     }
+    g_last_variant = v;
     const int kind = (A->fmt == MX_FMT_MXFP8_E4M3 || A->fmt == MX_FMT_MOSS_FP8) ? 0
                    : A->fmt == MX_FMT_MXFP4_E2M1                                ? 1
                    : A->fmt == MX_FMT_NVFP4                                     ? 2
@@ -814,5 +816,6 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
 }
 
 void set_gemm_variant(int v) { g_variant = (v >= 0 && v <= 3) ? v : 0; }
+int last_gemm_variant() { return g_last_variant; }
 
 }  // namespace mx

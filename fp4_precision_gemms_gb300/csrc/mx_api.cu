@@ -15,6 +15,7 @@ __device__ int g_status_word;
 std::atomic<uint64_t> g_kernel_launches{0};
 
 void set_gemm_variant(int v);
+int last_gemm_variant();
 
 int current_device(Device* d)
 {
@@ -588,5 +589,6 @@ void mx_debug_set_quant_impl(int impl) { g_quant_impl = (impl >= 0 && impl <= 2)
 
 // Test hook: force one GEMM kernel variant (0 = automatic).
 void mx_debug_set_gemm_variant(int variant) { set_gemm_variant(variant); }
+int mx_debug_last_gemm_variant(void) { return last_gemm_variant(); }
 
 }  // extern "C"

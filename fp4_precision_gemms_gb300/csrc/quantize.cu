@@ -114,6 +114,22 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
     return r;
 }
 
+// E2M1 codes of 8 values packed into one word, element 2i in the low nibble
+// of byte i (the K-major packing the MMA reads).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&a)[8])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]));
+    return r;
+}
+
 __device__ __forceinline__ float dec_e4m3_pos(uint32_t c)
 {
     const uint32_t e = (c >> 3) & 0xFu, m = c & 7u;
@@ -244,20 +260,134 @@ __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
 }
 
 // ---------------------------------------------------------- block encoding
-// Tensor-level constants of one producer pass.  For NVFP4 a block's divisor
-// d = fl32(dec(s_b) * s_t) takes one of 128 values (one per UE4M3 scale byte
-// s_b), so each CTA tabulates d and its correctly rounded reciprocal once.
+// Products in place of quotients.  A quotient fl32(x / D) (IEEE division) is
+// only ever used through step functions of it: an E2M1 or E4M3 code, or a
+// power-of-two scale rule.  With r within 3 ulp of 1/D, fl32(x * r) and
+// fl32(x / D) both lie within 2^-21 (relative) of x / D, so they take the same
+// step unless x / D is that close to a step boundary.  Every boundary these
+// steps use is mu * 2^k with a significand mu = 1 + j / 16 (E2M1 midpoints
+// 0.25 .. 5 need only j / 16 in {0, 1/4, 1/2, 3/4}).  For bf16 x that can
+// only happen when a bf16 value b lies within 2^-18 of mu * D (bf16 values
+// are 2^-8 apart in relative terms, so b is the bf16 rounding of mu * D) and
+// x = b * 2^k.  A certificate for D therefore checks, for each such b and
+// each binade where b * 2^k / D meets a boundary, that the product and the
+// quotient give the same step, trying r = RN(1/D) and its neighbours up to
+// 3 ulp away; it fails (returns 0: divide) when no candidate passes or more
+// than two significands have a near bf16 value.  D must lie in [2^-100,
+// 2^100] so that every x near a boundary is a normal bf16 value and no
+// product near one overflows or underflows.
+__device__ __forceinline__ bool bf16_near(float p, float& b)
+{
+    b = __bfloat162float(__float2bfloat16_rn(p));
+    return fabsf(b - p) <= p * 0x1p-18f;
+}
+
+__device__ __forceinline__ float ulp_step(float r, int k)
+{
+    return __uint_as_float(static_cast<uint32_t>(static_cast<int>(__float_as_uint(r)) + k));
+}
+
+constexpr int kCandidates = 7;  // r0, r0 + 1 ulp, r0 - 1 ulp, ... r0 - 3 ulp
+__device__ __forceinline__ int candidate_step(int c) { return (c & 1) ? (c + 1) / 2 : -(c / 2); }
+
+// E2M1 element codes of x / d: boundaries are the midpoints 0.25, 0.75, 1.25,
+// 1.75, 2.5, 3.5 and 5; returns the certified reciprocal of d or 0.
+__device__ __forceinline__ float certify_e2m1(float d)
+{
+    if (!(d >= 0x1p-100f && d <= 0x1p100f))
+        return 0.0f;
+    const float r0 = __frcp_rn(d);
+    const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+    uint32_t pass = (1u << kCandidates) - 1u;
+    int nnear = 0;
+    for (int j = 0; j < 4; ++j) {
+        const float mu = 1.0f + 0.25f * static_cast<float>(j);
+        float b;
+        if (!bf16_near(__fmul_rn(mu, d), b))
+            continue;
+        if (++nnear > 2)
+            return 0.0f;
+        for (int m = 0; m < 7; ++m) {
+            const float scale = __fdiv_rn(mids[m], mu);  // a power of two when m has mu's significand
+            if ((__float_as_uint(scale) & 0x7FFFFFu) != 0u)
+                continue;
+            const float x = __fmul_rn(b, scale);
+            const uint32_t want = cvt_e2m1x2(__fdiv_rn(x, d), 0.0f) & 0xFu;
+            for (int c = 0; c < kCandidates; ++c)
+                if ((cvt_e2m1x2(__fmul_rn(x, ulp_step(r0, candidate_step(c))), 0.0f) & 0xFu) != want)
+                    pass &= ~(1u << c);
+        }
+    }
+    return pass ? ulp_step(r0, candidate_step(__ffs(pass) - 1)) : 0.0f;
+}
+
+// E4M3 codes of q / D (MODE 0: the NVFP4 block scale) or every step of the
+// MOSS two-level scale (MODE 1: the power-of-two rule and the E4M3 codes of
+// (x / s_t) * 2^-e; there the product must equal the quotient exactly).  The
+// sixteen significands are split over the lanes of the calling warp; every
+// lane returns the same certified reciprocal or 0.
+template <int MODE>
+__device__ __forceinline__ float certify_e4m3_warp(float D)
+{
+    const int lane = threadIdx.x & 31;
+    const bool in_range = D >= 0x1p-100f && D <= 0x1p100f;
+    const float r0 = in_range ? __frcp_rn(D) : 0.0f;
+    uint32_t pass = (1u << kCandidates) - 1u;
+    bool near = false;
+    if (in_range && lane < 16) {
+        const float mu = 1.0f + static_cast<float>(lane) * 0.0625f;
+        float b;
+        near = bf16_near(__fmul_rn(mu, D), b);
+        if (near) {
+            if (MODE == 1) {
+                const float want = __fdiv_rn(b, D);
+                for (int c = 0; c < kCandidates; ++c)
+                    if (__fmul_rn(b, ulp_step(r0, candidate_step(c))) != want)
+                        pass &= ~(1u << c);
+            } else {
+                for (uint32_t code = 0; code < 126u; ++code) {  // midpoints of consecutive E4M3 values
+                    const float mid = 0.5f * (dec_e4m3_pos(code) + dec_e4m3_pos(code + 1u));
+                    const float scale = __fdiv_rn(mid, mu);
+                    if ((__float_as_uint(scale) & 0x7FFFFFu) != 0u)
+                        continue;
+                    const float x = __fmul_rn(b, scale);
+                    const uint32_t want = cvt_e4m3x2(__fdiv_rn(x, D), 0.0f) & 0x7Fu;
+                    for (int c = 0; c < kCandidates; ++c)
+                        if ((cvt_e4m3x2(__fmul_rn(x, ulp_step(r0, candidate_step(c))), 0.0f) & 0x7Fu) != want)
+                            pass &= ~(1u << c);
+                }
+            }
+        }
+    }
+    pass = __reduce_and_sync(0xFFFFFFFFu, pass);
+    const int nnear = __popc(__ballot_sync(0xFFFFFFFFu, near));
+    if (!in_range || nnear > 2 || pass == 0u)
+        return 0.0f;
+    return ulp_step(r0, candidate_step(__ffs(pass) - 1));
+}
+
+// Tensor-level constants of one producer pass.
+//  NVFP4: a block's divisor d = fl32(dec(s_b) * s_t) takes one of 128 values
+//  (one per UE4M3 scale byte s_b), so each CTA tabulates d, RN(1/d) and the
+//  certified reciprocal (-1 when d is not certified: those blocks divide).
+//  The block scale divides the block max by fl32(6 s_t), certified per tensor.
+//  MOSS: the level-1 division x / s_t, certified per tensor for the FLOOR and
+//  CEIL rules.
 struct ScaleCtx {
     float ts;              // tensor scale (1 for the MX formats)
     float rts;             // recip_for_div(ts) (MOSS)
     float nv_denom;        // fl32(6 * ts) (NVFP4)
     float rden;            // recip_for_div(nv_denom)
+    float rden_fast;       // NVFP4 block scale: certified reciprocal of nv_denom, or 0
+    float rts_fast;        // MOSS: certified reciprocal of ts, or 0
     const float2* nv_tab;  // [128] {d, recip_for_div(d)} per scale byte (NVFP4)
+    const float* nv_fast;  // [128] certified reciprocal of d (0 when d == 0), or -1 (NVFP4)
 };
 
-// Every thread calls this; the caller synchronises before the table is read.
+// Every thread calls this (whole warps); the caller synchronises before the
+// tables are read.
 template <int FMT>
-__device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* tab_smem)
+__device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* tab_smem, float* fast_smem, int rule)
 {
     ScaleCtx c;
     c.ts = tensor_scale_of(FMT, amax);
@@ -265,13 +395,44 @@ __device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* ta
     c.nv_denom = __fmul_rn(6.0f, c.ts);
     c.rden = recip_for_div(c.nv_denom);
     c.nv_tab = tab_smem;
+    c.nv_fast = fast_smem;
+    c.rden_fast = 0.0f;
+    c.rts_fast = 0.0f;
     if constexpr (FMT == MX_FMT_NVFP4) {
+        c.rden_fast = certify_e4m3_warp<0>(c.nv_denom);
         for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
             const float d = __fmul_rn(dec_e4m3_pos(static_cast<uint32_t>(sb)), c.ts);
             tab_smem[sb] = make_float2(d, recip_for_div(d));
+            const float rf = d == 0.0f ? 0.0f : certify_e2m1(d);
+            fast_smem[sb] = (d == 0.0f || rf != 0.0f) ? rf : -1.0f;
         }
     }
+    if constexpr (FMT == MX_FMT_MOSS_FP8) {
+        const float rf = certify_e4m3_warp<1>(c.ts);
+        c.rts_fast = (rule == MX_SCALE_FLOOR || rule == MX_SCALE_CEIL) ? rf : 0.0f;
+    }
     return c;
+}
+
+// MOSS level-1 scaling of one block: v <- fl32(v / s_t) for bf16 inputs v
+// whose max |v| is xmax; returns max |fl32(v / s_t)| (division by a positive
+// constant is monotone, so it is the scaled xmax).  The product path is taken
+// when certified and when the scaled block stays clear of the fp32 subnormal
+// and overflow ranges.
+template <int N>
+__device__ __forceinline__ float moss_block(float (&v)[N], float xmax, const ScaleCtx& sc)
+{
+    const float ymax = __fmul_rn(xmax, sc.rts_fast);
+    if (sc.rts_fast != 0.0f && (xmax == 0.0f || (ymax >= 0x1p-100f && ymax < 0x1p100f))) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            v[i] = __fmul_rn(v[i], sc.rts_fast);
+        return ymax;
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        v[i] = div_shared(v[i], sc.ts, sc.rts);
+    return div_shared(xmax, sc.ts, sc.rts);
 }
 
 // Encodes one scale block held as N consecutive values in registers (the
@@ -286,37 +447,18 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
     uint32_t sfbyte;
     bool zero = false;
     if constexpr (FMT == MX_FMT_NVFP4) {
-        const uint32_t sb = cvt_e4m3x2(div_shared(bmax, sc.nv_denom, sc.rden), 0.0f) & 0x7Fu;
-        const float2 drd = sc.nv_tab[sb];  // {fl32(dec(sb) * ts), its reciprocal}
+        const float qb = sc.rden_fast != 0.0f ? __fmul_rn(bmax, sc.rden_fast) : div_shared(bmax, sc.nv_denom, sc.rden);
+        const uint32_t sb = cvt_e4m3x2(qb, 0.0f) & 0x7Fu;
+        const float2 drd = sc.nv_tab[sb];  // {fl32(dec(sb) * ts), RN(1/d)}
+        const float rf = sc.nv_fast[sb];
         sfbyte = sb;
         if (drd.x == 0.0f) {
             zero = true;
-        } else {
-            if constexpr (!SR) {
-                if (drd.y != 0.0f) {
-                    // RNE needs only the E2M1 code of fl32(v / d), a monotone step
-                    // function of the quotient.  q0 = fl32(v * RN(1/d)) lies within
-                    // 2 ulp of fl32(v / d), so the codes of q0 (1 -+ 2^-20) bracket
-                    // the exact code; when they agree they are the exact code.
-                    constexpr float lo_f = 1.0f - 0x1p-20f, hi_f = 1.0f + 0x1p-20f;
-                    uint32_t agree = 1u;
+        } else if (!SR && rf > 0.0f) {  // certified: the product gives the quotient's code
 #pragma unroll
-                    for (int w = 0; w < N / 8; ++w) {
-                        uint32_t wlo = 0, whi = 0;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float qa = __fmul_rn(v[8 * w + 2 * i], drd.y);
-                            const float qb = __fmul_rn(v[8 * w + 2 * i + 1], drd.y);
-                            wlo |= cvt_e2m1x2(__fmul_rn(qa, lo_f), __fmul_rn(qb, lo_f)) << (8 * i);
-                            whi |= cvt_e2m1x2(__fmul_rn(qa, hi_f), __fmul_rn(qb, hi_f)) << (8 * i);
-                        }
-                        out[w] = wlo;
-                        agree &= (wlo == whi) ? 1u : 0u;
-                    }
-                    if (agree)
-                        return sfbyte;
-                }
-            }
+            for (int i = 0; i < N; ++i)
+                v[i] = __fmul_rn(v[i], rf);
+        } else {  // exact quotient (SR always needs it)
 #pragma unroll
             for (int i = 0; i < N; ++i)
                 v[i] = div_shared(v[i], drd.x, drd.y);
@@ -418,8 +560,9 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
     const int64_t items_per_row = (cpr + kThreads * U - 1) / (kThreads * U);
     const int64_t items = a.R * items_per_row;
     __shared__ float2 nv_tab[128];
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
-    const float ts = sc.ts, rts = sc.rts;
+    __shared__ float nv_fast[128];
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
+    const float ts = sc.ts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
     __syncthreads();
@@ -448,11 +591,6 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
                 fwht_lanes(v, 1, (lane & 1) != 0);
                 fwht_lanes(v, 2, (lane & 2) != 0);
             }
-            if constexpr (FMT == MX_FMT_MOSS_FP8) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    v[i] = div_shared(v[i], ts, rts);
-            }
             float bmax = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -460,6 +598,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
 #pragma unroll
             for (int m = 1; m < LPB; m <<= 1)
                 bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, m));
+            if constexpr (FMT == MX_FMT_MOSS_FP8)
+                bmax = moss_block(v, bmax, sc);
             if (c8 < cpr) {
                 uint32_t out[2];
                 const uint32_t sfb = encode_block<FMT, SR, 8>(v, bmax, sc, a.rule, a.seed,
@@ -489,9 +629,10 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
     constexpr int CPR = TC / 8;          // 16-byte chunks per tile row
     __shared__ __align__(16) uint16_t tile[SEG][TC];
     __shared__ float2 nv_tab[128];
+    __shared__ float nv_fast[128];
     const int64_t R = a.R, C = a.C;
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
-    const float ts = sc.ts, rts = sc.rts;
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
+    const float ts = sc.ts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
     const int64_t kgroups = sf_kgroups(R / BLOCK);
@@ -533,15 +674,12 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
                     blk[i] = __uint_as_float(static_cast<uint32_t>(tile[b * BLOCK + i][threadIdx.x]) << 16);
                 if constexpr (HAD)
                     fwht_local<BLOCK>(blk);
-                if constexpr (FMT == MX_FMT_MOSS_FP8) {
-#pragma unroll
-                    for (int i = 0; i < BLOCK; ++i)
-                        blk[i] = div_shared(blk[i], ts, rts);
-                }
                 float bmax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < BLOCK; ++i)
                     bmax = fmaxf(bmax, fabsf(blk[i]));
+                if constexpr (FMT == MX_FMT_MOSS_FP8)
+                    bmax = moss_block(blk, bmax, sc);
                 constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
                 const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
                 const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, sc, a.rule, a.seed,
@@ -560,18 +698,44 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
 
 // ------------------------------------------------------------ tile producer
 // Persistent producer over 64 x 256 tiles of x staged in shared memory by TMA
-// through a three-stage mbarrier pipeline.  From each staged tile it can emit
-// the rowwise operand (blocks along the 256 columns: each warp encodes whole
-// rows, 8 elements per lane, block maxima combined with shuffles), the colwise
-// operand (blocks along the 64 rows: each thread encodes one column into 32
-// bytes of codes), or both: one read of x then serves the forward operand and
-// the transposed operand a backward pass needs ("格式感知融合:让FP4预训练提速两倍的
-// 工程实践", section FP4加速为何常常"纸上富贵": operand packing, layout
-// construction and saving backward state are the costs around the GEMM).
-// Rounding is a compile-time choice per direction and the Hadamard transform
-// is compiled only for the MX formats, so a kernel holds only the code it runs.
+// through a three-stage mbarrier pipeline.  The eight warps consume the
+// stages without any CTA-wide barrier: each warp counts itself out of a stage
+// when it is done with it, and the last one out refills the stage.  From each
+// staged tile it can emit the rowwise operand (blocks along the 256 columns:
+// a warp encodes two rows per step, 8 elements per lane, block maxima
+// combined with shuffles), the colwise operand (blocks along the 64 rows: a
+// thread encodes one scale block of 4 adjacent columns for 16-row blocks, or
+// of 2 for 32-row blocks, read with 8- or 4-byte shared-memory loads), or both:
+// one read of x then serves the forward operand and the transposed operand a
+// backward pass needs ("格式感知融合:让FP4预训练提速两倍的工程实践", section
+// FP4加速为何常常"纸上富贵": operand packing, layout construction and saving
+// backward state are the costs around the GEMM).  Rounding is a compile-time
+// choice per direction and the Hadamard transform is compiled only for the MX
+// formats, so a kernel holds only the code it runs.
 constexpr int kTR = 64, kTC = 256, kTStages = 3;
 constexpr int kTileBytes = kTR * kTC * 2;
+
+// NVFP4 round-to-nearest-even encode of one block by products with certified
+// reciprocals (no division, no branch).  Returns the scale byte and sets
+// `redo` for a block whose products are not certified; the caller re-encodes
+// such a block with encode_block (exact division).  `v` is left unchanged.
+template <int N>
+__device__ __forceinline__ uint32_t nvfp4_encode_fast(const float (&v)[N], float bmax, const ScaleCtx& sc,
+                                                      uint32_t* out, bool& redo)
+{
+    const uint32_t sb = cvt_e4m3x2(__fmul_rn(bmax, sc.rden_fast), 0.0f) & 0x7Fu;
+    const float r = sc.nv_fast[sb];  // certified reciprocal, 0 for d == 0, -1 when not certified
+    redo = sc.rden_fast == 0.0f || r < 0.0f;
+#pragma unroll
+    for (int w = 0; w < N / 8; ++w) {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            q[i] = __fmul_rn(v[8 * w + i], r);
+        out[w] = cvt_e2m1x8(q);
+    }
+    return sb;
+}
 
 template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
 __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileArgs a)
@@ -580,52 +744,61 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     constexpr int LPB = BLOCK / 8;
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     constexpr bool HAD_OK = FMT == MX_FMT_MXFP8_E4M3 || FMT == MX_FMT_MXFP4_E2M1;
-    constexpr int SEG = FP4 ? 64 : 32;
+    constexpr int CW = BLOCK == 16 ? 4 : 2;  // colwise: columns per thread
+    constexpr int kColGroups = kTC / CW;
+    static_assert(kColGroups * (kTR / BLOCK) == kThreads, "one colwise task per encoding thread");
+    constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // 32-bit code words per colwise block
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t sbase = smem_u32(base);
-    const uint32_t bar0 = sbase + kTStages * kTileBytes;
+    const uint32_t full0 = sbase + kTStages * kTileBytes;
     __shared__ float2 nv_tab[128];
+    __shared__ float nv_fast[128];
+    __shared__ int stage_out[kTStages];  // warps done with the stage's current tile
+    __shared__ int64_t issued;           // tiles whose copy has been issued
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t R = a.R, C = a.C;
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab);
-    const float ts = sc.ts, rts = sc.rts;
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && tid == 0) {
-        *a.tensor_scale = ts;
+        *a.tensor_scale = sc.ts;
         if (a.tensor_scale_copy) {
-            *a.tensor_scale_copy = ts;
+            *a.tensor_scale_copy = sc.ts;
             *a.amax_copy = *a.amax;
         }
     }
-    const bool row_had = HAD_OK && a.row_had, col_had = HAD_OK && a.col_had;
     const int64_t ctiles = (C + kTC - 1) / kTC, tiles = ((R + kTR - 1) / kTR) * ctiles;
     const int64_t my_n = blockIdx.x < tiles ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const int64_t kg_row = sf_kgroups(C / BLOCK), kg_col = sf_kgroups(R / BLOCK);
-    const int64_t col_row_bytes = FP4 ? R / 2 : R;
-
-    auto issue = [&](int64_t i) {
+    auto issue = [&](int64_t i) {  // copy tile i of this CTA into stage i % kTStages
         const int st = static_cast<int>(i % kTStages);
         const int64_t t = blockIdx.x + i * gridDim.x;
         const int64_t rt = t / ctiles, ct = t - rt * ctiles;
-        mbar_arrive_expect_tx(bar0 + 8u * st, kTileBytes);
-        tma_load_2d(sbase + st * kTileBytes, &tmx, bar0 + 8u * st, static_cast<int32_t>(ct * kTC),
+        mbar_arrive_expect_tx(full0 + 8u * st, kTileBytes);
+        tma_load_2d(sbase + st * kTileBytes, &tmx, full0 + 8u * st, static_cast<int32_t>(ct * kTC),
                     static_cast<int32_t>(rt * kTR));
     };
     if (tid == 0) {
-        for (int st = 0; st < kTStages; ++st)
-            mbar_init(bar0 + 8u * st, 1);
+        for (int st = 0; st < kTStages; ++st) {
+            mbar_init(full0 + 8u * st, 1);
+            stage_out[st] = 0;
+        }
         fence_mbar_init();
         prefetch_tmap(&tmx);
-        for (int64_t i = 0; i < my_n && i < kTStages; ++i)
+        const int64_t first = my_n < kTStages ? my_n : kTStages;
+        for (int64_t i = 0; i < first; ++i)
             issue(i);
+        issued = first;
     }
-    __syncthreads();
-    int64_t i = 0;
-    for (; i < my_n; ++i) {
+    __syncthreads();  // scale table, barriers and counters are ready
+
+    // ---------------------------------------------------------- encoding warps
+    const bool row_had = HAD_OK && a.row_had, col_had = HAD_OK && a.col_had;
+    const int64_t kg_row = sf_kgroups(C / BLOCK), kg_col = sf_kgroups(R / BLOCK);
+    const int64_t col_row_bytes = FP4 ? R / 2 : R;
+    const int cg = tid % kColGroups, rb = tid / kColGroups;
+    for (int64_t i = 0; i < my_n; ++i) {
         const int st = static_cast<int>(i % kTStages);
-        const bool ok = mbar_wait_bounded(bar0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns);
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0)
+        if (!mbar_wait_bounded(full0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns)) {
+            if (lane == 0)
                 atomicExch(a.status, MX_ERR_TIMEOUT);
             break;
         }
@@ -634,101 +807,173 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
         const int64_t rt = t / ctiles, ct = t - rt * ctiles;
         const int64_t r0 = rt * kTR, c0 = ct * kTC;
         if constexpr (DO_ROW) {
-            // warp w encodes tile rows w, w + 8, ...; lane l owns columns 8l .. 8l + 7
+            // warp w encodes tile rows w + 8 j, two per step; lane l owns columns 8l .. 8l + 7
             const int64_t col = c0 + lane * 8;
-            for (int rr = warp; rr < kTR; rr += kThreads / 32) {
-                const int64_t row = r0 + rr;
-                if (row >= R)
-                    break;  // warp-uniform
-                const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * kTC + lane * 8);
-                float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-                if constexpr (HAD_OK) {
-                    if (row_had) {
-                        fwht_local<8>(v);
-                        fwht_lanes(v, 1, (lane & 1) != 0);
-                        fwht_lanes(v, 2, (lane & 2) != 0);
+#pragma unroll 1
+            for (int j = 0; j < kTR / 16; ++j) {
+                float v[2][8], bmax[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int rr = warp + 8 * (2 * j + h);
+                    const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * kTC + lane * 8);
+                    v[h][0] = bf16_lo(w.x), v[h][1] = bf16_hi(w.x), v[h][2] = bf16_lo(w.y), v[h][3] = bf16_hi(w.y);
+                    v[h][4] = bf16_lo(w.z), v[h][5] = bf16_hi(w.z), v[h][6] = bf16_lo(w.w), v[h][7] = bf16_hi(w.w);
+                    if constexpr (HAD_OK) {
+                        if (row_had) {
+                            fwht_local<8>(v[h]);
+                            fwht_lanes(v[h], 1, (lane & 1) != 0);
+                            fwht_lanes(v[h], 2, (lane & 2) != 0);
+                        }
                     }
-                }
-                if constexpr (FMT == MX_FMT_MOSS_FP8) {
+                    bmax[h] = 0.0f;
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        v[e] = div_shared(v[e], ts, rts);
+                        bmax[h] = fmaxf(bmax[h], fabsf(v[h][e]));
                 }
-                float bmax = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    bmax = fmaxf(bmax, fabsf(v[e]));
+                for (int m = 1; m < LPB; m <<= 1) {
+                    bmax[0] = fmaxf(bmax[0], __shfl_xor_sync(0xFFFFFFFFu, bmax[0], m));
+                    bmax[1] = fmaxf(bmax[1], __shfl_xor_sync(0xFFFFFFFFu, bmax[1], m));
+                }
+                if constexpr (FMT == MX_FMT_MOSS_FP8) {
+                    bmax[0] = moss_block(v[0], bmax[0], sc);
+                    bmax[1] = moss_block(v[1], bmax[1], sc);
+                }
+                uint32_t out[2][2], sfb[2];
+                if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
+                    bool redo0, redo1;
+                    sfb[0] = nvfp4_encode_fast<8>(v[0], bmax[0], sc, out[0], redo0);
+                    sfb[1] = nvfp4_encode_fast<8>(v[1], bmax[1], sc, out[1], redo1);
+                    if (redo0)
+                        sfb[0] = encode_block<FMT, false, 8>(v[0], bmax[0], sc, a.rule, 0, 0, 0, out[0]);
+                    if (redo1)
+                        sfb[1] = encode_block<FMT, false, 8>(v[1], bmax[1], sc, a.rule, 0, 0, 0, out[1]);
+                } else {
 #pragma unroll
-                for (int m = 1; m < LPB; m <<= 1)
-                    bmax = fmaxf(bmax, __shfl_xor_sync(0xFFFFFFFFu, bmax, m));
-                if (col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
-                    uint32_t out[2];
-                    const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
-                    const uint32_t sfb = encode_block<FMT, ROW_SR, 8>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
-                    if constexpr (FP4)
-                        *reinterpret_cast<uint32_t*>(a.row_codes + row * (C / 2) + col / 2) = out[0];
-                    else
-                        *reinterpret_cast<uint2*>(a.row_codes + row * C + col) = make_uint2(out[0], out[1]);
-                    if ((lane & (LPB - 1)) == 0)
-                        a.row_sf[sf_offset(row, col / BLOCK, kg_row)] = static_cast<uint8_t>(sfb);
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t row = r0 + warp + 8 * (2 * j + h);
+                        const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
+                        sfb[h] = encode_block<FMT, ROW_SR, 8>(v[h], bmax[h], sc, a.rule, a.seed, a.stream_id, L8, out[h]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t row = r0 + warp + 8 * (2 * j + h);
+                    if (row < R && col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
+                        if constexpr (FP4)
+                            *reinterpret_cast<uint32_t*>(a.row_codes + row * (C / 2) + col / 2) = out[h][0];
+                        else
+                            *reinterpret_cast<uint2*>(a.row_codes + row * C + col) = make_uint2(out[h][0], out[h][1]);
+                        if ((lane & (LPB - 1)) == 0)
+                            a.row_sf[sf_offset(row, col / BLOCK, kg_row)] = static_cast<uint8_t>(sfb[h]);
+                    }
                 }
             }
         }
         if constexpr (DO_COL) {
-            const int64_t c = c0 + tid;
-            const int nk = static_cast<int>(R - r0 < kTR ? R - r0 : kTR);  // valid rows, a multiple of 32
-            if (c < C) {
+            // Thread = CW adjacent columns x one scale block of rows: each
+            // shared-memory load brings CW columns of one row (a warp reads
+            // 32 * CW contiguous elements of that row: no bank conflicts), and
+            // each column's block is encoded in registers.
+            const int64_t kabs = r0 + rb * BLOCK;
+            if (kabs < R) {  // R % 32 == 0: a row block is wholly in or out
+                uint32_t pk[BLOCK][CW / 2];  // bf16 pairs: pk[e][p] = columns 2p, 2p + 1 of row e
 #pragma unroll
-                for (int k0 = 0; k0 < kTR; k0 += SEG) {
-                    if (k0 >= nk)
-                        break;
-                    uint32_t out[8];
+                for (int e = 0; e < BLOCK; ++e) {
+                    const uint16_t* src = tile + (rb * BLOCK + e) * kTC + cg * CW;
+                    if constexpr (CW == 4) {
+                        const uint2 w = *reinterpret_cast<const uint2*>(src);
+                        pk[e][0] = w.x;
+                        pk[e][CW / 2 - 1] = w.y;
+                    } else {
+                        pk[e][0] = *reinterpret_cast<const uint32_t*>(src);
+                    }
+                }
+                auto unpack = [&](int j, float (&blk)[BLOCK]) {
 #pragma unroll
-                    for (int b = 0; b < SEG / BLOCK; ++b) {
-                        const bool in = k0 + b * BLOCK < nk;
-                        float blk[BLOCK];
+                    for (int e = 0; e < BLOCK; ++e)
+                        blk[e] = (j & 1) ? bf16_hi(pk[e][j / 2]) : bf16_lo(pk[e][j / 2]);
+                };
+                uint32_t out[CW][WPB], sfb[CW];
+                bool redo[CW];
 #pragma unroll
-                        for (int e = 0; e < BLOCK; ++e)
-                            blk[e] = __uint_as_float(static_cast<uint32_t>(tile[(k0 + b * BLOCK + e) * kTC + tid]) << 16);
-                        if constexpr (HAD_OK) {
-                            if (col_had)
-                                fwht_local<BLOCK>(blk);
-                        }
-                        if constexpr (FMT == MX_FMT_MOSS_FP8) {
+                for (int j = 0; j < CW; ++j) {
+                    float blk[BLOCK];
+                    unpack(j, blk);
+                    if constexpr (HAD_OK) {
+                        if (col_had)
+                            fwht_local<BLOCK>(blk);
+                    }
+                    float bmax = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < BLOCK; ++e)
+                        bmax = fmaxf(bmax, fabsf(blk[e]));
+                    if constexpr (FMT == MX_FMT_MOSS_FP8)
+                        bmax = moss_block(blk, bmax, sc);
+                    if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
+                        sfb[j] = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out[j], redo[j]);
+                    } else {
+                        const int64_t c = c0 + cg * CW + j;
+                        const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + kabs / 8;
+                        sfb[j] = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out[j]);
+                        redo[j] = false;
+                    }
+                }
+                if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        if (redo[j]) {  // rare: products not certified for this block's scale
+                            float blk[BLOCK];
+                            unpack(j, blk);
+                            float bmax = 0.0f;
 #pragma unroll
                             for (int e = 0; e < BLOCK; ++e)
-                                blk[e] = div_shared(blk[e], ts, rts);
+                                bmax = fmaxf(bmax, fabsf(blk[e]));
+                            sfb[j] = encode_block<FMT, false, BLOCK>(blk, bmax, sc, a.rule, 0, 0, 0, out[j]);
                         }
-                        float bmax = 0.0f;
-#pragma unroll
-                        for (int e = 0; e < BLOCK; ++e)
-                            bmax = fmaxf(bmax, fabsf(blk[e]));
-                        constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;
-                        const int64_t kabs = r0 + k0 + b * BLOCK;
-                        const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + kabs / 8;
-                        const uint32_t sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8,
-                                                                              out + b * WPB);
-                        if (in)
-                            a.col_sf[sf_offset(c, kabs / BLOCK, kg_col)] = static_cast<uint8_t>(sfb);
                     }
-                    uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? (r0 + k0) / 2 : r0 + k0);
-                    reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                    if (k0 + SEG <= nk)
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                }
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    const int64_t c = c0 + cg * CW + j;
+                    if (c < C) {
+                        uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? kabs / 2 : kabs);
+                        if constexpr (WPB == 2) {
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(out[j][0], out[j][1]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < WPB / 4; ++q)
+                                reinterpret_cast<uint4*>(dst)[q] =
+                                    make_uint4(out[j][4 * q], out[j][4 * q + 1], out[j][4 * q + 2], out[j][4 * q + 3]);
+                        }
+                        a.col_sf[sf_offset(c, kabs / BLOCK, kg_col)] = static_cast<uint8_t>(sfb[j]);
+                    }
                 }
             }
         }
-        __syncthreads();  // every thread is done with this stage
-        if (tid == 0 && i + kTStages < my_n) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(i + kTStages);
+        __syncwarp();  // every lane of this warp is done reading the stage
+        if (lane == 0) {
+            __threadfence_block();  // release this warp's reads before counting out
+            if (atomicAdd(&stage_out[st], 1) == kThreads / 32 - 1) {  // last warp out refills
+                __threadfence_block();
+                stage_out[st] = 0;
+                if (i + kTStages < my_n) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(i + kTStages);
+                    atomicMax(reinterpret_cast<unsigned long long*>(&issued),
+                              static_cast<unsigned long long>(i + kTStages + 1));
+                }
+            }
         }
     }
-    if (i < my_n && tid == 0) {  // gave up: let the copies already issued land before exiting
-        for (int64_t j = i; j < my_n && j < i + kTStages; ++j)
-            (void)mbar_wait_bounded(bar0 + 8u * static_cast<int>(j % kTStages), static_cast<uint32_t>(j / kTStages) & 1u,
-                                    kWaitLimitNs);
+    // Leave only when no copy into this CTA's shared memory can still be in
+    // flight (after a timeout some issued tiles were never consumed).
+    __syncthreads();
+    if (tid == 0) {
+        const int64_t n = issued;
+        for (int64_t j = n > kTStages ? n - kTStages : 0; j < n; ++j)
+            (void)mbar_wait_bounded(full0 + 8u * static_cast<int>(j % kTStages),
+                                    static_cast<uint32_t>(j / kTStages) & 1u, kWaitLimitNs);
     }
 }
 

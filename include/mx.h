@@ -261,6 +261,10 @@ void mx_debug_set_quant_impl(int impl);
  * 128 x 256 tiles, 3 CTA-pair (cluster of two) 256 x 256 tiles. */
 void mx_debug_set_gemm_variant(int variant);
 
+/* Test/benchmark hook: the GEMM variant (numbered as above, never 0) that the
+ * most recent mx_gemm / mx_linear_* call launched, process-wide; 0 before any. */
+int mx_debug_last_gemm_variant(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -201,3 +201,52 @@ def test_dual_producer_rejects_ragged_rows(mx):
     with pytest.raises(mx.MXError) as e:
         mx.quantize_dual(torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda"), "mxfp8")
     assert e.value.code in (mx.MX_ERR_ALIGNMENT, mx.MX_ERR_INVALID_ARG)
+
+
+# ------------------------------------------- product-for-quotient certificate
+# NVFP4 and MOSS divide by a tensor-dependent scale; the producer multiplies by
+# the reciprocal only where it has certified that no bf16 input can land near a
+# rounding boundary, and divides exactly elsewhere.  These cases sweep tensor
+# scales across magnitudes, including power-of-two ones where every boundary
+# is hit exactly and the exact division must take over.
+AMAX_CASES = [None, 2688.0, 2688.0 * 2.0**-9, 2688.0 * 2.0**20, 448.0, 448.0 * 3, 448.0 * 2.0**-5,
+              3.1415927, 1.0e-3, 7.0e-3, 12345.678, 1.0e30, 1.0e-30, 3.0e38]
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "moss"])
+@pytest.mark.parametrize("amax", AMAX_CASES)
+def test_tensor_scale_sweep(mx, fmt, amax):
+    x = workloads.draw("student_t3", (256, 512), 17)
+    if amax is not None:
+        x = (x.float() * (amax / x.float().abs().max())).to(torch.bfloat16)
+    a_in = None if amax is None else torch.tensor([amax], dtype=torch.float32, device="cuda")
+    for direction in ("row", "col"):
+        q = mx.quantize(x.cuda(), fmt, direction, amax_in=a_in)
+        torch.cuda.synchronize()
+        ref = orc.quantize(bits(x), fmt, direction, amax_in=None if amax is None else float(np.float32(amax)))
+        assert_quant_equal(q, ref, f"{fmt}/{direction}/amax={amax}")
+
+
+@pytest.mark.parametrize("k", [-9, 0, 7])
+def test_nvfp4_ties_at_every_scale_byte(mx, k):
+    """Tensor scale 2^k: for every scale byte s_b the block holds 6 dec(s_b) 2^k
+    (which selects s_b) and every E2M1 midpoint times dec(s_b) 2^k, so each
+    quotient is an exact tie that a product with the rounded reciprocal could
+    push the wrong way."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    dec = np.array([orc.decode("e4m3", c) for c in range(128)])
+    rows = []
+    rng = np.random.default_rng(k + 100)
+    for sb in range(1, 127):
+        d = dec[sb] * 2.0**k
+        blk = np.array([6 * d] + [m * d for m in mids] + [-m * d for m in mids] + [0.0])
+        rows.append(np.concatenate([rng.permutation(blk) for _ in range(16)]))
+    rows += rows[:2]
+    x = torch.tensor(np.array(rows), dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(x.double().numpy(), np.array(rows))  # every value is exact in bf16
+    a_in = torch.tensor([2688.0 * 2.0**k], dtype=torch.float32, device="cuda")
+    for xx, direction in ((x, "row"), (x.t().contiguous(), "col")):
+        q = mx.quantize(xx.cuda(), "nvfp4", direction, amax_in=a_in)
+        torch.cuda.synchronize()
+        ref = orc.quantize(bits(xx), "nvfp4", direction, amax_in=2688.0 * 2.0**k)
+        assert_quant_equal(q, ref, f"ties k={k} {direction}")
