@@ -45,6 +45,12 @@ __host__ __device__ constexpr int elem_of(int fmt)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ void unpack8(const uint4& w, float* v)
+{
+    v[0] = bf16_lo(w.x), v[1] = bf16_hi(w.x), v[2] = bf16_lo(w.y), v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z), v[5] = bf16_hi(w.z), v[6] = bf16_lo(w.w), v[7] = bf16_hi(w.w);
+}
+
 // ------------------------------------------------------------ scale rules
 // b > 0 finite as (1 + mant * 2^-23) * 2^fb, exactly (subnormals normalised).
 struct Norm {
@@ -69,10 +75,16 @@ __device__ __forceinline__ Norm normalize_pos(float b)
 template <int ELEM>
 __device__ __forceinline__ int pow2_exponent(float b, int rule)
 {
-    if (b == 0.0f)
-        return 0;
     constexpr int fq = ELEM == kElemE4M3 ? 8 : 2;              // floor(log2 Q) (= emax)
     constexpr uint32_t mq = ELEM == kElemE4M3 ? 0x600000u : 0x400000u;  // Q significand bits
+    const uint32_t u = __float_as_uint(b);
+    const int E = static_cast<int>((u >> 23) & 0xFFu);
+    if (E != 0 && rule != MX_SCALE_NEAREST) {  // normal b: floor(log2 b) = E - 127
+        const int e = E - 127 - fq + ((rule == MX_SCALE_CEIL && (u & 0x7FFFFFu) > mq) ? 1 : 0);
+        return max(-127, e);
+    }
+    if (b == 0.0f)
+        return 0;
     const Norm n = normalize_pos(b);
     int e;
     if (rule == MX_SCALE_FLOOR) {
@@ -260,134 +272,101 @@ __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
 }
 
 // ---------------------------------------------------------- block encoding
-// Products in place of quotients.  A quotient fl32(x / D) (IEEE division) is
-// only ever used through step functions of it: an E2M1 or E4M3 code, or a
-// power-of-two scale rule.  With r within 3 ulp of 1/D, fl32(x * r) and
-// fl32(x / D) both lie within 2^-21 (relative) of x / D, so they take the same
-// step unless x / D is that close to a step boundary.  Every boundary these
-// steps use is mu * 2^k with a significand mu = 1 + j / 16 (E2M1 midpoints
-// 0.25 .. 5 need only j / 16 in {0, 1/4, 1/2, 3/4}).  For bf16 x that can
-// only happen when a bf16 value b lies within 2^-18 of mu * D (bf16 values
-// are 2^-8 apart in relative terms, so b is the bf16 rounding of mu * D) and
-// x = b * 2^k.  A certificate for D therefore checks, for each such b and
-// each binade where b * 2^k / D meets a boundary, that the product and the
-// quotient give the same step, trying r = RN(1/D) and its neighbours up to
-// 3 ulp away; it fails (returns 0: divide) when no candidate passes or more
-// than two significands have a near bf16 value.  D must lie in [2^-100,
-// 2^100] so that every x near a boundary is a normal bf16 value and no
-// product near one overflows or underflows.
-__device__ __forceinline__ bool bf16_near(float p, float& b)
+// Quotients by a tensor-dependent divisor D without division.  With the
+// double-word reciprocal hi = RN(1/D), lo = RN((1 - D hi) / D) (1 - D hi is
+// exact in fp32 for hi = RN(1/D)), q = fma(x, hi, x * lo) lies within 2^-46
+// (relative) of x / D before its one rounding, so q = RN(x / D) unless x / D
+// is that close to an fp32 rounding midpoint.  The quotient is only used
+// through step functions (E2M1 or E4M3 codes, power-of-two scale rules)
+// whose boundaries are mu * 2^k with significands mu = 1 + j / 16, and a
+// rounding difference can move a step only where q or RN(x / D) is such a
+// boundary, i.e. where x / D is next to (mu +- 2^-24) * 2^k (mu - 2^-25 below
+// a power of two).  For bf16 x that requires a bf16 value within 2^-46 of
+// W = (mu +- 2^-24) * D in some binade; the certificate checks every W once,
+// with a 2^-44 margin (bf16 values are 2^-8 apart, so a random D fails with
+// probability near 2^-30).  D must lie in
+// [2^-100, 2^100], so that x near a boundary is a normal bf16 value and x * lo
+// does not underflow there; callers guard the overflow side per block.
+struct Recip2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ Recip2 recip2(float D)
 {
-    b = __bfloat162float(__float2bfloat16_rn(p));
-    return fabsf(b - p) <= p * 0x1p-18f;
+    Recip2 r;
+    r.hi = __frcp_rn(D);
+    r.lo = __fmul_rn(__fmaf_rn(-D, r.hi, 1.0f), r.hi);
+    return r;
 }
 
-__device__ __forceinline__ float ulp_step(float r, int k)
+__device__ __forceinline__ float quot2(float x, const Recip2& r) { return __fmaf_rn(x, r.hi, __fmul_rn(x, r.lo)); }
+
+// Whether pattern mu = 1 + j / 2^NFRAC is clear of bf16 values on both
+// sides.  W = mu * D + s * D (s = +-2^-24, or -2^-25 below a power of two) is
+// held exactly as P_hi + P_lo + s * D (two-product of mu * D with an FMA);
+// when a bf16 value b is close, P_hi - b is exact and small, so the three
+// small terms sum to the distance with an error near 2^-48 W, well inside the
+// factor-4 margin.
+template <int NFRAC>
+__device__ __forceinline__ bool quot2_pattern_clear(float D, int j)
 {
-    return __uint_as_float(static_cast<uint32_t>(static_cast<int>(__float_as_uint(r)) + k));
+    const float mu = 1.0f + static_cast<float>(j) / static_cast<float>(1 << NFRAC);
+    const float p_hi = __fmul_rn(mu, D);
+    const float p_lo = __fmaf_rn(mu, D, -p_hi);
+    const float b = __bfloat162float(__float2bfloat16_rn(p_hi));
+    const float base = __fadd_rn(__fsub_rn(p_hi, b), p_lo);
+    const float up = __fadd_rn(base, __fmul_rn(D, 0x1p-24f));
+    const float down = __fsub_rn(base, __fmul_rn(D, j == 0 ? 0x1p-25f : 0x1p-24f));
+    const float tol = __fmul_rn(p_hi, 0x1p-44f);
+    return fabsf(up) > tol && fabsf(down) > tol;
 }
 
-constexpr int kCandidates = 7;  // r0, r0 + 1 ulp, r0 - 1 ulp, ... r0 - 3 ulp
-__device__ __forceinline__ int candidate_step(int c) { return (c & 1) ? (c + 1) / 2 : -(c / 2); }
+__device__ __forceinline__ bool in_quot2_range(float D) { return D >= 0x1p-100f && D <= 0x1p100f; }
 
-// E2M1 element codes of x / d: boundaries are the midpoints 0.25, 0.75, 1.25,
-// 1.75, 2.5, 3.5 and 5; returns the certified reciprocal of d or 0.
-__device__ __forceinline__ float certify_e2m1(float d)
+// E2M1 element codes (boundaries 0.25 .. 5: significands 1, 1.25, 1.5, 1.75).
+__device__ __forceinline__ bool quot2_certified_e2m1(float d)
 {
-    if (!(d >= 0x1p-100f && d <= 0x1p100f))
-        return 0.0f;
-    const float r0 = __frcp_rn(d);
-    const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
-    uint32_t pass = (1u << kCandidates) - 1u;
-    int nnear = 0;
-    for (int j = 0; j < 4; ++j) {
-        const float mu = 1.0f + 0.25f * static_cast<float>(j);
-        float b;
-        if (!bf16_near(__fmul_rn(mu, d), b))
-            continue;
-        if (++nnear > 2)
-            return 0.0f;
-        for (int m = 0; m < 7; ++m) {
-            const float scale = __fdiv_rn(mids[m], mu);  // a power of two when m has mu's significand
-            if ((__float_as_uint(scale) & 0x7FFFFFu) != 0u)
-                continue;
-            const float x = __fmul_rn(b, scale);
-            const uint32_t want = cvt_e2m1x2(__fdiv_rn(x, d), 0.0f) & 0xFu;
-            for (int c = 0; c < kCandidates; ++c)
-                if ((cvt_e2m1x2(__fmul_rn(x, ulp_step(r0, candidate_step(c))), 0.0f) & 0xFu) != want)
-                    pass &= ~(1u << c);
-        }
-    }
-    return pass ? ulp_step(r0, candidate_step(__ffs(pass) - 1)) : 0.0f;
+    if (!in_quot2_range(d))
+        return false;
+    bool ok = true;
+    for (int j = 0; j < 4; ++j)
+        ok &= quot2_pattern_clear<2>(d, j);
+    return ok;
 }
 
-// E4M3 codes of q / D (MODE 0: the NVFP4 block scale) or every step of the
-// MOSS two-level scale (MODE 1: the power-of-two rule and the E4M3 codes of
-// (x / s_t) * 2^-e; there the product must equal the quotient exactly).  The
-// sixteen significands are split over the lanes of the calling warp; every
-// lane returns the same certified reciprocal or 0.
-template <int MODE>
-__device__ __forceinline__ float certify_e4m3_warp(float D)
+// E4M3 codes and power-of-two rule edges (significands 1 + j / 16); the
+// sixteen patterns are split over the lanes of the calling warp.
+__device__ __forceinline__ bool quot2_certified_e4m3_warp(float D)
 {
     const int lane = threadIdx.x & 31;
-    const bool in_range = D >= 0x1p-100f && D <= 0x1p100f;
-    const float r0 = in_range ? __frcp_rn(D) : 0.0f;
-    uint32_t pass = (1u << kCandidates) - 1u;
-    bool near = false;
-    if (in_range && lane < 16) {
-        const float mu = 1.0f + static_cast<float>(lane) * 0.0625f;
-        float b;
-        near = bf16_near(__fmul_rn(mu, D), b);
-        if (near) {
-            if (MODE == 1) {
-                const float want = __fdiv_rn(b, D);
-                for (int c = 0; c < kCandidates; ++c)
-                    if (__fmul_rn(b, ulp_step(r0, candidate_step(c))) != want)
-                        pass &= ~(1u << c);
-            } else {
-                for (uint32_t code = 0; code < 126u; ++code) {  // midpoints of consecutive E4M3 values
-                    const float mid = 0.5f * (dec_e4m3_pos(code) + dec_e4m3_pos(code + 1u));
-                    const float scale = __fdiv_rn(mid, mu);
-                    if ((__float_as_uint(scale) & 0x7FFFFFu) != 0u)
-                        continue;
-                    const float x = __fmul_rn(b, scale);
-                    const uint32_t want = cvt_e4m3x2(__fdiv_rn(x, D), 0.0f) & 0x7Fu;
-                    for (int c = 0; c < kCandidates; ++c)
-                        if ((cvt_e4m3x2(__fmul_rn(x, ulp_step(r0, candidate_step(c))), 0.0f) & 0x7Fu) != want)
-                            pass &= ~(1u << c);
-                }
-            }
-        }
-    }
-    pass = __reduce_and_sync(0xFFFFFFFFu, pass);
-    const int nnear = __popc(__ballot_sync(0xFFFFFFFFu, near));
-    if (!in_range || nnear > 2 || pass == 0u)
-        return 0.0f;
-    return ulp_step(r0, candidate_step(__ffs(pass) - 1));
+    const bool ok = lane >= 16 || quot2_pattern_clear<4>(D, lane);
+    return __all_sync(0xFFFFFFFFu, ok) && in_quot2_range(D);
 }
 
 // Tensor-level constants of one producer pass.
 //  NVFP4: a block's divisor d = fl32(dec(s_b) * s_t) takes one of 128 values
-//  (one per UE4M3 scale byte s_b), so each CTA tabulates d, RN(1/d) and the
-//  certified reciprocal (-1 when d is not certified: those blocks divide).
-//  The block scale divides the block max by fl32(6 s_t), certified per tensor.
-//  MOSS: the level-1 division x / s_t, certified per tensor for the FLOOR and
-//  CEIL rules.
+//  (one per UE4M3 scale byte s_b), so each CTA tabulates {d, RN(1/d)} for the
+//  exact division and the certified double-word reciprocal of d ({0, 0} for
+//  d == 0: sign-kept zero codes; hi < 0 when not certified: those blocks
+//  divide).  The block scale divides the block max by fl32(6 s_t).
+//  MOSS: the level-1 division x / s_t (FLOOR and CEIL rules).
 struct ScaleCtx {
     float ts;              // tensor scale (1 for the MX formats)
-    float rts;             // recip_for_div(ts) (MOSS)
+    float rts;             // recip_for_div(ts) (MOSS exact path)
     float nv_denom;        // fl32(6 * ts) (NVFP4)
     float rden;            // recip_for_div(nv_denom)
-    float rden_fast;       // NVFP4 block scale: certified reciprocal of nv_denom, or 0
-    float rts_fast;        // MOSS: certified reciprocal of ts, or 0
+    Recip2 den2;           // double-word reciprocal of nv_denom
+    Recip2 ts2;            // double-word reciprocal of ts
+    bool den2_ok;          // NVFP4 block scale certified
+    bool ts2_ok;           // MOSS level-1 scaling certified
     const float2* nv_tab;  // [128] {d, recip_for_div(d)} per scale byte (NVFP4)
-    const float* nv_fast;  // [128] certified reciprocal of d (0 when d == 0), or -1 (NVFP4)
+    const float2* nv_q;    // [128] certified {hi, lo} of 1/d per scale byte (NVFP4)
 };
 
 // Every thread calls this (whole warps); the caller synchronises before the
 // tables are read.
 template <int FMT>
-__device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* tab_smem, float* fast_smem, int rule)
+__device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* tab_smem, float2* q_smem, int rule)
 {
     ScaleCtx c;
     c.ts = tensor_scale_of(FMT, amax);
@@ -395,44 +374,54 @@ __device__ __forceinline__ ScaleCtx make_scale_ctx(const float* amax, float2* ta
     c.nv_denom = __fmul_rn(6.0f, c.ts);
     c.rden = recip_for_div(c.nv_denom);
     c.nv_tab = tab_smem;
-    c.nv_fast = fast_smem;
-    c.rden_fast = 0.0f;
-    c.rts_fast = 0.0f;
+    c.nv_q = q_smem;
+    c.den2 = recip2(in_quot2_range(c.nv_denom) ? c.nv_denom : 1.0f);
+    c.ts2 = recip2(in_quot2_range(c.ts) ? c.ts : 1.0f);
+    c.den2_ok = false;
+    c.ts2_ok = false;
     if constexpr (FMT == MX_FMT_NVFP4) {
-        c.rden_fast = certify_e4m3_warp<0>(c.nv_denom);
+        c.den2_ok = quot2_certified_e4m3_warp(c.nv_denom);
         for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
             const float d = __fmul_rn(dec_e4m3_pos(static_cast<uint32_t>(sb)), c.ts);
             tab_smem[sb] = make_float2(d, recip_for_div(d));
-            const float rf = d == 0.0f ? 0.0f : certify_e2m1(d);
-            fast_smem[sb] = (d == 0.0f || rf != 0.0f) ? rf : -1.0f;
+            const Recip2 r = recip2(in_quot2_range(d) ? d : 1.0f);
+            q_smem[sb] = d == 0.0f ? make_float2(0.0f, 0.0f)
+                       : quot2_certified_e2m1(d) ? make_float2(r.hi, r.lo) : make_float2(-1.0f, 0.0f);
         }
     }
-    if constexpr (FMT == MX_FMT_MOSS_FP8) {
-        const float rf = certify_e4m3_warp<1>(c.ts);
-        c.rts_fast = (rule == MX_SCALE_FLOOR || rule == MX_SCALE_CEIL) ? rf : 0.0f;
-    }
+    if constexpr (FMT == MX_FMT_MOSS_FP8)
+        c.ts2_ok = (rule == MX_SCALE_FLOOR || rule == MX_SCALE_CEIL) && quot2_certified_e4m3_warp(c.ts);
     return c;
 }
 
 // MOSS level-1 scaling of one block: v <- fl32(v / s_t) for bf16 inputs v
-// whose max |v| is xmax; returns max |fl32(v / s_t)| (division by a positive
-// constant is monotone, so it is the scaled xmax).  The product path is taken
-// when certified and when the scaled block stays clear of the fp32 subnormal
-// and overflow ranges.
+// whose max |v| is xmax; returns max |fl32(v / s_t)| (a correctly rounded
+// division by a positive constant is monotone, so it is the scaled xmax).  The
+// product path needs the certificate and a scaled block clear of the fp32
+// subnormal and overflow ranges.
 template <int N>
 __device__ __forceinline__ float moss_block(float (&v)[N], float xmax, const ScaleCtx& sc)
 {
-    const float ymax = __fmul_rn(xmax, sc.rts_fast);
-    if (sc.rts_fast != 0.0f && (xmax == 0.0f || (ymax >= 0x1p-100f && ymax < 0x1p100f))) {
+    const float ymax = quot2(xmax, sc.ts2);
+    if (sc.ts2_ok && (xmax == 0.0f || (ymax >= 0x1p-100f && ymax < 0x1p100f))) {
 #pragma unroll
         for (int i = 0; i < N; ++i)
-            v[i] = __fmul_rn(v[i], sc.rts_fast);
+            v[i] = quot2(v[i], sc.ts2);
         return ymax;
     }
 #pragma unroll
     for (int i = 0; i < N; ++i)
         v[i] = div_shared(v[i], sc.ts, sc.rts);
     return div_shared(xmax, sc.ts, sc.rts);
+}
+
+// NVFP4 block scale byte: UE4M3_RNE(fl32(bmax / fl32(6 s_t))).  A quotient of
+// 2^100 or more saturates either way (clamping also absorbs an overflowed
+// product).
+__device__ __forceinline__ uint32_t nvfp4_scale_byte(float bmax, const ScaleCtx& sc)
+{
+    const float qb = sc.den2_ok ? fminf(quot2(bmax, sc.den2), 0x1p100f) : div_shared(bmax, sc.nv_denom, sc.rden);
+    return cvt_e4m3x2(qb, 0.0f) & 0x7Fu;
 }
 
 // Encodes one scale block held as N consecutive values in registers (the
@@ -447,17 +436,17 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
     uint32_t sfbyte;
     bool zero = false;
     if constexpr (FMT == MX_FMT_NVFP4) {
-        const float qb = sc.rden_fast != 0.0f ? __fmul_rn(bmax, sc.rden_fast) : div_shared(bmax, sc.nv_denom, sc.rden);
-        const uint32_t sb = cvt_e4m3x2(qb, 0.0f) & 0x7Fu;
+        const uint32_t sb = nvfp4_scale_byte(bmax, sc);
         const float2 drd = sc.nv_tab[sb];  // {fl32(dec(sb) * ts), RN(1/d)}
-        const float rf = sc.nv_fast[sb];
+        const float2 q2 = sc.nv_q[sb];     // certified {hi, lo}, or hi < 0
         sfbyte = sb;
         if (drd.x == 0.0f) {
             zero = true;
-        } else if (!SR && rf > 0.0f) {  // certified: the product gives the quotient's code
+        } else if (!SR && q2.x > 0.0f && __fmul_rn(bmax, q2.x) < 0x1p100f) {  // certified
+            const Recip2 r{q2.x, q2.y};
 #pragma unroll
             for (int i = 0; i < N; ++i)
-                v[i] = __fmul_rn(v[i], rf);
+                v[i] = quot2(v[i], r);
         } else {  // exact quotient (SR always needs it)
 #pragma unroll
             for (int i = 0; i < N; ++i)
@@ -560,8 +549,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
     const int64_t items_per_row = (cpr + kThreads * U - 1) / (kThreads * U);
     const int64_t items = a.R * items_per_row;
     __shared__ float2 nv_tab[128];
-    __shared__ float nv_fast[128];
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
+    __shared__ float2 nv_q[128];
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_q, a.rule);
     const float ts = sc.ts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
@@ -629,9 +618,9 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
     constexpr int CPR = TC / 8;          // 16-byte chunks per tile row
     __shared__ __align__(16) uint16_t tile[SEG][TC];
     __shared__ float2 nv_tab[128];
-    __shared__ float nv_fast[128];
+    __shared__ float2 nv_q[128];
     const int64_t R = a.R, C = a.C;
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_q, a.rule);
     const float ts = sc.ts;
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && threadIdx.x == 0)
         *a.tensor_scale = ts;
@@ -715,23 +704,25 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
 constexpr int kTR = 64, kTC = 256, kTStages = 3;
 constexpr int kTileBytes = kTR * kTC * 2;
 
-// NVFP4 round-to-nearest-even encode of one block by products with certified
-// reciprocals (no division, no branch).  Returns the scale byte and sets
-// `redo` for a block whose products are not certified; the caller re-encodes
-// such a block with encode_block (exact division).  `v` is left unchanged.
+// NVFP4 round-to-nearest-even encode of one block by certified double-word
+// reciprocal products (no division, no branch).  Returns the scale byte and
+// sets `redo` for a block whose divisor is not certified or whose quotients
+// could overflow; the caller re-encodes such a block with encode_block.  `v`
+// is left unchanged.
 template <int N>
 __device__ __forceinline__ uint32_t nvfp4_encode_fast(const float (&v)[N], float bmax, const ScaleCtx& sc,
                                                       uint32_t* out, bool& redo)
 {
-    const uint32_t sb = cvt_e4m3x2(__fmul_rn(bmax, sc.rden_fast), 0.0f) & 0x7Fu;
-    const float r = sc.nv_fast[sb];  // certified reciprocal, 0 for d == 0, -1 when not certified
-    redo = sc.rden_fast == 0.0f || r < 0.0f;
+    const uint32_t sb = nvfp4_scale_byte(bmax, sc);
+    const float2 q2 = sc.nv_q[sb];  // {0, 0} for d == 0 (sign-kept zeros), hi < 0 when not certified
+    const Recip2 r{q2.x, q2.y};
+    redo = q2.x < 0.0f || !(__fmul_rn(bmax, q2.x) < 0x1p100f);
 #pragma unroll
     for (int w = 0; w < N / 8; ++w) {
         float q[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            q[i] = __fmul_rn(v[8 * w + i], r);
+            q[i] = quot2(v[8 * w + i], r);
         out[w] = cvt_e2m1x8(q);
     }
     return sb;
@@ -741,7 +732,6 @@ template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
 __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileArgs a)
 {
     constexpr int BLOCK = fmt_block(FMT);
-    constexpr int LPB = BLOCK / 8;
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     constexpr bool HAD_OK = FMT == MX_FMT_MXFP8_E4M3 || FMT == MX_FMT_MXFP4_E2M1;
     constexpr int CW = BLOCK == 16 ? 4 : 2;  // colwise: columns per thread
@@ -753,12 +743,12 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     const uint32_t sbase = smem_u32(base);
     const uint32_t full0 = sbase + kTStages * kTileBytes;
     __shared__ float2 nv_tab[128];
-    __shared__ float nv_fast[128];
+    __shared__ float2 nv_q[128];
     __shared__ int stage_out[kTStages];  // warps done with the stage's current tile
     __shared__ int64_t issued;           // tiles whose copy has been issued
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t R = a.R, C = a.C;
-    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_fast, a.rule);
+    const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_q, a.rule);
     if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && tid == 0) {
         *a.tensor_scale = sc.ts;
         if (a.tensor_scale_copy) {
@@ -807,66 +797,63 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
         const int64_t rt = t / ctiles, ct = t - rt * ctiles;
         const int64_t r0 = rt * kTR, c0 = ct * kTC;
         if constexpr (DO_ROW) {
-            // warp w encodes tile rows w + 8 j, two per step; lane l owns columns 8l .. 8l + 7
-            const int64_t col = c0 + lane * 8;
+            // Lane = one scale block of one tile row, read as BLOCK / 8 16-byte
+            // chunks.  Plain round-to-nearest passes take the chunks in a
+            // lane-rotated order (slot i holds chunk (i + rot) % CH), which makes
+            // each quarter-warp's loads hit 32 distinct banks; codes are stored
+            // chunk by chunk at their own positions, so the order never needs
+            // undoing.  SR and the Hadamard transform need the natural order.
+            constexpr int CH = BLOCK / 8;                              // chunks per block
+            constexpr int BPR = kTC / BLOCK;                           // blocks per tile row
+            constexpr int RPS = 32 / BPR;                              // tile rows per warp step
+            constexpr int STEPS = kTR / (RPS * (kThreads / 32));
+            constexpr int CB = FP4 ? 4 : 8;                            // code bytes per chunk
+            const int kbl = lane % BPR;
+            const int64_t col = c0 + kbl * BLOCK;
+            const int64_t kb = col / BLOCK;
+            const int64_t sf_in_row = (kb >> 2) * 512 + (kb & 3);
+            const int rot = (ROW_SR || row_had) ? 0 : (CH == 2 ? (lane >> 2) & 1 : (lane >> 1) & 3);
 #pragma unroll 1
-            for (int j = 0; j < kTR / 16; ++j) {
-                float v[2][8], bmax[2];
+            for (int s2 = 0; s2 < STEPS; ++s2) {
+                const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
+                const int64_t row = r0 + rr;
+                const uint16_t* src = tile + rr * kTC + kbl * BLOCK;
+                float v[BLOCK];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int rr = warp + 8 * (2 * j + h);
-                    const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * kTC + lane * 8);
-                    v[h][0] = bf16_lo(w.x), v[h][1] = bf16_hi(w.x), v[h][2] = bf16_lo(w.y), v[h][3] = bf16_hi(w.y);
-                    v[h][4] = bf16_lo(w.z), v[h][5] = bf16_hi(w.z), v[h][6] = bf16_lo(w.w), v[h][7] = bf16_hi(w.w);
-                    if constexpr (HAD_OK) {
-                        if (row_had) {
-                            fwht_local<8>(v[h]);
-                            fwht_lanes(v[h], 1, (lane & 1) != 0);
-                            fwht_lanes(v[h], 2, (lane & 2) != 0);
-                        }
-                    }
-                    bmax[h] = 0.0f;
+                for (int i = 0; i < CH; ++i)
+                    unpack8(*reinterpret_cast<const uint4*>(src + ((i + rot) & (CH - 1)) * 8), v + 8 * i);
+                if constexpr (HAD_OK) {
+                    if (row_had)
+                        fwht_local<BLOCK>(v);
+                }
+                float bmax = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        bmax[h] = fmaxf(bmax[h], fabsf(v[h][e]));
-                }
-#pragma unroll
-                for (int m = 1; m < LPB; m <<= 1) {
-                    bmax[0] = fmaxf(bmax[0], __shfl_xor_sync(0xFFFFFFFFu, bmax[0], m));
-                    bmax[1] = fmaxf(bmax[1], __shfl_xor_sync(0xFFFFFFFFu, bmax[1], m));
-                }
-                if constexpr (FMT == MX_FMT_MOSS_FP8) {
-                    bmax[0] = moss_block(v[0], bmax[0], sc);
-                    bmax[1] = moss_block(v[1], bmax[1], sc);
-                }
-                uint32_t out[2][2], sfb[2];
+                for (int e = 0; e < BLOCK; ++e)
+                    bmax = fmaxf(bmax, fabsf(v[e]));
+                if constexpr (FMT == MX_FMT_MOSS_FP8)
+                    bmax = moss_block(v, bmax, sc);
+                uint32_t out[FP4 ? BLOCK / 8 : BLOCK / 4], sfb;
                 if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
-                    bool redo0, redo1;
-                    sfb[0] = nvfp4_encode_fast<8>(v[0], bmax[0], sc, out[0], redo0);
-                    sfb[1] = nvfp4_encode_fast<8>(v[1], bmax[1], sc, out[1], redo1);
-                    if (redo0)
-                        sfb[0] = encode_block<FMT, false, 8>(v[0], bmax[0], sc, a.rule, 0, 0, 0, out[0]);
-                    if (redo1)
-                        sfb[1] = encode_block<FMT, false, 8>(v[1], bmax[1], sc, a.rule, 0, 0, 0, out[1]);
+                    bool redo;
+                    sfb = nvfp4_encode_fast<BLOCK>(v, bmax, sc, out, redo);
+                    if (redo)  // rare: this block's divisor is not certified
+                        sfb = encode_block<FMT, false, BLOCK>(v, bmax, sc, a.rule, 0, 0, 0, out);
                 } else {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t row = r0 + warp + 8 * (2 * j + h);
-                        const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
-                        sfb[h] = encode_block<FMT, ROW_SR, 8>(v[h], bmax[h], sc, a.rule, a.seed, a.stream_id, L8, out[h]);
-                    }
+                    const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
+                    sfb = encode_block<FMT, ROW_SR, BLOCK>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
                 }
+                if (row < R && col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
+                    uint8_t* dst = a.row_codes + row * (FP4 ? C / 2 : C) + (FP4 ? col / 2 : col);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int64_t row = r0 + warp + 8 * (2 * j + h);
-                    if (row < R && col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
+                    for (int i = 0; i < CH; ++i) {
+                        const int c = (i + rot) & (CH - 1);
                         if constexpr (FP4)
-                            *reinterpret_cast<uint32_t*>(a.row_codes + row * (C / 2) + col / 2) = out[h][0];
+                            *reinterpret_cast<uint32_t*>(dst + c * CB) = out[i];
                         else
-                            *reinterpret_cast<uint2*>(a.row_codes + row * C + col) = make_uint2(out[h][0], out[h][1]);
-                        if ((lane & (LPB - 1)) == 0)
-                            a.row_sf[sf_offset(row, col / BLOCK, kg_row)] = static_cast<uint8_t>(sfb[h]);
+                            *reinterpret_cast<uint2*>(dst + c * CB) = make_uint2(out[2 * i], out[2 * i + 1]);
                     }
+                    const int64_t sf_row = ((row >> 7) * kg_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+                    a.row_sf[sf_row + sf_in_row] = static_cast<uint8_t>(sfb);
                 }
             }
         }
@@ -894,8 +881,24 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                     for (int e = 0; e < BLOCK; ++e)
                         blk[e] = (j & 1) ? bf16_hi(pk[e][j / 2]) : bf16_lo(pk[e][j / 2]);
                 };
-                uint32_t out[CW][WPB], sfb[CW];
-                bool redo[CW];
+                const int64_t cbase = c0 + cg * CW;
+                const int64_t sf_col = sf_offset(cbase, kabs / BLOCK, kg_col);  // + 16 j for column cbase + j
+                auto store = [&](int j, const uint32_t (&out)[WPB], uint32_t sfb) {
+                    const int64_t c = cbase + j;
+                    if (c < C) {
+                        uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? kabs / 2 : kabs);
+                        if constexpr (WPB == 2) {
+                            *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < WPB / 4; ++q)
+                                reinterpret_cast<uint4*>(dst)[q] =
+                                    make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+                        }
+                        a.col_sf[sf_col + 16 * j] = static_cast<uint8_t>(sfb);
+                    }
+                };
+                uint32_t redo_mask = 0;
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
                     float blk[BLOCK];
@@ -910,43 +913,35 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                         bmax = fmaxf(bmax, fabsf(blk[e]));
                     if constexpr (FMT == MX_FMT_MOSS_FP8)
                         bmax = moss_block(blk, bmax, sc);
+                    uint32_t out[WPB], sfb;
                     if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
-                        sfb[j] = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out[j], redo[j]);
+                        bool redo;
+                        sfb = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out, redo);
+                        redo_mask |= (redo ? 1u : 0u) << j;
                     } else {
-                        const int64_t c = c0 + cg * CW + j;
-                        const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + kabs / 8;
-                        sfb[j] = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out[j]);
-                        redo[j] = false;
+                        const uint64_t L8 = static_cast<uint64_t>(cbase + j) * (R / 8) + kabs / 8;
+                        sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
                     }
+                    store(j, out, sfb);
                 }
                 if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
+                    if (redo_mask) {  // rare: a block whose divisor is not certified
 #pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        if (redo[j]) {  // rare: products not certified for this block's scale
-                            float blk[BLOCK];
-                            unpack(j, blk);
-                            float bmax = 0.0f;
+                        for (int j = 0; j < CW; ++j) {
+                            if (redo_mask & (1u << j)) {
+                                float blk[BLOCK];  // re-read from the stage (still held by this warp)
 #pragma unroll
-                            for (int e = 0; e < BLOCK; ++e)
-                                bmax = fmaxf(bmax, fabsf(blk[e]));
-                            sfb[j] = encode_block<FMT, false, BLOCK>(blk, bmax, sc, a.rule, 0, 0, 0, out[j]);
+                                for (int e = 0; e < BLOCK; ++e)
+                                    blk[e] = __uint_as_float(static_cast<uint32_t>(tile[(rb * BLOCK + e) * kTC + cg * CW + j]) << 16);
+                                float bmax = 0.0f;
+#pragma unroll
+                                for (int e = 0; e < BLOCK; ++e)
+                                    bmax = fmaxf(bmax, fabsf(blk[e]));
+                                uint32_t out[WPB];
+                                const uint32_t sfb = encode_block<FMT, false, BLOCK>(blk, bmax, sc, a.rule, 0, 0, 0, out);
+                                store(j, out, sfb);
+                            }
                         }
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < CW; ++j) {
-                    const int64_t c = c0 + cg * CW + j;
-                    if (c < C) {
-                        uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? kabs / 2 : kabs);
-                        if constexpr (WPB == 2) {
-                            *reinterpret_cast<uint2*>(dst) = make_uint2(out[j][0], out[j][1]);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < WPB / 4; ++q)
-                                reinterpret_cast<uint4*>(dst)[q] =
-                                    make_uint4(out[j][4 * q], out[j][4 * q + 1], out[j][4 * q + 2], out[j][4 * q + 3]);
-                        }
-                        a.col_sf[sf_offset(c, kabs / BLOCK, kg_col)] = static_cast<uint8_t>(sfb[j]);
                     }
                 }
             }

@@ -210,7 +210,7 @@ def test_dual_producer_rejects_ragged_rows(mx):
 # scales across magnitudes, including power-of-two ones where every boundary
 # is hit exactly and the exact division must take over.
 AMAX_CASES = [None, 2688.0, 2688.0 * 2.0**-9, 2688.0 * 2.0**20, 448.0, 448.0 * 3, 448.0 * 2.0**-5,
-              3.1415927, 1.0e-3, 7.0e-3, 12345.678, 1.0e30, 1.0e-30, 3.0e38]
+              3.1415927, 1.0e-3, 7.0e-3, 12345.678, 1.0e30, 1.0e-30, 3.0e38, 266.0, 224.0, 0.59375]
 
 
 @pytest.mark.parametrize("fmt", ["nvfp4", "moss"])
