@@ -377,11 +377,15 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 //   warp 0        TMA producer (both CTAs): code and scale tiles, completing on
 //                 the rank-0 CTA's stage barrier (two arrivals per stage).
 //   warp 1        TMEM allocation (both CTAs, jointly); in rank 0 one thread
-//                 issues the scale copies and MMAs for the pair and frees
-//                 stages and the accumulator with multicast commits.
+//                 issues the MMAs for the pair and frees stages and the
+//                 accumulator with multicast commits.
 //   warps 2-9     epilogue (both CTAs): pull this CTA's 128 x 256 accumulator
 //                 rows from TMEM into registers, release the accumulator to the
 //                 next tile's MMAs, then scale and store.
+//   warp 10       in rank 0 one thread copies each stage's scale factors into
+//                 TMEM (tcgen05.cp) as soon as the stage is full and signals
+//                 the MMA thread: issuing a copy costs the issuing thread tens
+//                 of cycles, which on the MMA thread left the tensor pipe idle.
 // Scale factors live in one TMEM slot per pipeline stage.
 template <int KIND, int STAGES_>
 struct CfgPair {
@@ -408,7 +412,8 @@ struct CfgPair {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int SMEM_BYTES = OFF_BAR + (2 * STAGES + 3) * 8 + 16;
+    static constexpr int OFF_SFBAR = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // scale slot s copied
+    static constexpr int SMEM_BYTES = OFF_SFBAR + STAGES * 8;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
     static constexpr int SFT = STAGES;  // one scale slot per pipeline stage
     static constexpr int SFA_COLS = 4 * NCHUNK;
@@ -418,7 +423,8 @@ struct CfgPair {
     static constexpr int TM_USED = TM_SFB + SFT * SFB_COLS;
     static constexpr int TM_ALLOC = 512;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int THREADS = 64 + EPI_WARPS * 32;
+    static constexpr int SF_WARP = 2 + EPI_WARPS;             // the scale-copy warp
+    static constexpr int THREADS = 64 + EPI_WARPS * 32 + 32;
     static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;
     static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
     static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // per CTA per stage
@@ -484,6 +490,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
         mbar_init(accf, 1);
         mbar_init(acce, 2);  // one arrival from each CTA's epilogue
         mbar_init(tdone, G::EPI_WARPS);
+        for (int st = 0; st < STAGES; ++st)
+            mbar_init(s0 + G::OFF_SFBAR + 8u * st, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
@@ -565,18 +573,16 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
                         stop = true;
                         break;
                     }
+                    // the scale-copy warp has put this stage's scale factors in its slot
+                    if (!mbar_wait_bounded(s0 + G::OFF_SFBAR + 8u * s, round & 1u, p.wait_ns)) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + G::TM_SFA + slot * G::SFA_COLS;
                     const uint32_t sfb_t = tmem + G::TM_SFB + slot * G::SFB_COLS;
-#pragma unroll
-                    for (int c = 0; c < G::NCHUNK; ++c)
-                        tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(s0 + G::OFF_SFA + s * G::SFA_BYTES + c * 512));
-#pragma unroll
-                    for (int r = 0; r < G::SFB_RT; ++r)
-#pragma unroll
-                        for (int c = 0; c < G::NCHUNK; ++c)
-                            tc_cp_sf_pair(sfb_t + 8 * c + 4 * r,
-                                          sdesc_sf(s0 + G::OFF_SFB + s * G::SFB_BYTES + (r * G::NCHUNK + c) * 512));
                     const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES);
                     const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES);
 #pragma unroll
@@ -592,6 +598,46 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
                     tc_commit_pair(empty(s), 0x3);
                 }
                 tc_commit_pair(accf, 0x3);  // this tile's accumulator is complete in both CTAs
+            }
+        }
+        __syncwarp();
+    } else if (warp == G::SF_WARP) {
+        // Scale-factor copies (tcgen05.cp) into each stage's TMEM slot, issued
+        // from their own thread so that the MMA thread issues only MMAs.  A
+        // slot is free once its stage is full again: the producer refilled the
+        // stage only after the MMAs that read the slot had completed.
+        if (lane == 0 && rank == 0) {
+            int it = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
+                    if (!mbar_wait_bounded(full(s), round & 1u, p.wait_ns) || *abort_flag) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
+                    const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
+#pragma unroll
+                    for (int c = 0; c < G::NCHUNK; ++c)
+                        tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(s0 + G::OFF_SFA + s * G::SFA_BYTES + c * 512));
+#pragma unroll
+                    for (int r = 0; r < G::SFB_RT; ++r)
+#pragma unroll
+                        for (int c = 0; c < G::NCHUNK; ++c)
+                            tc_cp_sf_pair(sfb_t + 8 * c + 4 * r,
+                                          sdesc_sf(s0 + G::OFF_SFB + s * G::SFB_BYTES + (r * G::NCHUNK + c) * 512));
+                    tc_commit_pair(s0 + G::OFF_SFBAR + 8u * s, 0x1);  // to the MMA thread's CTA
+                }
+            }
+            if (stop && it > 0) {  // the last copies must finish before TMEM is released
+                const int l = it - 1;
+                (void)mbar_wait_bounded(s0 + G::OFF_SFBAR + 8u * (l % STAGES), static_cast<uint32_t>(l / STAGES) & 1u,
+                                        kWaitLimitNs);
             }
         }
         __syncwarp();
