@@ -322,7 +322,8 @@ def run_ours(args, world, rank, local):
 def run_e2e(mx, wl, dev_inputs, device, args, world):
     """The same step through the public linear-layer API with host buffers:
     pinned-host -> device copies of every input, mx.linear_fwd / linear_bwd,
-    device -> pinned-host copies of every output, all inside the timed region."""
+    device -> pinned-host copies of every output, all inside the timed region
+    (copies overlap the compute of neighbouring layers on their own streams)."""
     host_in = {k: v.cpu().pin_memory() for k, v in dev_inputs.items()}
     bufs = []
     for fmt in wl.formats:
@@ -345,17 +346,41 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
     d2h = sum(b["Y"].nbytes + b["dX"].nbytes + b["dW"].nbytes for b in bufs)
     flops = sum(6.0 * b["g"].tokens * b["g"].k_in * b["g"].n_out for b in bufs)
 
+    # Three streams: host->device copies, compute, device->host copies.  Unit
+    # u's inputs land while unit u-1 computes and its outputs leave while unit
+    # u+1 computes; events keep a buffer from being overwritten before the
+    # previous step is done with it.
+    compute = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    for b in bufs:
+        b["in_ready"], b["computed"], b["out_done"] = ev(), ev(), ev()
+        b["computed"].record(compute)
+        b["out_done"].record(compute)
+
     def step():
         for b in bufs:
             g = b["g"]
-            b["X"].copy_(host_in[g.x.name], non_blocking=True)
-            b["W"].copy_(host_in[g.w.name], non_blocking=True)
-            b["dY"].copy_(host_in[g.dy.name], non_blocking=True)
+            h2d_s.wait_event(b["computed"])  # the previous step no longer reads these inputs
+            with torch.cuda.stream(h2d_s):
+                b["X"].copy_(host_in[g.x.name], non_blocking=True)
+                b["W"].copy_(host_in[g.w.name], non_blocking=True)
+                b["dY"].copy_(host_in[g.dy.name], non_blocking=True)
+            b["in_ready"].record(h2d_s)
+        for b in bufs:
+            compute.wait_event(b["in_ready"])
+            compute.wait_event(b["out_done"])  # the previous step's outputs have left
             mx.linear_fwd(b["X"], b["W"], b["fmt"], workspace=b["wsf"], out=b["Y"])
             mx.linear_bwd(b["dY"], b["X"], b["W"], b["fmt"], workspace=b["wsb"], dX=b["dX"], dW=b["dW"])
-            b["hY"].copy_(b["Y"], non_blocking=True)
-            b["hdX"].copy_(b["dX"], non_blocking=True)
-            b["hdW"].copy_(b["dW"], non_blocking=True)
+            b["computed"].record(compute)
+            d2h_s.wait_event(b["computed"])
+            with torch.cuda.stream(d2h_s):
+                b["hY"].copy_(b["Y"], non_blocking=True)
+                b["hdX"].copy_(b["dX"], non_blocking=True)
+                b["hdW"].copy_(b["dW"], non_blocking=True)
+            b["out_done"].record(d2h_s)
+        for b in bufs:  # the step ends when its last result is on the host
+            compute.wait_event(b["out_done"])
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
