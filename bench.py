@@ -481,7 +481,8 @@ def run_reference(args, world, rank):
 
 def run_case(args):
     """One kernel on its own, for tuning and small ncu captures:
-    gemm:<fmt>:MxNxK  or  quant:<fmt>:<row|col>:RxC  (bf16 Student-t inputs)."""
+    gemm:<fmt>:MxNxK, gemmq:<fmt>:<out fmt>:MxNxK (quantized epilogue) or
+    quant:<fmt>:<row|col|dual>:RxC  (bf16 Student-t inputs)."""
     import fp4_precision_gemms_gb300 as mx
     mx.build()
     mx.set_gemm_variant(args.gemm_variant)
@@ -497,6 +498,14 @@ def run_case(args):
         b = mx.quantize(workloads.draw("normal", (N, K), 2, 0.02, device=dev), fmt)
         out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         fn = lambda: mx.gemm(a, b, out=out)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif parts[0] == "gemmq":  # GEMM whose epilogue writes the next layer's MX operand
+        fmt, ofmt = parts[1], parts[2]
+        M, N, K = (int(v) for v in parts[3].split("x"))
+        a = mx.quantize(workloads.draw("student_t3", (M, K), 1, device=dev), fmt)
+        b = mx.quantize(workloads.draw("normal", (N, K), 2, 0.02, device=dev), fmt)
+        q = mx.MXTensor(ofmt, M, N, dev)
+        fn = lambda: mx.gemm_quantized(a, b, ofmt, out=q)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
     else:
         fmt, direction = parts[1], parts[2]

@@ -29,6 +29,7 @@ MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
 MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
+            "mx_gemm_quantized",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
             "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_gemm_variant",
@@ -90,6 +91,9 @@ def lib():
             L.mx_dequantize.argtypes = [C.POINTER(_CTensor), p, p]
             L.mx_gemm.restype = i32
             L.mx_gemm.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float, p, i64, i32, p]
+            L.mx_gemm_quantized.restype = i32
+            L.mx_gemm_quantized.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float,
+                                            C.POINTER(_CTensor), p]
             L.mx_linear_workspace_bytes.restype = sz
             L.mx_linear_workspace_bytes.argtypes = [i64, i64, i64, i32, i32]
             L.mx_linear_fwd.restype = i32
@@ -257,6 +261,17 @@ def gemm(a: MXTensor, b: MXTensor, extra_alpha: float = 1.0, out_dtype=torch.flo
     rc = lib().mx_gemm(C.byref(ca), C.byref(cb), float(extra_alpha), _ptr(out), out.stride(0),
                        OUT[out.dtype], _stream(stream))
     _check(rc, "mx_gemm")
+    return out
+
+
+def gemm_quantized(a: MXTensor, b: MXTensor, fmt: str = "mxfp8", extra_alpha: float = 1.0,
+                   out: MXTensor | None = None, stream=None) -> MXTensor:
+    """alpha * dq(a) dq(b)^T quantized in the GEMM epilogue into the rowwise MX
+    operand (rows M = a.rows, K = N = b.rows) of format fmt (mxfp8 or mxfp4)."""
+    out = out if out is not None else MXTensor(fmt, a.rows, b.rows, a.codes.device)
+    ca, cb, co = a._c(), b._c(), out._c()
+    _check(lib().mx_gemm_quantized(C.byref(ca), C.byref(cb), float(extra_alpha), C.byref(co), _stream(stream)),
+           "mx_gemm_quantized")
     return out
 
 

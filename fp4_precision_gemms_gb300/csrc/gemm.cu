@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "mx_codec.cuh"
 #include "mx_internal.cuh"
 #include "mx_ptx.cuh"
 
@@ -74,6 +75,85 @@ struct Cfg {
     static_assert(BN % 128 == 0 && BN <= 256, "tile N");
 };
 
+// Epilogue outputs: fp32 or bf16 C, or C quantized on the fly into the
+// rowwise MX operand a following GEMM consumes (codes + E8M0 scales in the
+// tensor core's scale layout): the epilogue thread already holds 32
+// consecutive columns of one row, which is one MX scale block.
+enum EpiMode { EPI_F32 = 0, EPI_BF16 = 1, EPI_MXFP8 = 2, EPI_MXFP4 = 3 };
+
+// Stores columns col0 .. col0 + 31 of one output row; v = alpha * acc (fp32).
+// c is the output (or the codes of the quantized output), ldc its row stride
+// in elements (codes: bytes = N for MXFP8, N / 2 for MXFP4).
+__device__ __forceinline__ void store_chunk(int mode, void* c, int64_t ldc, uint8_t* q_sf, int64_t q_kgroups, int N,
+                                            int row, int col0, float (&v)[32])
+{
+    const bool full_chunk = col0 + 32 <= N;
+    if (mode == EPI_BF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(c) + static_cast<int64_t>(row) * ldc + col0;
+        if (full_chunk) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * w + 2 * h], v[8 * w + 2 * h + 1]);
+                    pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                reinterpret_cast<uint4*>(dst)[w] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col0 + i < N)
+                    dst[i] = __float2bfloat16_rn(v[i]);
+        }
+    } else if (mode == EPI_F32) {
+        float* dst = static_cast<float*>(c) + static_cast<int64_t>(row) * ldc + col0;
+        if (full_chunk) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col0 + i < N)
+                    dst[i] = v[i];
+        }
+    } else {  // N % 32 == 0: the chunk is one whole scale block
+        float bmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            bmax = fmaxf(bmax, fabsf(v[i]));
+        uint8_t* dst = static_cast<uint8_t*>(c) + static_cast<int64_t>(row) * ldc;
+        int e;
+        if (mode == EPI_MXFP8) {
+            e = pow2_exponent<kElemE4M3>(bmax, MX_SCALE_FLOOR);
+            const float s2 = exp2_neg(e);
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], s2), __fmul_rn(v[4 * i + 1], s2)) |
+                       (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], s2), __fmul_rn(v[4 * i + 3], s2)) << 16);
+            reinterpret_cast<uint4*>(dst + col0)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(dst + col0)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+            e = pow2_exponent<kElemE2M1>(bmax, MX_SCALE_FLOOR);
+            const float s2 = exp2_neg(e);
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    q[j] = __fmul_rn(v[8 * i + j], s2);
+                w[i] = cvt_e2m1x8(q);
+            }
+            *reinterpret_cast<uint4*>(dst + col0 / 2) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        q_sf[sf_offset(row, col0 / 32, q_kgroups)] = static_cast<uint8_t>(e + 127);
+    }
+}
+
 struct GemmParams {
     const uint8_t* sfa;
     const uint8_t* sfb;
@@ -83,7 +163,9 @@ struct GemmParams {
     void* c;
     int64_t ldc;
     int M, N, K;
-    int out_bf16;
+    int out_mode;     // an EpiMode
+    uint8_t* q_sf;    // scale bytes of a quantized output (EPI_MXFP8 / EPI_MXFP4)
+    int64_t q_kgroups;
     int64_t kgroups;  // 4-block SF groups along K (same for A and B)
     int m_tiles, n_tiles, group_m;  // tile grid and the M-extent of a raster group
     int* status;
@@ -242,39 +324,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
-                    const bool full_chunk = col0 + 32 <= p.N;
-                    if (p.out_bf16) {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
-                        if (full_chunk) {
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                uint32_t pk[4];
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * w + 2 * h], v[8 * w + 2 * h + 1]);
-                                    pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
-                                }
-                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    dst[i] = __float2bfloat16_rn(v[i]);
-                        }
-                    } else {
-                        float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
-                        if (full_chunk) {
-#pragma unroll
-                            for (int w = 0; w < 8; ++w)
-                                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    dst[i] = v[i];
-                        }
-                    }
+                    store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
         }
@@ -325,8 +375,8 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_b
 }
 
 template <int KIND, int BN, int STAGES>
-int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
-                const Device& d, cudaStream_t s)
+int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
+                uint8_t* q_sf, const Device& d, cudaStream_t s)
 {
     using G = Cfg<KIND, BN, STAGES>;
     static int configured_device = -1;  // attribute set once per device for this instantiation
@@ -352,7 +402,9 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.out_bf16 = out_dtype == MX_OUT_BF16;
+    p.out_mode = out_mode;
+    p.q_sf = q_sf;
+    p.q_kgroups = sf_kgroups(N / 32);
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.status = d.status;
     p.wait_ns = kWaitLimitNs;
@@ -439,7 +491,9 @@ struct PairParams {
     void* c;
     int64_t ldc;
     int M, N, K;
-    int out_bf16;
+    int out_mode;
+    uint8_t* q_sf;
+    int64_t q_kgroups;
     int64_t kgroups;
     int m_tiles, n_tiles, group_m;  // 256 x 256 tiles
     int* status;
@@ -685,39 +739,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __fmul_rn(__uint_as_float(r[j][i]), alpha);
-                    const bool full_chunk = col0 + 32 <= p.N;
-                    if (p.out_bf16) {
-                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
-                        if (full_chunk) {
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                uint32_t pk[4];
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * w + 2 * h], v[8 * w + 2 * h + 1]);
-                                    pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
-                                }
-                                reinterpret_cast<uint4*>(dst)[w] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    dst[i] = __float2bfloat16_rn(v[i]);
-                        }
-                    } else {
-                        float* dst = static_cast<float*>(p.c) + static_cast<int64_t>(row) * p.ldc + col0;
-                        if (full_chunk) {
-#pragma unroll
-                            for (int w = 0; w < 8; ++w)
-                                reinterpret_cast<float4*>(dst)[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < p.N)
-                                    dst[i] = v[i];
-                        }
-                    }
+                    store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
         }
@@ -751,8 +773,8 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
 }
 
 template <int KIND, int STAGES>
-int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
-                const Device& d, cudaStream_t s)
+int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
+                uint8_t* q_sf, const Device& d, cudaStream_t s)
 {
     using G = CfgPair<KIND, STAGES>;
     auto kernel = bs_gemm_pair_kernel<KIND, STAGES>;
@@ -795,7 +817,9 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.out_bf16 = out_dtype == MX_OUT_BF16;
+    p.out_mode = out_mode;
+    p.q_sf = q_sf;
+    p.q_kgroups = sf_kgroups(N / 32);
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.m_tiles = static_cast<int>((M + 255) / 256);
     p.n_tiles = static_cast<int>((N + 255) / 256);
@@ -812,12 +836,12 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 }
 
 template <int KIND>
-int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_dtype,
-                const Device& d, cudaStream_t s, int bn)
+int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
+                uint8_t* q_sf, const Device& d, cudaStream_t s, int bn)
 {
     if (bn == 128)
-        return launch_tile<KIND, 128, 4>(A, B, extra, C, ldc, out_dtype, d, s);
-    return launch_tile<KIND, 256, 4>(A, B, extra, C, ldc, out_dtype, d, s);
+        return launch_tile<KIND, 128, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s);
+    return launch_tile<KIND, 256, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s);
 }
 
 }  // namespace
@@ -827,8 +851,8 @@ int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 static int g_variant = 0;
 static int g_last_variant = 0;  // the variant the last launch_gemm chose
 
-int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
-                const Device& d, cudaStream_t s)
+int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_mode,
+                const Device& d, cudaStream_t s, uint8_t* q_sf)
 {
     if (A->rows == 0 || B->rows == 0)
         return MX_OK;
@@ -848,16 +872,16 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         return MX_ERR_INVALID_ARG;
     if (v == 3) {
         switch (kind) {
-        case 0: return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
-        case 1: return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
-        default: return launch_pair<2, 5>(A, B, extra_alpha, C, ldc, out_dtype, d, s);
+        case 0: return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        case 1: return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        default: return launch_pair<2, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         }
     }
     const int bn = v == 1 ? 128 : 256;
     switch (kind) {
-    case 0: return launch_kind<0>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
-    case 1: return launch_kind<1>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
-    default: return launch_kind<2>(A, B, extra_alpha, C, ldc, out_dtype, d, s, bn);
+    case 0: return launch_kind<0>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
+    case 1: return launch_kind<1>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
+    default: return launch_kind<2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
     }
 }
 

@@ -340,6 +340,38 @@ int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C
     return launch_gemm(A, B, extra, C, ldc, out_dtype, d, s);
 }
 
+// The GEMM with its output quantized in the epilogue into the rowwise MX
+// operand `out` (rows M, K = N) that a following GEMM consumes.
+int gemm_quantized_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, mx_tensor* out, const Device& d,
+                        cudaStream_t s)
+{
+    int rc = check_operand(A);
+    if (rc == MX_OK)
+        rc = check_operand(B);
+    if (rc != MX_OK)
+        return rc;
+    if (A->fmt != B->fmt || A->k != B->k || A->hadamard != B->hadamard || !out)
+        return MX_ERR_INVALID_ARG;
+    if (out->fmt != MX_FMT_MXFP8_E4M3 && out->fmt != MX_FMT_MXFP4_E2M1)
+        return MX_ERR_UNSUPPORTED;
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    if (N % 32 != 0 || K % gemm_k_multiple(A->fmt) != 0)
+        return MX_ERR_ALIGNMENT;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return MX_ERR_UNSUPPORTED;
+    if ((rc = check_output(out, out->fmt, M, N)) != MX_OK || !aligned16(out->sf))
+        return rc != MX_OK ? rc : MX_ERR_ALIGNMENT;
+    fill_meta(out, M, N, out->fmt, 0);
+    if (M == 0 || N == 0)
+        return MX_OK;
+    if (K == 0)
+        return MX_ERR_UNSUPPORTED;  // an all-zero product has no use as an operand here
+    const float extra = A->hadamard ? extra_alpha * (1.0f / 32.0f) : extra_alpha;
+    const int mode = out->fmt == MX_FMT_MXFP8_E4M3 ? 2 : 3;
+    const int64_t row_bytes = out->fmt == MX_FMT_MXFP8_E4M3 ? N : N / 2;
+    return launch_gemm(A, B, extra, out->codes, row_bytes, mode, d, s, out->sf);
+}
+
 }  // namespace
 
 extern "C" {
@@ -418,6 +450,15 @@ int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, 
     if (rc != MX_OK)
         return rc;
     return gemm_impl(A, B, extra_alpha, C, ldc, out_dtype, d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm_quantized(const mx_tensor* A, const mx_tensor* B, float extra_alpha, mx_tensor* out, void* stream)
+{
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return gemm_quantized_impl(A, B, extra_alpha, out, d, static_cast<cudaStream_t>(stream));
 }
 
 size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass)

@@ -183,6 +183,22 @@ int mx_dequantize(const mx_tensor* A, float* out, void* stream);
 int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
             int out_dtype, void* stream);
 
+/* The block-scaled GEMM with its result quantized in the epilogue into the
+ * rowwise MX operand that a following GEMM consumes ([FAF]
+ * 格式感知融合的设计思路: the producer writes the consumer's layout, here the
+ * GEMM itself is the producer).  out->fmt is MX_FMT_MXFP8_E4M3 or
+ * MX_FMT_MXFP4_E2M1; the function sets out->rows = M = A->rows, out->k = N =
+ * B->rows, out->block = 32, out->hadamard = 0.  Each 32-column block of a row
+ * of v = alpha * acc (the fp32 value mx_gemm would return as fp32, same alpha
+ * rule) gets the FLOOR-rule E8M0 scale and round-to-nearest-even codes, exactly
+ * as mx_quantize would encode an fp32 input; codes are K-major (out->codes,
+ * mx_codes_bytes(out->fmt, M, N) bytes, 16-byte aligned) and scale bytes in the
+ * tensor-core layout (out->sf, mx_sf_bytes bytes, 16-byte aligned; the padding
+ * is not written).  Requires N % 32 == 0, K > 0 and the mx_gemm rules for A and
+ * B.  Errors: MX_ERR_UNSUPPORTED for another output format, MX_ERR_ALIGNMENT
+ * for N % 32 != 0 or misaligned buffers, MX_ERR_INVALID_ARG otherwise. */
+int mx_gemm_quantized(const mx_tensor* A, const mx_tensor* B, float extra_alpha, mx_tensor* out, void* stream);
+
 /* Workspace bytes for mx_linear_fwd (pass 0) and mx_linear_bwd (pass 1). */
 size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass);
 

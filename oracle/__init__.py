@@ -88,6 +88,8 @@ def lib():
             L.orc_quantize.restype = i32
             L.orc_quantize.argtypes = [p, i64, i64, i64, i32, i32, i32, i32, i32, u64, u32, i32,
                                        p, p, p, p, p]
+            L.orc_quantize_rows_f32.restype = i32
+            L.orc_quantize_rows_f32.argtypes = [p, i64, i64, i64, i32, p, p]
             L.orc_dequantize.restype = None
             L.orc_dequantize.argtypes = [p, p, i64, i64, i32, i32, p]
             L.orc_gemm_alpha.restype = C.c_float
@@ -216,6 +218,19 @@ def quantize(x_bits: np.ndarray, fmt: str, direction: str = "row", rounding: str
         raise ValueError(f"oracle quantize rejected the arguments (code {rc})")
     tsv = float(ts[0]) if fmt in ("moss", "nvfp4") else None
     return OracleQuant(fmt, rows, k, codes, sf, float(amax[0]), tsv, bool(hadamard))
+
+
+def quantize_rows_f32(x: np.ndarray, fmt: str) -> OracleQuant:
+    """Rowwise MXFP8 / MXFP4 quantization (FLOOR rule, RNE) of an fp32 matrix [R, C]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    R, Cc = x.shape
+    kbytes = Cc // 2 if fmt in FP4 else Cc
+    codes = np.zeros((R, kbytes), dtype=np.uint8)
+    sf = np.zeros((R, Cc // 32), dtype=np.uint8)
+    rc = lib().orc_quantize_rows_f32(_ptr(x), R, Cc, Cc, FMT[fmt], _ptr(codes), _ptr(sf))
+    if rc != 0:
+        raise ValueError(f"oracle quantize_rows_f32 rejected the arguments (code {rc})")
+    return OracleQuant(fmt, R, Cc, codes, sf, 0.0, None, False)
 
 
 def gemm_alpha(ts_a: float | None, ts_b: float | None, extra: float = 1.0) -> float:

@@ -445,6 +445,43 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
     return ORC_OK;
 }
 
+/* Rowwise MX quantization of an fp32 matrix x [R, C] (row stride ld): the
+ * MXFP8 / MXFP4 steps of orc_quantize (FLOOR rule, round-to-nearest-even)
+ * applied to fp32 values instead of bf16 ones: per block of 32 consecutive
+ * elements of a row, e = FLOOR(max|y|), code = cast(fl32(y * 2^-e)), scale byte
+ * e + 127.  This is what a GEMM epilogue that emits the next layer's operand
+ * ([FAF] 格式感知融合的设计思路: the producer writes the consumer's layout)
+ * must produce from its fp32 output.                                        */
+int orc_quantize_rows_f32(const float* x, int64_t R, int64_t C, int64_t ld, int fmt,
+                          uint8_t* codes, uint8_t* sf_logical)
+{
+    if (!x || !codes || !sf_logical || R < 0 || C < 0 || ld < C)
+        return ORC_ERR_ARG;
+    if (fmt != ORC_FMT_MXFP8 && fmt != ORC_FMT_MXFP4)
+        return ORC_ERR_UNSUPPORTED;
+    if (C % 32 != 0)
+        return ORC_ERR_ARG;
+    const int elem = fmt_elem(fmt);
+    const int64_t kblocks = C / 32;
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (r = 0; r < R; ++r) {
+        for (int64_t kb = 0; kb < kblocks; ++kb) {
+            const float* y = x + r * ld + kb * 32;
+            float b = 0.0f;
+            for (int i = 0; i < 32; ++i)
+                if (fabsf(y[i]) > b)
+                    b = fabsf(y[i]);
+            const int e = orc_pow2_exponent(b, ORC_RULE_FLOOR, elem);
+            const float s2 = ldexpf(1.0f, -e);
+            for (int i = 0; i < 32; ++i)
+                put_code(codes, r, kb * 32 + i, C, elem, encode_elem(y[i] * s2, elem, ORC_ROUND_RNE, 0u));
+            sf_logical[r * kblocks + kb] = (uint8_t)(e + 127);
+        }
+    }
+    return ORC_OK;
+}
+
 static double dec_code(const uint8_t* codes, int64_t r, int64_t k, int64_t K, int elem)
 {
     if (elem == ORC_ELEM_E4M3)

@@ -56,6 +56,8 @@ int      orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int d
                       int block, int rounding, int rule, uint64_t seed, uint32_t stream_id,
                       int hadamard, const float* amax_in, uint8_t* codes, uint8_t* sf_logical,
                       float* amax_out, float* tensor_scale_out);
+int      orc_quantize_rows_f32(const float* x, int64_t R, int64_t C, int64_t ld, int fmt,
+                               uint8_t* codes, uint8_t* sf_logical);
 void     orc_dequantize(const uint8_t* codes, const uint8_t* sf_logical, int64_t rows, int64_t k,
                         int fmt, int block, double* out);
 float    orc_gemm_alpha(const float* ts_a, const float* ts_b, float extra);

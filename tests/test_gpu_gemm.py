@@ -6,7 +6,7 @@ import torch
 
 import oracle as orc
 import workloads
-from parity import assert_gemm_close, bits
+from parity import assert_gemm_close, assert_quant_equal, bits
 
 pytestmark = pytest.mark.gpu
 
@@ -137,3 +137,61 @@ def test_pair_kernel_many_tiles_and_tails(mx, fmt):
         ref, cabs = orc.gemm(ra, rb, rows=rows)
         assert_gemm_close(c[torch.as_tensor(rows, device=c.device)], ref, cabs, f"pair {fmt}")
     mx.set_gemm_variant("auto")
+
+
+# ------------------------------------------------ quantized epilogue (next layer)
+@pytest.mark.parametrize("in_fmt", FMTS)
+@pytest.mark.parametrize("out_fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+def test_gemm_quantized_epilogue(mx, in_fmt, out_fmt, variant):
+    """The operand the epilogue writes equals the oracle's rowwise MX quantization
+    of the same kernel's fp32 output, bit for bit: both runs issue the same MMAs
+    in the same order, so the fp32 sums are identical."""
+    mx.set_gemm_variant(variant)
+    M, N, K = 424, 640, 512
+    a = workloads.draw("student_t3", (M, K), 91)
+    b = workloads.draw("normal", (N, K), 92, 0.02)
+    qa, qb, _, _ = quant_pair(mx, a, b, in_fmt)
+    c32 = mx.gemm(qa, qb, extra_alpha=0.75, out_dtype=torch.float32)
+    q = mx.gemm_quantized(qa, qb, out_fmt, extra_alpha=0.75)
+    torch.cuda.synchronize()
+    assert (q.rows, q.k) == (M, N)
+    assert_quant_equal(q, orc.quantize_rows_f32(c32.cpu().numpy(), out_fmt), f"{in_fmt}->{out_fmt} {variant}")
+    mx.set_gemm_variant("auto")
+
+
+@pytest.mark.parametrize("out_fmt", ["mxfp8", "mxfp4"])
+def test_gemm_quantized_many_tiles_feeds_next_gemm(mx, out_fmt):
+    """Pair kernel over many 256 x 256 tiles with a ragged M tail; the result is a
+    valid operand: a second GEMM consuming it matches the oracle GEMM of the
+    oracle-quantized first result."""
+    mx.set_gemm_variant("pair")
+    # N is the next GEMM's K (a multiple of 128 / 256); 1408 leaves a ragged 256-column tile
+    M, N, K = 1280 + 72, (1408 if out_fmt == "mxfp8" else 1792), 512
+    a = workloads.draw("student_t3", (M, K), 93)
+    b = workloads.draw("normal", (N, K), 94, 0.02)
+    qa, qb, _, _ = quant_pair(mx, a, b, "mxfp8")
+    c32 = mx.gemm(qa, qb, out_dtype=torch.float32)
+    q = mx.gemm_quantized(qa, qb, out_fmt)
+    ref = orc.quantize_rows_f32(c32.cpu().numpy(), out_fmt)
+    assert_quant_equal(q, ref, f"many tiles -> {out_fmt}")
+    w2 = workloads.draw("normal", (256, N), 95, 0.02)
+    q2 = mx.quantize(w2.cuda(), out_fmt)
+    r2 = orc.quantize(bits(w2), out_fmt)
+    y = mx.gemm(q, q2)
+    yref, yabs = orc.gemm(ref, r2)
+    assert_gemm_close(y, yref, yabs, "second GEMM on the epilogue operand")
+    mx.set_gemm_variant("auto")
+
+
+def test_gemm_quantized_rejects(mx):
+    x = workloads.draw("normal", (256, 256), 1).cuda()
+    q = mx.quantize(x, "mxfp8")
+    qn = mx.quantize(workloads.draw("normal", (48, 256), 2).cuda(), "mxfp8")  # N = 48: not whole blocks
+    with pytest.raises(mx.MXError) as e:  # the C entry checks N % 32 itself
+        mx.gemm_quantized(q, qn, "mxfp8", out=mx.MXTensor("mxfp8", 256, 64))
+    assert e.value.code == mx.MX_ERR_ALIGNMENT
+    with pytest.raises(mx.MXError) as e:
+        mx.gemm_quantized(q, q, "nvfp4")
+    assert e.value.code == mx.MX_ERR_UNSUPPORTED
+    assert mx.last_device_status() == mx.MX_OK

@@ -386,3 +386,51 @@ def test_gemm_exact_on_small_integers():
         assert np.array_equal(qa.dequantize(), a.double().numpy())
         c, _ = orc.gemm(qa, qb)
         assert np.array_equal(c, exact)
+
+
+# ---------------------------------------- fp32 rowwise MX (GEMM epilogue) ---
+def test_e4m3_rne_matches_torch_float8_on_random_fp32():
+    """The encoder on fp32 values off the bf16 grid (an epilogue quantizes fp32 sums)."""
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.normal(0, 50, 20000), np.exp2(rng.uniform(-12, 9.5, 20000)) *
+                        rng.choice([-1, 1], 20000)]).astype(np.float32)
+    ref = torch.from_numpy(x).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.encode_rne("e4m3", float(v)) for v in x], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_quantize_rows_f32_equals_bf16_quantize_on_bf16_values(fmt):
+    """On values that bf16 holds exactly, the fp32 entry reproduces the pinned
+    bf16 quantizer code for code and scale for scale (every finite bf16 value,
+    shuffled, plus a heavy-tailed matrix)."""
+    pats = workloads.all_bf16_patterns()
+    g = torch.Generator().manual_seed(1)
+    x = torch.zeros(510 * 128, dtype=torch.bfloat16)
+    x[:pats.numel()] = pats[torch.randperm(pats.numel(), generator=g)]
+    for xb in (x.view(510, 128), workloads.draw("outliers", (96, 320), 3)):
+        bits = xb.contiguous().view(torch.int16).numpy().view(np.uint16)
+        a = orc.quantize(bits, fmt)
+        b = orc.quantize_rows_f32(xb.float().numpy(), fmt)
+        assert np.array_equal(a.codes, b.codes) and np.array_equal(a.sf_logical, b.sf_logical)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+def test_quantize_rows_f32_is_nearest_at_the_floor_scale(fmt):
+    """Off the bf16 grid: each block's scale is 2^(floor(log2 max|y|) - emax) and
+    each code decodes to a nearest grid value of y at that scale (brute force)."""
+    elem, emax = ("e4m3", 8) if fmt == "mxfp8" else ("e2m1", 2)
+    rng = np.random.default_rng(4)
+    y = (rng.standard_t(3, (8, 64)) * np.exp2(rng.integers(-20, 20, (8, 1)))).astype(np.float32)
+    q = orc.quantize_rows_f32(y, fmt)
+    deq = q.dequantize()
+    grid = np.array(sorted({orc.decode(elem, c) for c in range(0x7F if elem == "e4m3" else 8)}))
+    for r in range(8):
+        for kb in range(2):
+            blk = y[r, kb * 32:(kb + 1) * 32].astype(np.float64)
+            e = math.floor(math.log2(np.abs(blk).max())) - emax
+            assert q.sf_logical[r, kb] == e + 127
+            s = 2.0 ** e
+            for v, dv in zip(blk, deq[r, kb * 32:(kb + 1) * 32]):
+                a = min(abs(v) / s, grid[-1])
+                assert abs(abs(dv) / s - a) <= np.abs(grid - a).min() + 1e-12
