@@ -174,7 +174,7 @@ def dual_bytes(fmt: str, elems: int, amax_pass: bool) -> float:
     return elems * (2.0 + (2.0 if amax_pass else 0.0) + 2.0 * (CODE_BYTES[fmt] + 1.0 / BLOCK[fmt]))
 
 
-KERNEL_SOURCES = {"gemm": ("gemm.cu", "mx_ptx.cuh"), "quant": ("quantize.cu", "mx_ptx.cuh")}
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "mx_ptx.cuh", "mx_codec.cuh"), "quant": ("quantize.cu", "mx_ptx.cuh", "mx_codec.cuh")}
 
 
 def source_hash(kind: str) -> str:

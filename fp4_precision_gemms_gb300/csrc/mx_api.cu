@@ -129,8 +129,6 @@ int check_direction(int fmt, int rounding, int hadamard)
 {
     if (rounding != MX_ROUND_RNE && rounding != MX_ROUND_SR)
         return MX_ERR_INVALID_ARG;
-    if (rounding == MX_ROUND_SR && !fmt_is_fp4(fmt))
-        return MX_ERR_UNSUPPORTED;
     if (hadamard && !(fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MXFP4_E2M1))
         return MX_ERR_UNSUPPORTED;
     return MX_OK;

@@ -74,6 +74,30 @@ __device__ __forceinline__ uint32_t e2m1_sr(float s, uint32_t u16)
     return sign | (static_cast<float>(u16) < p16 ? code + 1u : code);
 }
 
+// Stochastic rounding onto the E4M3 grid with the same rule (up iff
+// u16 < p * 2^16, p = (|s| - lo) / (hi - lo)), saturating at 448.  lo is |s|
+// with its significand cut to 3 bits (normal range) or a multiple of 2^-9
+// (subnormal range); the step is a power of two, so every operation is exact.
+__device__ __forceinline__ uint32_t e4m3_sr(float s, uint32_t u16)
+{
+    const uint32_t sign = (__float_as_uint(s) >> 31) << 7;
+    const float a = fabsf(s);
+    if (a >= 448.0f)
+        return sign | 0x7Eu;
+    float lo, inv_step;  // inv_step = 2^16 / (hi - lo)
+    if (a < 0x1p-6f) {
+        lo = __fmul_rn(floorf(__fmul_rn(a, 512.0f)), 0x1p-9f);
+        inv_step = 0x1p25f;
+    } else {
+        lo = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);
+        const int e = static_cast<int>((__float_as_uint(lo) >> 23) & 0xFFu) - 127;  // -6 .. 8
+        inv_step = __uint_as_float(static_cast<uint32_t>(127 + 19 - e) << 23);   // 2^(16 - (e - 3))
+    }
+    const uint32_t code = cvt_e4m3x2(lo, 0.0f) & 0x7Fu;  // lo is on the grid
+    const float t = __fmul_rn(__fsub_rn(a, lo), inv_step);
+    return sign | (static_cast<float>(u16) < t ? code + 1u : code);
+}
+
 // ------------------------------------------------------------- Philox4x32-10
 // Salmon et al., SC'11: two 32x32 -> 64 multiplies per round, ten rounds, the
 // key bumped by the Weyl constants between rounds.
@@ -358,9 +382,23 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
         sfbyte = static_cast<uint32_t>(e + 127);
     }
     if constexpr (ELEM == kElemE4M3) {
+        if constexpr (SR) {
 #pragma unroll
-        for (int w = 0; w < N / 4; ++w)
-            out[w] = cvt_e4m3x2(v[4 * w], v[4 * w + 1]) | (cvt_e4m3x2(v[4 * w + 2], v[4 * w + 3]) << 16);
+            for (int g = 0; g < N / 8; ++g) {
+                uint32_t u[8];
+                sr_bits8(seed, sid, L8 + g, u);
+                uint32_t b[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    b[i] = e4m3_sr(v[8 * g + i], u[i]);
+                out[2 * g] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+                out[2 * g + 1] = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+            }
+        } else {
+#pragma unroll
+            for (int w = 0; w < N / 4; ++w)
+                out[w] = cvt_e4m3x2(v[4 * w], v[4 * w + 1]) | (cvt_e4m3x2(v[4 * w + 2], v[4 * w + 3]) << 16);
+        }
     } else {
 #pragma unroll
         for (int w = 0; w < N / 8; ++w) {
@@ -988,23 +1026,17 @@ int launch_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
-// Stochastic rounding exists only for the E2M1 formats; the host rejects it
-// for the others, so only those instantiations are built.
+// Rounding is a compile-time choice per direction.
 template <int FMT, bool DO_ROW, bool DO_COL>
 int launch_tile_sr(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
 {
-    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     const bool rsr = DO_ROW && t.row_sr, csr = DO_COL && t.col_sr;
-    if constexpr (FP4) {
-        if (rsr && csr)
-            return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, DO_COL>(t, ld, d, s);
-        if (rsr)
-            return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, false>(t, ld, d, s);
-        if (csr)
-            return launch_tile<FMT, DO_ROW, DO_COL, false, DO_COL>(t, ld, d, s);
-    }
-    if (rsr || csr)
-        return MX_ERR_UNSUPPORTED;
+    if (rsr && csr)
+        return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, DO_COL>(t, ld, d, s);
+    if (rsr)
+        return launch_tile<FMT, DO_ROW, DO_COL, DO_ROW, false>(t, ld, d, s);
+    if (csr)
+        return launch_tile<FMT, DO_ROW, DO_COL, false, DO_COL>(t, ld, d, s);
     return launch_tile<FMT, DO_ROW, DO_COL, false, false>(t, ld, d, s);
 }
 
@@ -1048,6 +1080,9 @@ int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s)
     const bool had = q.hadamard != 0;
     switch (q.fmt) {
     case MX_FMT_MXFP8_E4M3:
+        if (sr)
+            return had ? launch_q<MX_FMT_MXFP8_E4M3, true, true>(q, d, s)
+                       : launch_q<MX_FMT_MXFP8_E4M3, true, false>(q, d, s);
         return had ? launch_q<MX_FMT_MXFP8_E4M3, false, true>(q, d, s)
                    : launch_q<MX_FMT_MXFP8_E4M3, false, false>(q, d, s);
     case MX_FMT_MXFP4_E2M1:
@@ -1059,7 +1094,7 @@ int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s)
     case MX_FMT_NVFP4:
         return sr ? launch_q<MX_FMT_NVFP4, true, false>(q, d, s) : launch_q<MX_FMT_NVFP4, false, false>(q, d, s);
     case MX_FMT_MOSS_FP8:
-        return launch_q<MX_FMT_MOSS_FP8, false, false>(q, d, s);
+        return sr ? launch_q<MX_FMT_MOSS_FP8, true, false>(q, d, s) : launch_q<MX_FMT_MOSS_FP8, false, false>(q, d, s);
     default:
         return MX_ERR_INVALID_ARG;
     }

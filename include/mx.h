@@ -73,8 +73,9 @@ typedef enum mx_format {
 } mx_format;
 
 /* RNE: round to nearest, ties to even, saturating at the largest finite
- * value.  SR: stochastic rounding ([FAF] 两个关键的数值技巧), E2M1 formats
- * only: element L = r*K + k of the K-major operand rounds up iff u16 < p*2^16,
+ * value.  SR: stochastic rounding ([FAF] 两个关键的数值技巧; the pages attach it
+ * to E2M1, the same rule applies to E4M3, saturating at 448): element
+ * L = r*K + k of the K-major operand rounds up iff u16 < p*2^16,
  * p its distance fraction between the two neighbouring grid points and u16
  * the 16-bit half (L odd: high, even: low) of word (L&7)>>1 of
  * Philox4x32-10(counter = {L>>3, L>>35, stream_id, 0}, key = {seed, seed>>32}). */
@@ -137,7 +138,7 @@ int mx_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, void* 
 /* The fused quantize producer: bf16 x[R, C] (row stride ld elements) ->
  * codes + block scales (+ amax and tensor scale) in *out.
  *   block      32 for MXFP8/MXFP4/MOSS, 16 for NVFP4 (MX_ERR_UNSUPPORTED else).
- *   rounding   MX_ROUND_SR only with E2M1 formats.
+ *   rounding   MX_ROUND_RNE or MX_ROUND_SR (every format).
  *   hadamard   1: multiply every 32-element K-block by the fixed-sign
  *              Sylvester H32 (unnormalised, five fp32 butterfly stages in
  *              the order h = 1, 2, 4, 8, 16) before scaling; MX formats only
@@ -230,7 +231,7 @@ int mx_linear_fwd_noalloc(const void* X, const void* W, int64_t T, int64_t Kin, 
  * gradient, both on the mxfp route). */
 typedef struct mx_bwd_opts {
     int32_t wgrad_hadamard;   /* 1: H32 along tokens on both wgrad operands (MX formats) */
-    int32_t wgrad_dy_rounding;/* mx_rounding for dY^T in wgrad (SR: E2M1 formats) */
+    int32_t wgrad_dy_rounding;/* mx_rounding for dY^T in wgrad */
     uint64_t seed;            /* SR Philox key */
     uint32_t stream_id;       /* SR Philox counter word 2 */
     int32_t reserved;

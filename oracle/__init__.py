@@ -69,6 +69,8 @@ def lib():
                 getattr(L, n).argtypes = [C.c_float]
             L.orc_encode_e2m1_sr.restype = C.c_uint
             L.orc_encode_e2m1_sr.argtypes = [C.c_float, C.c_uint]
+            L.orc_encode_e4m3_sr.restype = C.c_uint
+            L.orc_encode_e4m3_sr.argtypes = [C.c_float, C.c_uint]
             L.orc_pow2_exponent.restype = i32
             L.orc_pow2_exponent.argtypes = [C.c_float, i32, i32]
             L.orc_philox4x32_10.restype = None
@@ -120,6 +122,10 @@ def encode_rne(elem: str, v: float) -> int:
 
 def encode_e2m1_sr(v: float, u16: int) -> int:
     return int(lib().orc_encode_e2m1_sr(float(np.float32(v)), int(u16)))
+
+
+def encode_e4m3_sr(v: float, u16: int) -> int:
+    return int(lib().orc_encode_e4m3_sr(float(np.float32(v)), int(u16)))
 
 
 def pow2_exponent(block_amax: float, rule: str, elem: str) -> int:

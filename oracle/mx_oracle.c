@@ -156,6 +156,28 @@ unsigned orc_encode_e2m1_sr(float v, unsigned u16)
     return s | (((double)(u16 & 0xffffu) < p * 65536.0) ? lo + 1u : lo);
 }
 
+/* Stochastic rounding onto the E4M3 grid: the same rule as E2M1 (round up
+ * iff u16 * 2^-16 < p, p = (|v| - lo) / (hi - lo), lo <= |v| < hi adjacent
+ * grid values, 0 and the subnormals included), saturating at 448.  The pages
+ * attach stochastic rounding to the E2M1 route only ([FAF] 两个关键的数值技巧);
+ * this is the same rule on the E4M3 grid.                                   */
+unsigned orc_encode_e4m3_sr(float v, unsigned u16)
+{
+    unsigned s = signbit(v) ? 0x80u : 0u;
+    double a = fabs((double)v);
+    if (a >= orc_decode_e4m3(0x7eu))
+        return s | 0x7eu;
+    unsigned lo = 0u;
+    for (unsigned c = 0u; c <= 0x7eu; ++c)
+        if (orc_decode_e4m3(c) <= a)
+            lo = c;
+    double glo = orc_decode_e4m3(lo), ghi = orc_decode_e4m3(lo + 1u);
+    if (a == glo)
+        return s | lo;
+    double p = (a - glo) / (ghi - glo);
+    return s | (((double)(u16 & 0xffffu) < p * 65536.0) ? lo + 1u : lo);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Power-of-two block scales ([MOSS] Power-of-Two 的关键优势: dequantising  */
 /* by 2^k is an exact exponent shift).  Returns e so that the block is      */
@@ -311,7 +333,7 @@ static int fmt_block(int fmt) { return fmt == ORC_FMT_NVFP4 ? 16 : 32; }
 static unsigned encode_elem(float s, int elem, int rounding, unsigned u16)
 {
     if (elem == ORC_ELEM_E4M3)
-        return orc_encode_e4m3_rne(s);
+        return rounding == ORC_ROUND_SR ? orc_encode_e4m3_sr(s, u16) : orc_encode_e4m3_rne(s);
     return rounding == ORC_ROUND_SR ? orc_encode_e2m1_sr(s, u16) : orc_encode_e2m1_rne(s);
 }
 
@@ -362,8 +384,6 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
     if (block != fmt_block(fmt))
         return ORC_ERR_UNSUPPORTED;
     const int elem = fmt_elem(fmt);
-    if (rounding == ORC_ROUND_SR && elem != ORC_ELEM_E2M1)
-        return ORC_ERR_UNSUPPORTED;
     if (hadamard && !(fmt == ORC_FMT_MXFP8 || fmt == ORC_FMT_MXFP4))
         return ORC_ERR_UNSUPPORTED;
     if (fmt == ORC_FMT_NVFP4 && rule != ORC_RULE_DEFAULT)

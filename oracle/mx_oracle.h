@@ -41,6 +41,7 @@ double   orc_decode_e8m0(unsigned code);
 unsigned orc_encode_e4m3_rne(float v);
 unsigned orc_encode_e2m1_rne(float v);
 unsigned orc_encode_e2m1_sr(float v, unsigned u16);
+unsigned orc_encode_e4m3_sr(float v, unsigned u16);
 int      orc_pow2_exponent(float block_amax, int rule, int elem);
 
 void     orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);

@@ -72,3 +72,18 @@ def test_workspace_too_small(mx):
     with pytest.raises(mx.MXError) as e:
         mx.linear_fwd(X, W, "mxfp8", workspace=ws)
     assert e.value.code == mx.MX_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "moss"])
+def test_e4m3_wgrad_stochastic_rounding(mx, fmt):
+    """E4M3 formats take SR on the weight gradient's dY^T too (same Philox stream)."""
+    T, Kin, Nout = 512, 256, 384
+    X = workloads.draw("normal", (T, Kin), 86)
+    W = workloads.draw("normal", (Nout, Kin), 87, 0.02)
+    dY = workloads.draw("student_t3", (T, Nout), 88, 1e-3)
+    _, dW = mx.linear_bwd(dY.cuda(), X.cuda(), W.cuda(), fmt, wgrad_dy_rounding="sr", seed=9, stream_id=2,
+                          need_dx=False)
+    ra = orc.quantize(bits(dY), fmt, "col", rounding="sr", seed=9, stream_id=2)
+    rb = orc.quantize(bits(X), fmt, "col")
+    ref, cabs = orc.gemm(ra, rb)
+    assert_gemm_close(dW, ref, cabs, f"wgrad {fmt} SR")

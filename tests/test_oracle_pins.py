@@ -333,8 +333,6 @@ def test_nvfp4_scales():
 def test_quantize_rejects_unsupported():
     x = _bits(workloads.draw("normal", (32, 32), 1))
     with pytest.raises(ValueError):
-        orc.quantize(x, "mxfp8", rounding="sr")
-    with pytest.raises(ValueError):
         orc.quantize(x, "nvfp4", hadamard=True)
     with pytest.raises(ValueError):
         orc.quantize(_bits(workloads.draw("normal", (32, 24), 1)), "mxfp8")
@@ -434,3 +432,60 @@ def test_quantize_rows_f32_is_nearest_at_the_floor_scale(fmt):
             for v, dv in zip(blk, deq[r, kb * 32:(kb + 1) * 32]):
                 a = min(abs(v) / s, grid[-1])
                 assert abs(abs(dv) / s - a) <= np.abs(grid - a).min() + 1e-12
+
+
+# ------------------------------------------------- E4M3 stochastic rounding ---
+def test_e4m3_sr_unbiased_and_probability():
+    """E4M3 SR rounds |v| up to the next grid value with probability
+    (|v| - lo) / (hi - lo): the empirical frequency and mean over uniform u16
+    match, in every binade, the subnormals and at saturation."""
+    grid = sorted({orc.decode("e4m3", c) for c in range(0x7F)})
+    rng = np.random.default_rng(12)
+    for v in [1e-4, 0.0029, 0.013, 0.9, 1.0625, 3.3, 17.0, 100.5, 300.0, 447.0, -6.1, -0.3]:
+        n = 4000
+        us = rng.integers(0, 65536, n)
+        dec = np.array([orc.decode("e4m3", orc.encode_e4m3_sr(v, int(u))) for u in us])
+        a = abs(v)
+        lo = max(g for g in grid if g <= a)
+        hi = min(g for g in grid if g > a)
+        p = (a - lo) / (hi - lo)
+        assert set(np.abs(dec)) <= {lo, hi}
+        assert np.all(np.sign(dec[dec != 0]) == np.sign(v))
+        frac_up = np.mean(np.abs(dec) == hi)
+        assert abs(frac_up - p) < 4 * math.sqrt(p * (1 - p) / n) + 1e-3
+        sd = (hi - lo) * math.sqrt(p * (1 - p) / n)
+        assert abs(dec.mean() - v) < 4 * sd + 1e-6
+    for g in grid[::7] + [448.0]:
+        for u in (0, 65535):
+            assert orc.decode("e4m3", orc.encode_e4m3_sr(g, u)) == g
+    assert orc.decode("e4m3", orc.encode_e4m3_sr(1000.0, 0)) == 448.0
+    # exact threshold: halfway between 1.0 and 1.125 rounds up iff u16 < 32768
+    assert orc.encode_e4m3_sr(1.0625, 32767) == 0x39 and orc.encode_e4m3_sr(1.0625, 32768) == 0x38
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "moss"])
+def test_e4m3_sr_quantize_is_unbiased_at_the_chosen_scale(fmt):
+    """Quantize with SR: per element the code is one of the two grid neighbours
+    of the scaled value (the RNE result's scale), and averaged over seeds the
+    dequantized tensor approaches the scaled input."""
+    x = workloads.draw("student_t3", (32, 64), 21)
+    xb = _bits(x)
+    rne = orc.quantize(xb, fmt)
+    acc = np.zeros((32, 64))
+    n = 64
+    for seed in range(n):
+        q = orc.quantize(xb, fmt, rounding="sr", seed=seed)
+        assert np.array_equal(q.sf_logical, rne.sf_logical)
+        acc += q.dequantize()  # code x block scale (the tensor scale is applied in the GEMM epilogue)
+    y = x.double().numpy()
+    if fmt == "moss":
+        y = (x.float() / np.float32(rne.tensor_scale)).double().numpy()
+    grid = np.array(sorted({orc.decode("e4m3", c) for c in range(0x7F)}))
+    s = np.repeat(np.exp2(rne.sf_logical.astype(np.float64) - 127), 32, axis=1)
+    a = np.minimum(np.abs(y) / s, 448.0)
+    hi = grid[np.minimum(np.searchsorted(grid, a, side="right"), len(grid) - 1)]
+    lo = grid[np.maximum(np.searchsorted(grid, a, side="right") - 1, 0)]
+    bound = 5 * s * (hi - lo) / (2 * math.sqrt(n)) + 1e-12
+    sat = np.abs(y) / s >= 448.0  # the FLOOR rule lets a block max land in (448, 512): it saturates
+    assert np.all(np.abs(acc / n - y)[~sat] <= bound[~sat])
+    assert np.allclose(np.abs(acc / n)[sat], 448.0 * s[sat])
