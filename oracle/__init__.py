@@ -23,13 +23,14 @@ _SRC = os.path.join(_HERE, "mx_oracle.c")
 _LIB = os.path.join(_HERE, "liborc.so")
 
 # Oracle-private enum values (mirror mx_oracle.h).
-FMT = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3}
+FMT = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3, "nvfp4_local": 4}
+LOCAL_REGION = 128  # operand rows per FP32 scale in nvfp4_local
 ROUND = {"rne": 0, "sr": 1}
 RULE = {"default": 0, "floor": 1, "ceil": 2, "nearest": 3}
 DIR = {"row": 0, "col": 1}
 ELEM = {"e4m3": 0, "e2m1": 1}
-BLOCK = {"mxfp8": 32, "mxfp4": 32, "nvfp4": 16, "moss": 32}
-FP4 = {"mxfp4", "nvfp4"}
+BLOCK = {"mxfp8": 32, "mxfp4": 32, "nvfp4": 16, "moss": 32, "nvfp4_local": 16}
+FP4 = {"mxfp4", "nvfp4", "nvfp4_local"}
 
 _lock = threading.Lock()
 _lib = None
@@ -214,14 +215,17 @@ def quantize(x_bits: np.ndarray, fmt: str, direction: str = "row", rounding: str
     kbytes = k // 2 if fmt in FP4 else k
     codes = np.zeros((rows, kbytes), dtype=np.uint8)
     sf = np.zeros((rows, k // block), dtype=np.uint8)
-    amax = np.zeros(1, dtype=np.float32)
-    ts = np.ones(1, dtype=np.float32)
-    ain = None if amax_in is None else np.array([amax_in], dtype=np.float32)
+    nreg = max(1, -(-rows // LOCAL_REGION)) if fmt == "nvfp4_local" else 1
+    amax = np.zeros(nreg, dtype=np.float32)
+    ts = np.ones(nreg, dtype=np.float32)
+    ain = None if amax_in is None else np.atleast_1d(np.asarray(amax_in, dtype=np.float32))
     rc = lib().orc_quantize(_ptr(x), R, Cc, Cc, DIR[direction], FMT[fmt], block, ROUND[rounding],
                             RULE[rule], seed, stream_id, int(bool(hadamard)), _ptr(ain),
                             _ptr(codes), _ptr(sf), _ptr(amax), _ptr(ts))
     if rc != 0:
         raise ValueError(f"oracle quantize rejected the arguments (code {rc})")
+    if fmt == "nvfp4_local":  # one FP32 scale per region of LOCAL_REGION operand rows
+        return OracleQuant(fmt, rows, k, codes, sf, amax.copy(), ts.copy(), bool(hadamard))
     tsv = float(ts[0]) if fmt in ("moss", "nvfp4") else None
     return OracleQuant(fmt, rows, k, codes, sf, float(amax[0]), tsv, bool(hadamard))
 
@@ -248,6 +252,20 @@ def gemm_alpha(ts_a: float | None, ts_b: float | None, extra: float = 1.0) -> fl
 def gemm(A: OracleQuant, B: OracleQuant, extra_alpha: float = 1.0, rows=None, cols=None):
     """fp64 C = alpha * dq(A) dq(B)^T over the selected rows/cols; returns (C, Cabs)."""
     assert A.fmt == B.fmt and A.k == B.k
+    if A.fmt == "nvfp4_local":
+        # alpha varies with the region pair (row // LOCAL_REGION, col // LOCAL_REGION): the
+        # scales are constant along K, so they factor out of each output's K-sum
+        r = np.arange(A.rows) if rows is None else np.asarray(rows, dtype=np.int64)
+        c = np.arange(B.rows) if cols is None else np.asarray(cols, dtype=np.int64)
+        # the same codes and block scales read as NVFP4 without a tensor scale (alpha 1)
+        ones = OracleQuant("nvfp4", A.rows, A.k, A.codes, A.sf_logical, 0.0, None, A.hadamard)
+        onesb = OracleQuant("nvfp4", B.rows, B.k, B.codes, B.sf_logical, 0.0, None, B.hadamard)
+        c1, a1 = gemm(ones, onesb, 1.0, r, c)
+        al = np.array([[gemm_alpha(float(A.tensor_scale[i // LOCAL_REGION]), float(B.tensor_scale[j // LOCAL_REGION]),
+                                   extra_alpha) for j in range(0, B.rows, LOCAL_REGION)]
+                       for i in range(0, A.rows, LOCAL_REGION)], dtype=np.float64)
+        alpha = al[np.ix_(r // LOCAL_REGION, c // LOCAL_REGION)]
+        return alpha * c1, np.abs(alpha) * a1
     alpha = gemm_alpha(A.tensor_scale, B.tensor_scale, extra_alpha)
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     c = None if cols is None else np.ascontiguousarray(cols, dtype=np.int64)

@@ -328,7 +328,8 @@ static int fmt_elem(int fmt)
     return (fmt == ORC_FMT_MXFP8 || fmt == ORC_FMT_MOSS) ? ORC_ELEM_E4M3 : ORC_ELEM_E2M1;
 }
 
-static int fmt_block(int fmt) { return fmt == ORC_FMT_NVFP4 ? 16 : 32; }
+static int fmt_block(int fmt) { return (fmt == ORC_FMT_NVFP4 || fmt == ORC_FMT_NVFP4_LOCAL) ? 16 : 32; }
+static int fmt_is_nvfp4(int fmt) { return fmt == ORC_FMT_NVFP4 || fmt == ORC_FMT_NVFP4_LOCAL; }
 
 static unsigned encode_elem(float s, int elem, int rounding, unsigned u16)
 {
@@ -379,14 +380,14 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
 {
     if (!x || !codes || !sf_logical || R < 0 || C < 0 || ld < C)
         return ORC_ERR_ARG;
-    if (fmt < ORC_FMT_MXFP8 || fmt > ORC_FMT_MOSS || (dir != ORC_ROWWISE && dir != ORC_COLWISE))
+    if (fmt < ORC_FMT_MXFP8 || fmt > ORC_FMT_NVFP4_LOCAL || (dir != ORC_ROWWISE && dir != ORC_COLWISE))
         return ORC_ERR_ARG;
     if (block != fmt_block(fmt))
         return ORC_ERR_UNSUPPORTED;
     const int elem = fmt_elem(fmt);
     if (hadamard && !(fmt == ORC_FMT_MXFP8 || fmt == ORC_FMT_MXFP4))
         return ORC_ERR_UNSUPPORTED;
-    if (fmt == ORC_FMT_NVFP4 && rule != ORC_RULE_DEFAULT)
+    if (fmt_is_nvfp4(fmt) && rule != ORC_RULE_DEFAULT)
         return ORC_ERR_UNSUPPORTED; /* NVFP4 block scales are E4M3, not powers of two */
     if (rule == ORC_RULE_DEFAULT)
         rule = (fmt == ORC_FMT_MOSS) ? ORC_RULE_CEIL : ORC_RULE_FLOOR;
@@ -396,20 +397,51 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
         return ORC_ERR_ARG;
     const int64_t kblocks = K / block;
 
-    float amax = 0.0f;
-    if (fmt == ORC_FMT_MOSS || fmt == ORC_FMT_NVFP4 || amax_out) {
-        amax = amax_in ? *amax_in : orc_amax_bf16(x, R, C, ld);
+    /* Tensor scales.  One per tensor, except ORC_FMT_NVFP4_LOCAL: one per
+     * region of ORC_LOCAL_REGION consecutive operand rows (all of K), the
+     * scale domain of the producer that writes that region ([FAF]
+     * 格式感知融合的设计思路: "CTA-local" nvfp), amax and tensor scale then
+     * being arrays of ceil(rows / ORC_LOCAL_REGION) entries.                 */
+    const int local = fmt == ORC_FMT_NVFP4_LOCAL;
+    const int64_t nreg = local ? (rows + ORC_LOCAL_REGION - 1) / ORC_LOCAL_REGION : 1;
+    float* amaxv = (float*)calloc((size_t)(nreg > 0 ? nreg : 1), sizeof(float));
+    float* tsv = (float*)malloc(sizeof(float) * (size_t)(nreg > 0 ? nreg : 1));
+    if (!amaxv || !tsv) {
+        free(amaxv);
+        free(tsv);
+        return ORC_ERR_ARG;
     }
-    float ts = 1.0f;
-    if (fmt == ORC_FMT_MOSS && amax != 0.0f)
-        ts = amax / 448.0f;
-    if (fmt == ORC_FMT_NVFP4 && amax != 0.0f)
-        ts = amax / 2688.0f;
-    if (amax_out)
-        *amax_out = amax;
-    if (tensor_scale_out && (fmt == ORC_FMT_MOSS || fmt == ORC_FMT_NVFP4))
-        *tensor_scale_out = ts;
-    const float nv_denom = 6.0f * ts;
+    if (local) {
+        for (int64_t g = 0; g < nreg; ++g) {
+            if (amax_in) {
+                amaxv[g] = amax_in[g];
+                continue;
+            }
+            float m = 0.0f;
+            const int64_t r1 = (g + 1) * ORC_LOCAL_REGION < rows ? (g + 1) * ORC_LOCAL_REGION : rows;
+            for (int64_t rr = g * ORC_LOCAL_REGION; rr < r1; ++rr)
+                for (int64_t k = 0; k < K; ++k) {
+                    float v = fabsf(orc_bf16_to_f32((dir == ORC_ROWWISE) ? x[rr * ld + k] : x[k * ld + rr]));
+                    if (v > m)
+                        m = v;
+                }
+            amaxv[g] = m;
+        }
+    } else if (fmt == ORC_FMT_MOSS || fmt == ORC_FMT_NVFP4 || amax_out) {
+        amaxv[0] = amax_in ? *amax_in : orc_amax_bf16(x, R, C, ld);
+    }
+    for (int64_t g = 0; g < (nreg > 0 ? nreg : 1); ++g) {
+        float ts = 1.0f;
+        if (fmt == ORC_FMT_MOSS && amaxv[g] != 0.0f)
+            ts = amaxv[g] / 448.0f;
+        if (fmt_is_nvfp4(fmt) && amaxv[g] != 0.0f)
+            ts = amaxv[g] / 2688.0f;
+        tsv[g] = ts;
+        if (amax_out && (local || g == 0))
+            amax_out[g] = amaxv[g];
+        if (tensor_scale_out && (fmt == ORC_FMT_MOSS || fmt_is_nvfp4(fmt)) && (local || g == 0))
+            tensor_scale_out[g] = ts;
+    }
 
     int64_t r;
 #pragma omp parallel for schedule(dynamic, 16)
@@ -424,6 +456,8 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
             }
             if (hadamard)
                 orc_fwht32(y);
+            const float ts = tsv[local ? r / ORC_LOCAL_REGION : 0];
+            const float nv_denom = 6.0f * ts;
             if (fmt == ORC_FMT_MOSS)
                 for (int i = 0; i < block; ++i)
                     y[i] = y[i] / ts;
@@ -432,7 +466,7 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
                 if (fabsf(y[i]) > b)
                     b = fabsf(y[i]);
             uint8_t sfb;
-            if (fmt == ORC_FMT_NVFP4) {
+            if (fmt_is_nvfp4(fmt)) {
                 unsigned sb = orc_encode_e4m3_rne(b / nv_denom); /* b >= 0: sign bit 0 */
                 float d = (float)orc_decode_e4m3(sb) * ts;
                 for (int i = 0; i < block; ++i) {
@@ -462,6 +496,8 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
             sf_logical[r * kblocks + kb] = sfb;
         }
     }
+    free(amaxv);
+    free(tsv);
     return ORC_OK;
 }
 
@@ -512,7 +548,7 @@ static double dec_code(const uint8_t* codes, int64_t r, int64_t k, int64_t K, in
 
 static double dec_sf(uint8_t s, int fmt)
 {
-    return fmt == ORC_FMT_NVFP4 ? orc_decode_e4m3(s) : orc_decode_e8m0(s);
+    return fmt_is_nvfp4(fmt) ? orc_decode_e4m3(s) : orc_decode_e8m0(s);
 }
 
 /* out[r, k] = dec(code) * dec(block scale), exact in fp64 (no tensor scale). */

@@ -25,7 +25,9 @@ extern "C" {
 #endif
 
 /* Oracle-private enums (deliberately separate from the library's). */
-enum { ORC_FMT_MXFP8 = 0, ORC_FMT_MXFP4 = 1, ORC_FMT_NVFP4 = 2, ORC_FMT_MOSS = 3 };
+enum { ORC_FMT_MXFP8 = 0, ORC_FMT_MXFP4 = 1, ORC_FMT_NVFP4 = 2, ORC_FMT_MOSS = 3, ORC_FMT_NVFP4_LOCAL = 4 };
+/* Rows of the K-major operand that share one FP32 scale in ORC_FMT_NVFP4_LOCAL. */
+enum { ORC_LOCAL_REGION = 128 };
 enum { ORC_ROUND_RNE = 0, ORC_ROUND_SR = 1 };
 enum { ORC_RULE_DEFAULT = 0, ORC_RULE_FLOOR = 1, ORC_RULE_CEIL = 2, ORC_RULE_NEAREST = 3 };
 enum { ORC_ROWWISE = 0, ORC_COLWISE = 1 };

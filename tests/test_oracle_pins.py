@@ -489,3 +489,42 @@ def test_e4m3_sr_quantize_is_unbiased_at_the_chosen_scale(fmt):
     sat = np.abs(y) / s >= 448.0  # the FLOOR rule lets a block max land in (448, 512): it saturates
     assert np.all(np.abs(acc / n - y)[~sat] <= bound[~sat])
     assert np.allclose(np.abs(acc / n)[sat], 448.0 * s[sat])
+
+
+# ------------------------------------------------ CTA-local NVFP4 (regions) ---
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_nvfp4_local_is_global_nvfp4_per_region(direction):
+    """nvfp4_local = the pinned global NVFP4 quantizer applied to each region of
+    128 operand rows on its own (last region ragged), codes, scales, amax and
+    tensor scale alike."""
+    x = workloads.draw("lognormal_cols", (320, 416), 7)
+    xb = _bits(x)
+    q = orc.quantize(xb, "nvfp4_local", direction)
+    rows = q.rows
+    assert q.tensor_scale.shape == (-(-rows // 128),)
+    for g in range(q.tensor_scale.shape[0]):
+        sl = slice(128 * g, min(128 * (g + 1), rows))
+        part = xb[sl] if direction == "row" else np.ascontiguousarray(xb[:, sl])
+        ref = orc.quantize(part, "nvfp4", direction)
+        assert np.array_equal(ref.codes, q.codes[sl]) and np.array_equal(ref.sf_logical, q.sf_logical[sl])
+        assert np.float32(ref.amax) == q.amax[g] and np.float32(ref.tensor_scale) == q.tensor_scale[g]
+    # a caller's per-region amax replaces the computed one
+    ain = q.amax * 2
+    q2 = orc.quantize(xb, "nvfp4_local", direction, amax_in=ain)
+    assert np.array_equal(q2.amax, ain.astype(np.float32))
+    part = xb[:128] if direction == "row" else np.ascontiguousarray(xb[:, :128])
+    ref = orc.quantize(part, "nvfp4", direction, amax_in=float(ain[0]))
+    assert np.array_equal(ref.codes, q2.codes[:128])
+
+
+def test_nvfp4_local_gemm_matches_numpy_with_region_scales():
+    """Region scales are constant along K, so they factor out of each output:
+    C[i, j] = s_A[i // 128] s_B[j // 128] sum_k dq(A)[i, k] dq(B)[j, k]."""
+    a = workloads.draw("student_t3", (300, 256), 8)
+    b = workloads.draw("normal", (260, 256), 9, 0.02)
+    qa, qb = orc.quantize(_bits(a), "nvfp4_local"), orc.quantize(_bits(b), "nvfp4_local")
+    c, _ = orc.gemm(qa, qb, extra_alpha=0.5)
+    ta = np.repeat(qa.tensor_scale.astype(np.float64), 128)[:300]
+    tb = np.repeat(qb.tensor_scale.astype(np.float64), 128)[:260]
+    ref = (qa.dequantize() * ta[:, None]) @ (qb.dequantize() * tb[:, None]).T * 0.5
+    assert np.allclose(c, ref, rtol=1e-6, atol=0)
