@@ -17,9 +17,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmx_gb300.so")
 
-FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3}
-BLOCK = {"mxfp8": 32, "mxfp4": 32, "nvfp4": 16, "moss": 32}
-FP4 = ("mxfp4", "nvfp4")
+FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2, "moss": 3, "nvfp4_local": 4}
+BLOCK = {"mxfp8": 32, "mxfp4": 32, "nvfp4": 16, "moss": 32, "nvfp4_local": 16}
+FP4 = ("mxfp4", "nvfp4", "nvfp4_local")
 ROUNDING = {"rne": 0, "sr": 1}
 RULES = {"default": 0, "floor": 1, "ceil": 2, "nearest": 3}
 DIRS = {"row": 0, "col": 1}
@@ -28,7 +28,7 @@ OUT = {torch.float32: 0, torch.bfloat16: 1}
 MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
 MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
-EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
+EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_scale_count", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
             "mx_gemm_quantized",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
@@ -77,6 +77,8 @@ def lib():
             L.mx_codes_bytes.argtypes = [i32, i64, i64]
             L.mx_sf_bytes.restype = sz
             L.mx_sf_bytes.argtypes = [i32, i64, i64]
+            L.mx_scale_count.restype = sz
+            L.mx_scale_count.argtypes = [i32, i64]
             L.mx_amax.restype = i32
             L.mx_amax.argtypes = [p, i64, i64, i64, p, p]
             L.mx_quantize.restype = i32
@@ -168,22 +170,24 @@ class MXTensor:
         kb = self.k // 2 if fmt in FP4 else self.k
         self.codes = torch.empty((self.rows, kb), dtype=torch.uint8, device=device)
         self.sf = torch.empty(max(ns, 1), dtype=torch.uint8, device=device)
-        self.scalars = torch.zeros(2, dtype=torch.float32, device=device)  # amax, tensor scale
+        # amax and tensor scale: one each, or one per 128-row region (nvfp4_local)
+        self.nscale = max(1, int(L.mx_scale_count(FORMATS[fmt], self.rows)))
+        self.scalars = torch.zeros(2 * self.nscale, dtype=torch.float32, device=device)
 
     @property
     def amax(self):
-        return self.scalars[0:1]
+        return self.scalars[0:self.nscale]
 
     @property
     def tensor_scale(self):
-        return self.scalars[1:2]
+        return self.scalars[self.nscale:2 * self.nscale]
 
     def _c(self) -> _CTensor:
         t = _CTensor()
         t.codes = self.codes.data_ptr()
         t.sf = self.sf.data_ptr()
         t.amax = self.scalars.data_ptr()
-        t.tensor_scale = self.scalars.data_ptr() + 4
+        t.tensor_scale = self.scalars.data_ptr() + 4 * self.nscale
         t.rows, t.k = self.rows, self.k
         t.fmt, t.block, t.hadamard = FORMATS[self.fmt], self.block, int(self.hadamard)
         return t

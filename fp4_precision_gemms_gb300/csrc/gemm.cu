@@ -154,6 +154,14 @@ __device__ __forceinline__ void store_chunk(int mode, void* c, int64_t ldc, uint
     }
 }
 
+// The epilogue factor of output (row, col) when the tensor scales are per
+// region of 128 operand rows (NVFP4_LOCAL): fl32(fl32(sA * sB) * extra), the
+// same product order as the global alpha; constant over a 32-column chunk.
+__device__ __forceinline__ float region_alpha(const float* tsa, const float* tsb, float extra, int row, int col0)
+{
+    return __fmul_rn(__fmul_rn(tsa[row >> 7], tsb[col0 >> 7]), extra);
+}
+
 struct GemmParams {
     const uint8_t* sfa;
     const uint8_t* sfb;
@@ -164,6 +172,7 @@ struct GemmParams {
     int64_t ldc;
     int M, N, K;
     int out_mode;     // an EpiMode
+    int ts_region;    // tsa / tsb are per-128-row arrays (NVFP4_LOCAL)
     uint8_t* q_sf;    // scale bytes of a quantized output (EPI_MXFP8 / EPI_MXFP4)
     int64_t q_kgroups;
     int64_t kgroups;  // 4-block SF groups along K (same for A and B)
@@ -320,10 +329,11 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld_wait();
                 const int col0 = n_tile * BN + j * 32;
                 if (row < p.M && col0 < p.N) {
+                    const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+                        v[i] = __fmul_rn(__uint_as_float(r[i]), al);
                     store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
@@ -403,6 +413,7 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.out_mode = out_mode;
+    p.ts_region = fmt_is_local(A->fmt) ? 1 : 0;
     p.q_sf = q_sf;
     p.q_kgroups = sf_kgroups(N / 32);
     p.kgroups = sf_kgroups(K / G::BLOCK);
@@ -492,6 +503,7 @@ struct PairParams {
     int64_t ldc;
     int M, N, K;
     int out_mode;
+    int ts_region;
     uint8_t* q_sf;
     int64_t q_kgroups;
     int64_t kgroups;
@@ -735,10 +747,11 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
                     const int col0 = nt * 256 + half * 128 + j * 32;
                     if (col0 >= p.N)
                         break;
+                    const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), alpha);
+                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
                     store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
@@ -818,6 +831,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.out_mode = out_mode;
+    p.ts_region = fmt_is_local(A->fmt) ? 1 : 0;
     p.q_sf = q_sf;
     p.q_kgroups = sf_kgroups(N / 32);
     p.kgroups = sf_kgroups(K / G::BLOCK);
@@ -866,7 +880,7 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
     g_last_variant = v;
     const int kind = (A->fmt == MX_FMT_MXFP8_E4M3 || A->fmt == MX_FMT_MOSS_FP8) ? 0
                    : A->fmt == MX_FMT_MXFP4_E2M1                                ? 1
-                   : A->fmt == MX_FMT_NVFP4                                     ? 2
+                   : fmt_is_nvfp4(A->fmt)                                       ? 2
                                                                                 : -1;
     if (kind < 0)
         return MX_ERR_INVALID_ARG;

@@ -61,7 +61,7 @@ namespace {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool valid_fmt(int fmt) { return fmt >= MX_FMT_MXFP8_E4M3 && fmt <= MX_FMT_MOSS_FP8; }
+bool valid_fmt(int fmt) { return fmt >= MX_FMT_MXFP8_E4M3 && fmt <= MX_FMT_NVFP4_LOCAL; }
 
 int64_t codes_row_bytes(int fmt, int64_t k) { return fmt_is_fp4(fmt) ? k / 2 : k; }
 
@@ -92,14 +92,15 @@ size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
     size_t off = 0;
     const size_t cb = round_up(mx_codes_bytes(fmt, rows, k), 256);
     const size_t sb = round_up(mx_sf_bytes(fmt, rows, k), 256);
+    const size_t nb = round_up(sizeof(float) * std::max<int64_t>(scale_count(fmt, rows), 1), 128);
     if (t) {
         std::memset(t, 0, sizeof *t);
         t->codes = ws ? ws + off : nullptr;
         t->sf = ws ? ws + off + cb : nullptr;
         t->amax = ws ? reinterpret_cast<float*>(ws + off + cb + sb) : nullptr;
-        t->tensor_scale = ws ? reinterpret_cast<float*>(ws + off + cb + sb + 16) : nullptr;
+        t->tensor_scale = ws ? reinterpret_cast<float*>(ws + off + cb + sb + nb) : nullptr;
     }
-    off += cb + sb + 256;
+    off += cb + sb + 2 * nb;
     return off;
 }
 
@@ -157,9 +158,22 @@ void fill_meta(mx_tensor* out, int64_t rows, int64_t k, int fmt, int hadamard)
 }
 
 // Makes out->amax hold max|x| (copied from amax_in or reduced from x).
-int prepare_amax(const void* x, int64_t R, int64_t C, int64_t ld, const float* amax_in, mx_tensor* out,
+int prepare_amax(const void* x, int64_t R, int64_t C, int64_t ld, const float* amax_in, mx_tensor* out, int dir,
                  const Device& d, cudaStream_t s)
 {
+    if (fmt_is_local(out->fmt)) {  // region maxima of the operand's rows, then the scales
+        const int64_t n = scale_count(out->fmt, out->rows);
+        int rc = MX_OK;
+        if (amax_in) {
+            if (amax_in != out->amax && cudaMemcpyAsync(out->amax, amax_in, sizeof(float) * n,
+                                                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+                return MX_ERR_CUDA;
+        } else {
+            const bool rowwise = dir == MX_ROWWISE;
+            rc = launch_region_amax(x, R, C, ld, rowwise ? out->amax : nullptr, rowwise ? nullptr : out->amax, d, s);
+        }
+        return rc != MX_OK ? rc : launch_local_scales(out->amax, out->tensor_scale, n, d, s);
+    }
     if (amax_in) {
         if (amax_in != out->amax &&
             cudaMemcpyAsync(out->amax, amax_in, sizeof(float), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -197,11 +211,12 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
     fill_meta(out, rows, k, fmt, hadamard);
     const bool ts = fmt_has_tensor_scale(fmt);
-    if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, out, d, s)) != MX_OK)
+    if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, out, dir, d, s)) != MX_OK)
         return rc;
     if (R == 0 || C == 0)
-        return ts ? set_unit_scale(out, s) : MX_OK;
-    const bool tile = g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE);
+        return (ts && !fmt_is_local(fmt)) ? set_unit_scale(out, s) : MX_OK;
+    // the direct producers have no region scales: NVFP4_LOCAL always takes the tile producer
+    const bool tile = g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE) || fmt_is_local(fmt);
     if (tile) {
         TileArgs t = {};
         t.x = x;
@@ -213,6 +228,7 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         t.stream_id = stream_id;
         t.amax = out->amax;
         t.tensor_scale = out->tensor_scale;
+        (dir == MX_ROWWISE ? t.row_ts_v : t.col_ts_v) = out->tensor_scale;
         uint8_t* codes = static_cast<uint8_t*>(out->codes);
         if (dir == MX_ROWWISE) {
             t.row_codes = codes;
@@ -271,8 +287,20 @@ int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt,
     fill_meta(row_out, R, C, fmt, row_hadamard);
     fill_meta(col_out, C, R, fmt, col_hadamard);
     const bool ts = fmt_has_tensor_scale(fmt);
-    if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, row_out, d, s)) != MX_OK)
+    if (fmt_is_local(fmt)) {
+        // row regions of x for the rowwise operand, column regions for the colwise one,
+        // both from one pass over x
+        if (amax_in)
+            return MX_ERR_UNSUPPORTED;
+        if ((rc = launch_region_amax(x, R, C, ld, row_out->amax, col_out->amax, d, s)) != MX_OK ||
+            (rc = launch_local_scales(row_out->amax, row_out->tensor_scale, scale_count(fmt, R), d, s)) != MX_OK ||
+            (rc = launch_local_scales(col_out->amax, col_out->tensor_scale, scale_count(fmt, C), d, s)) != MX_OK)
+            return rc;
+        if (R == 0 || C == 0)
+            return MX_OK;
+    } else if (ts && (rc = prepare_amax(x, R, C, ld, amax_in, row_out, MX_ROWWISE, d, s)) != MX_OK) {
         return rc;
+    }
     if (R == 0 || C == 0) {
         if (!ts)
             return MX_OK;
@@ -292,10 +320,12 @@ int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt,
     t.stream_id = stream_id;
     t.amax = row_out->amax;
     t.tensor_scale = row_out->tensor_scale;
-    if (ts) {
+    if (ts && !fmt_is_local(fmt)) {
         t.amax_copy = col_out->amax;
         t.tensor_scale_copy = col_out->tensor_scale;
     }
+    t.row_ts_v = row_out->tensor_scale;
+    t.col_ts_v = col_out->tensor_scale;
     t.row_codes = static_cast<uint8_t*>(row_out->codes);
     t.row_sf = row_out->sf;
     t.row_sr = row_rounding == MX_ROUND_SR;
@@ -457,6 +487,11 @@ int mx_gemm_quantized(const mx_tensor* A, const mx_tensor* B, float extra_alpha,
     if (rc != MX_OK)
         return rc;
     return gemm_quantized_impl(A, B, extra_alpha, out, d, static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_scale_count(int fmt, int64_t rows)
+{
+    return valid_fmt(fmt) && rows >= 0 ? static_cast<size_t>(scale_count(fmt, rows)) : 0;
 }
 
 size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass)

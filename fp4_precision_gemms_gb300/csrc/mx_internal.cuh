@@ -9,9 +9,16 @@
 namespace mx {
 
 // Element encodings and block sizes per format.
-__host__ __device__ constexpr bool fmt_is_fp4(int fmt) { return fmt == MX_FMT_MXFP4_E2M1 || fmt == MX_FMT_NVFP4; }
-__host__ __device__ constexpr int fmt_block(int fmt) { return fmt == MX_FMT_NVFP4 ? 16 : 32; }
-__host__ __device__ constexpr bool fmt_has_tensor_scale(int fmt) { return fmt == MX_FMT_NVFP4 || fmt == MX_FMT_MOSS_FP8; }
+__host__ __device__ constexpr bool fmt_is_nvfp4(int fmt) { return fmt == MX_FMT_NVFP4 || fmt == MX_FMT_NVFP4_LOCAL; }
+__host__ __device__ constexpr bool fmt_is_fp4(int fmt) { return fmt == MX_FMT_MXFP4_E2M1 || fmt_is_nvfp4(fmt); }
+__host__ __device__ constexpr int fmt_block(int fmt) { return fmt_is_nvfp4(fmt) ? 16 : 32; }
+__host__ __device__ constexpr bool fmt_has_tensor_scale(int fmt) { return fmt_is_nvfp4(fmt) || fmt == MX_FMT_MOSS_FP8; }
+__host__ __device__ constexpr bool fmt_is_local(int fmt) { return fmt == MX_FMT_NVFP4_LOCAL; }
+constexpr int kLocalRegion = MX_LOCAL_REGION;  // operand rows per FP32 scale (NVFP4_LOCAL)
+__host__ __device__ inline int64_t scale_count(int fmt, int64_t rows)
+{
+    return fmt_is_local(fmt) ? (rows > 0 ? (rows + kLocalRegion - 1) / kLocalRegion : 1) : (fmt_has_tensor_scale(fmt) ? 1 : 0);
+}
 
 // Scale-factor layout of the tensor core: 512-byte tiles of 128 rows x 4 K-blocks.
 __host__ __device__ inline int64_t sf_kgroups(int64_t kblocks) { return (kblocks + 3) / 4; }
@@ -68,6 +75,11 @@ struct TileArgs {
     int col_sr, col_had;
     int* status;
     uint64_t wait_ns;
+    // NVFP4_LOCAL: tensor-scale arrays of the rowwise and colwise operands, one
+    // entry per 128 operand rows (rows of x for the rowwise operand, columns of
+    // x for the colwise one).
+    const float* row_ts_v;
+    const float* col_ts_v;
 };
 
 // Number of kernels this library has launched in the process.
@@ -76,6 +88,12 @@ inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_re
 
 int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d,
                 cudaStream_t s);
+// NVFP4_LOCAL region maxima of bf16 x [R, C]: amax_rows[g] = max |x| over rows
+// 128 g .. 128 g + 127, amax_cols[g] over columns 128 g .. (either may be null).
+int launch_region_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax_rows, float* amax_cols,
+                       const Device& d, cudaStream_t s);
+// NVFP4_LOCAL tensor scales: ts[g] = fl32(amax[g] / 2688), or 1 where amax[g] == 0.
+int launch_local_scales(const float* amax, float* ts, int64_t n, const Device& d, cudaStream_t s);
 int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s);
 int launch_quantize_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s);
 int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStream_t s);

@@ -639,6 +639,52 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
 constexpr int kTR = 64, kTC = 256, kTStages = 3;
 constexpr int kTileBytes = kTR * kTC * 2;
 
+// NVFP4 block encode under a region's own FP32 scale ts (NVFP4_LOCAL): the
+// NVFP4 steps with exact IEEE quotients (the shared-divisor division), since
+// the scale differs from region to region.  Produces the scale byte and N/8
+// words of codes; `v` is overwritten.
+template <bool SR, int N>
+__device__ __forceinline__ uint32_t nvfp4_local_encode(float (&v)[N], float bmax, float ts, uint64_t seed, uint32_t sid,
+                                                       uint64_t L8, uint32_t* out)
+{
+    const float den = __fmul_rn(6.0f, ts);
+    const uint32_t sb = cvt_e4m3x2(div_shared(bmax, den, recip_for_div(den)), 0.0f) & 0x7Fu;
+    const float d = __fmul_rn(dec_e4m3_pos(sb), ts);
+    if (d == 0.0f) {  // the block scale decodes to 0: sign-kept zero codes
+#pragma unroll
+        for (int w = 0; w < N / 8; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                word |= ((__float_as_uint(v[8 * w + i]) >> 31) << 3) << (4 * i);
+            out[w] = word;
+        }
+        return sb;
+    }
+    const float r = recip_for_div(d);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        v[i] = div_shared(v[i], d, r);
+#pragma unroll
+    for (int w = 0; w < N / 8; ++w) {
+        if constexpr (SR) {
+            uint32_t u[8], word = 0;
+            sr_bits8(seed, sid, L8 + w, u);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                word |= e2m1_sr(v[8 * w + i], u[i]) << (4 * i);
+            out[w] = word;
+        } else {
+            float q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                q[i] = v[8 * w + i];
+            out[w] = cvt_e2m1x8(q);
+        }
+    }
+    return sb;
+}
+
 // NVFP4 round-to-nearest-even encode of one block by certified double-word
 // reciprocal products (no division, no branch).  Returns the scale byte and
 // sets `redo` for a block whose divisor is not certified or whose quotients
@@ -684,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t R = a.R, C = a.C;
     const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_q, a.rule);
-    if (fmt_has_tensor_scale(FMT) && blockIdx.x == 0 && tid == 0) {
+    if ((FMT == MX_FMT_NVFP4 || FMT == MX_FMT_MOSS_FP8) && blockIdx.x == 0 && tid == 0) {
         *a.tensor_scale = sc.ts;
         if (a.tensor_scale_copy) {
             *a.tensor_scale_copy = sc.ts;
@@ -768,7 +814,10 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                 if constexpr (FMT == MX_FMT_MOSS_FP8)
                     bmax = moss_block(v, bmax, sc);
                 uint32_t out[FP4 ? BLOCK / 8 : BLOCK / 4], sfb;
-                if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
+                if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
+                    const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
+                    sfb = nvfp4_local_encode<ROW_SR, BLOCK>(v, bmax, a.row_ts_v[r0 >> 7], a.seed, a.stream_id, L8, out);
+                } else if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
                     bool redo;
                     sfb = nvfp4_encode_fast<BLOCK>(v, bmax, sc, out, redo);
                     if (redo)  // rare: this block's divisor is not certified
@@ -849,7 +898,11 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                     if constexpr (FMT == MX_FMT_MOSS_FP8)
                         bmax = moss_block(blk, bmax, sc);
                     uint32_t out[WPB], sfb;
-                    if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
+                    if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
+                        const uint64_t L8 = static_cast<uint64_t>(cbase + j) * (R / 8) + kabs / 8;
+                        const float ts = cbase < C ? a.col_ts_v[cbase >> 7] : 1.0f;  // past C: zero fill, not stored
+                        sfb = nvfp4_local_encode<COL_SR, BLOCK>(blk, bmax, ts, a.seed, a.stream_id, L8, out);
+                    } else if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
                         bool redo;
                         sfb = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out, redo);
                         redo_mask |= (redo ? 1u : 0u) << j;
@@ -905,6 +958,66 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
             (void)mbar_wait_bounded(full0 + 8u * static_cast<int>(j % kTStages),
                                     static_cast<uint32_t>(j / kTStages) & 1u, kWaitLimitNs);
     }
+}
+
+// NVFP4_LOCAL region maxima.  CTA (x, y) covers input rows
+// 128 y .. 128 y + 127 and columns 2048 x .. 2048 x + 2047: thread t owns the
+// 8-column chunk t of every row (a warp reads 512 contiguous bytes per row),
+// so its columns stay in one 128-column region; row and column maxima are
+// combined in the CTA and land with one atomicMax each (|x| bits order like
+// the values).
+constexpr int kRegSlab = 2048;
+__global__ void __launch_bounds__(kThreads) region_amax_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
+                                                               int64_t ld, unsigned* __restrict__ amax_rows,
+                                                               unsigned* __restrict__ amax_cols)
+{
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kLocalRegion;
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * kRegSlab + threadIdx.x * 8;
+    const int64_t r1 = r0 + kLocalRegion < R ? r0 + kLocalRegion : R;
+    uint32_t m2 = 0;  // two packed |bf16| maxima
+    if (c < C) {
+        for (int64_t r = r0; r < r1; ++r) {
+            const uint16_t* p = x + r * ld + c;
+            if (c + 8 <= C) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+                m2 = __vmaxu2(m2, w.x & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, w.y & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, w.z & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, w.w & 0x7FFF7FFFu);
+            } else {
+                for (int64_t e = 0; c + e < C; ++e)
+                    m2 = __vmaxu2(m2, static_cast<uint32_t>(p[e]) & 0x7FFFu);
+            }
+        }
+    }
+    unsigned m = max(m2 & 0xFFFFu, m2 >> 16) << 16;  // bf16 bits -> fp32 bits of |x|
+    // columns: the 16 threads of a 128-column region are one half-warp
+    unsigned mc = m;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1)
+        mc = max(mc, __shfl_xor_sync(0xFFFFFFFFu, mc, o));
+    if (amax_cols && (threadIdx.x & 15) == 0 && c < C)
+        atomicMax(amax_cols + (c >> 7), mc);
+    if (amax_rows) {
+        unsigned mr = __reduce_max_sync(0xFFFFFFFFu, m);
+        __shared__ unsigned wmax[kThreads / 32];
+        if ((threadIdx.x & 31) == 0)
+            wmax[threadIdx.x >> 5] = mr;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            mr = threadIdx.x < kThreads / 32 ? wmax[threadIdx.x] : 0u;
+            mr = __reduce_max_sync(0xFFFFFFFFu, mr);
+            if (threadIdx.x == 0)
+                atomicMax(amax_rows + blockIdx.y, mr);
+        }
+    }
+}
+
+__global__ void local_scales_kernel(const float* __restrict__ amax, float* __restrict__ ts, int64_t n)
+{
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < n;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        ts[g] = amax[g] == 0.0f ? 1.0f : __fdiv_rn(amax[g], 2688.0f);
 }
 
 __global__ void __launch_bounds__(kThreads) dequant_kernel(const uint8_t* __restrict__ codes,
@@ -1048,6 +1161,7 @@ int launch_tile_fmt(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t
     case MX_FMT_MXFP4_E2M1: return launch_tile_sr<MX_FMT_MXFP4_E2M1, DO_ROW, DO_COL>(t, ld, d, s);
     case MX_FMT_NVFP4: return launch_tile_sr<MX_FMT_NVFP4, DO_ROW, DO_COL>(t, ld, d, s);
     case MX_FMT_MOSS_FP8: return launch_tile_sr<MX_FMT_MOSS_FP8, DO_ROW, DO_COL>(t, ld, d, s);
+    case MX_FMT_NVFP4_LOCAL: return launch_tile_sr<MX_FMT_NVFP4_LOCAL, DO_ROW, DO_COL>(t, ld, d, s);
     default: return MX_ERR_INVALID_ARG;
     }
 }
@@ -1070,6 +1184,34 @@ int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, co
         grid.y = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(R, (static_cast<int64_t>(d.sms) * 8 + grid.x - 1) / grid.x)));
     }
     amax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld, reinterpret_cast<unsigned*>(amax));
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_region_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax_rows, float* amax_cols,
+                       const Device& d, cudaStream_t s)
+{
+    const int64_t gr = (R + kLocalRegion - 1) / kLocalRegion, gc = (C + kLocalRegion - 1) / kLocalRegion;
+    if (amax_rows && cudaMemsetAsync(amax_rows, 0, sizeof(float) * std::max<int64_t>(gr, 1), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (amax_cols && cudaMemsetAsync(amax_cols, 0, sizeof(float) * std::max<int64_t>(gc, 1), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (R == 0 || C == 0)
+        return MX_OK;
+    const dim3 grid(static_cast<unsigned>((C + kRegSlab - 1) / kRegSlab), static_cast<unsigned>(gr));
+    region_amax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld,
+                                                 reinterpret_cast<unsigned*>(amax_rows),
+                                                 reinterpret_cast<unsigned*>(amax_cols));
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+int launch_local_scales(const float* amax, float* ts, int64_t n, const Device& d, cudaStream_t s)
+{
+    if (n <= 0)
+        return MX_OK;
+    const int grid = static_cast<int>(std::min<int64_t>((n + kThreads - 1) / kThreads, d.sms));
+    local_scales_kernel<<<grid, kThreads, 0, s>>>(amax, ts, n);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }

@@ -64,13 +64,23 @@ typedef enum mx_status {
  *             scale amax / (448 * 6) ([FAF] nvfp, block scaling under a
  *             global scale).
  * MOSS_FP8:   E4M3 codes, FP32 tensor scale amax / 448 times a power-of-two
- *             micro scale per 32 elements ([MOSS] 创新 1, 两级缩放实现). */
+ *             micro scale per 32 elements ([MOSS] 创新 1, 两级缩放实现).
+ * NVFP4_LOCAL: NVFP4 with the FP32 scale local to each region of
+ *             MX_LOCAL_REGION (128) consecutive operand rows over all of K
+ *             instead of global ([FAF] 格式感知融合的设计思路: "CTA-local" nvfp).
+ *             amax and tensor_scale are arrays of mx_scale_count(fmt, rows)
+ *             entries; a GEMM applies s_A[i / 128] * s_B[j / 128] per output.
+ *             No global amax is needed. */
 typedef enum mx_format {
     MX_FMT_MXFP8_E4M3 = 0,
     MX_FMT_MXFP4_E2M1 = 1,
     MX_FMT_NVFP4 = 2,
-    MX_FMT_MOSS_FP8 = 3
+    MX_FMT_MOSS_FP8 = 3,
+    MX_FMT_NVFP4_LOCAL = 4
 } mx_format;
+
+/* Operand rows that share one FP32 scale in MX_FMT_NVFP4_LOCAL. */
+#define MX_LOCAL_REGION 128
 
 /* RNE: round to nearest, ties to even, saturating at the largest finite
  * value.  SR: stochastic rounding ([FAF] 两个关键的数值技巧; the pages attach it
@@ -130,6 +140,11 @@ typedef struct mx_tensor {
 /* Byte sizes of an operand's buffers (0 for invalid arguments). */
 size_t mx_codes_bytes(int fmt, int64_t rows, int64_t k);
 size_t mx_sf_bytes(int fmt, int64_t rows, int64_t k);
+
+/* Entries of an operand's amax and tensor_scale arrays: 1 for MOSS_FP8 and
+ * NVFP4, ceil(rows / MX_LOCAL_REGION) (at least 1) for NVFP4_LOCAL, 0 for the
+ * formats without a tensor scale and for an invalid fmt. */
+size_t mx_scale_count(int fmt, int64_t rows);
 
 /* amax[0] = max |x| over a bf16 matrix x[R, C] with row stride ld elements
  * (ld >= C, ld % 8 == 0, x 16-byte aligned).  [MOSS] 两级缩放实现, level 1. */

@@ -37,9 +37,11 @@ def assert_quant_equal(q, ref, what=""):
         raise AssertionError(f"{what}: {bad.size} scale bytes differ; first at swizzled offset "
                              f"{bad[0]}: gpu {got[bad[0]]} oracle {exp[bad[0]]}")
     if ref.tensor_scale is not None:
-        sc = q.scalars.cpu().numpy()
-        assert np.float32(sc[0]) == np.float32(ref.amax), (what, sc[0], ref.amax)
-        assert np.float32(sc[1]) == np.float32(ref.tensor_scale), (what, sc[1], ref.tensor_scale)
+        am = q.amax.cpu().numpy().astype(np.float32)
+        ts = q.tensor_scale.cpu().numpy().astype(np.float32)
+        assert np.array_equal(am, np.atleast_1d(np.asarray(ref.amax, dtype=np.float32))), (what, am, ref.amax)
+        assert np.array_equal(ts, np.atleast_1d(np.asarray(ref.tensor_scale, dtype=np.float32))), \
+            (what, ts, ref.tensor_scale)
 
 
 def assert_gemm_close(c_gpu: torch.Tensor, c_ref: np.ndarray, c_abs: np.ndarray, what="",

@@ -10,7 +10,8 @@ from parity import assert_gemm_close, assert_quant_equal, bits
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
+FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss", "nvfp4_local"]
+FP4 = ("mxfp4", "nvfp4", "nvfp4_local")
 
 
 @pytest.fixture(scope="module")
@@ -52,7 +53,7 @@ def test_scale_factor_layout_one_hot(mx, fmt, variant):
     layout definition gives) and check every output against the oracle GEMM
     computed with the same raised logical scales."""
     mx.set_gemm_variant(variant)
-    M, N, K = 256, 384, 1024 if fmt in ("mxfp4", "nvfp4") else 512
+    M, N, K = 256, 384, 1024 if fmt in FP4 else 512
     a = torch.ones(M, K, dtype=torch.bfloat16)
     b = torch.ones(N, K, dtype=torch.bfloat16)
     qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
@@ -63,7 +64,7 @@ def test_scale_factor_layout_one_hot(mx, fmt, variant):
         for row in range(r.rows):
             blk = int(rng.integers(0, kb))
             # E8M0: +1 doubles the scale; UE4M3 (0x7E here): -8 halves it
-            new = int(r.sf_logical[row, blk]) + (1 if fmt != "nvfp4" else -8)
+            new = int(r.sf_logical[row, blk]) + (1 if fmt not in ("nvfp4", "nvfp4_local") else -8)
             r.sf_logical[row, blk] = new
             sf[orc.sf_index(row, blk, kb)] = new
         q.sf.copy_(torch.from_numpy(sf))
@@ -77,7 +78,7 @@ def test_scale_factor_layout_one_hot(mx, fmt, variant):
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_random_gemm(mx, fmt, mnk, out_dtype):
     M, N, K = mnk
-    if fmt in ("mxfp4", "nvfp4") and K % 256:
+    if fmt in FP4 and K % 256:
         K = 256 * ((K + 255) // 256)
     a = workloads.draw("student_t3", (M, K), 40 + M)
     b = workloads.draw("normal", (N, K), 41 + N, 0.02)

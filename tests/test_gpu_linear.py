@@ -11,7 +11,7 @@ from parity import assert_gemm_close, assert_quant_equal, bits
 
 pytestmark = pytest.mark.gpu
 
-FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss"]
+FMTS = ["mxfp8", "mxfp4", "nvfp4", "moss", "nvfp4_local"]
 
 
 @pytest.fixture(scope="module")

@@ -247,3 +247,39 @@ def test_nvfp4_ties_at_every_scale_byte(mx, k):
         torch.cuda.synchronize()
         ref = orc.quantize(bits(xx), "nvfp4", direction, amax_in=2688.0 * 2.0**k)
         assert_quant_equal(q, ref, f"ties k={k} {direction}")
+
+
+# ----------------------------------------------------- CTA-local NVFP4 (f2)
+LOCAL_SHAPES = [(416, 544), (256, 4096), (4096, 96), (96, 288), (320, 128)]
+
+
+@pytest.mark.parametrize("shape", LOCAL_SHAPES)
+@pytest.mark.parametrize("kind", ["student_t3", "lognormal_cols"])
+def test_nvfp4_local_row_col_dual(mx, shape, kind):
+    """One FP32 scale per 128 operand rows (ragged last region): codes, scale
+    bytes and the amax / tensor-scale arrays equal the oracle's, rowwise,
+    colwise and from the dual pass (row regions and column regions of x)."""
+    x = workloads.draw(kind, shape, 500 + shape[0])
+    for direction in ("row", "col"):
+        q, ref = run_both(mx, x, "nvfp4_local", direction)
+        assert_quant_equal(q, ref, f"local/{direction}/{shape}")
+    qr, qc = mx.quantize_dual(x.cuda(), "nvfp4_local")
+    torch.cuda.synchronize()
+    assert_quant_equal(qr, orc.quantize(bits(x), "nvfp4_local", "row"), f"local dual row {shape}")
+    assert_quant_equal(qc, orc.quantize(bits(x), "nvfp4_local", "col"), f"local dual col {shape}")
+
+
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_nvfp4_local_sr_and_amax_in(mx, direction):
+    x = workloads.draw("student_t3", (384, 512), 33, 1e-3)
+    q, ref = run_both(mx, x, "nvfp4_local", direction, rounding="sr", seed=5, stream_id=1)
+    assert_quant_equal(q, ref, f"local SR {direction}")
+    n = -(-(384 if direction == "row" else 512) // 128)
+    ain = torch.linspace(1e-3, 4e-3, n, dtype=torch.float32)
+    q = mx.quantize(x.cuda(), "nvfp4_local", direction, amax_in=ain.cuda())
+    torch.cuda.synchronize()
+    ref = orc.quantize(bits(x), "nvfp4_local", direction, amax_in=ain.numpy())
+    assert_quant_equal(q, ref, f"local amax_in {direction}")
+    with pytest.raises(mx.MXError) as e:  # the dual pass computes its own region maxima
+        mx.quantize_dual(x.cuda(), "nvfp4_local", amax_in=ain.cuda())
+    assert e.value.code == mx.MX_ERR_UNSUPPORTED
