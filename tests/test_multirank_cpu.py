@@ -2,7 +2,7 @@
 
 The block-scaled linear layer shards with no exchange except two: the NVFP4 /
 MOSS tensor amax (one max over shards) and the token-split weight gradient (one
-sum of dW partials).  Each rank runs the oracle on its shard; the combined
+sum of dW partials).  CTA-local NVFP4 needs no amax exchange at all.  Each rank runs the oracle on its shard; the combined
 result must equal the unsharded oracle.  The benchmark's max-over-ranks timing
 helper is checked the same way.
 """
@@ -57,7 +57,17 @@ def _worker(rank, world, port, q):
             ref, _ = orc.gemm(orc.quantize(bits(dY), fmt, "col"), orc.quantize(bits(Xw), fmt, "col"))
             assert np.allclose(t.numpy(), ref, rtol=1e-12, atol=1e-300)
 
-        # 3) the benchmark's job time is the slowest rank's
+        # 3) CTA-local NVFP4: row shards aligned to the 128-row regions need no
+        #    exchange at all; each rank's result is its slice of the unsharded one
+        Xl = workloads.draw("student_t3", (512, 256), 8)
+        rows4 = slice(rank * 256, (rank + 1) * 256)
+        fullq = orc.quantize(bits(Xl), "nvfp4_local")
+        partq = orc.quantize(bits(Xl[rows4]), "nvfp4_local")
+        assert np.array_equal(partq.codes, fullq.codes[rows4])
+        assert np.array_equal(partq.sf_logical, fullq.sf_logical[rows4])
+        assert np.array_equal(partq.tensor_scale, fullq.tensor_scale[rank * 2:(rank + 1) * 2])
+
+        # 4) the benchmark's job time is the slowest rank's
         assert bench.reduce_max(10.0 + rank, world) == 10.0 + world - 1
         q.put((rank, "ok"))
     except Exception as e:  # report to the parent instead of hanging the group
