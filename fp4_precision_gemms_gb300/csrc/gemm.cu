@@ -384,6 +384,22 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tile raster: the group size in M-tiles of the grouped order (tiles walk M
+// within a group, then N).  When all of B fits comfortably in L2 (129 MB),
+// N-fastest order (groups of one M-tile) keeps B resident and streams A
+// once; when A fits, one group of all M-tiles keeps A resident and streams B
+// once; otherwise a group holds about 16 MiB of A row tiles.
+int raster_group_m(int64_t M, int64_t N, int64_t kbytes, int bm, int m_tiles)
+{
+    constexpr int64_t kResident = int64_t(48) << 20;
+    if (N * kbytes <= kResident)
+        return 1;
+    if (M * kbytes <= kResident)
+        return m_tiles;
+    const int64_t a_tile_bytes = static_cast<int64_t>(bm) * kbytes;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+}
+
 template <int KIND, int BN, int STAGES>
 int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s)
@@ -421,9 +437,7 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.wait_ns = kWaitLimitNs;
     p.m_tiles = static_cast<int>((M + G::BM - 1) / G::BM);
     p.n_tiles = static_cast<int>((N + BN - 1) / BN);
-    // A group keeps about 16 MiB of A row tiles resident in L2.
-    const int64_t a_tile_bytes = static_cast<int64_t>(G::BM) * kbytes;
-    p.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+    p.group_m = raster_group_m(M, N, kbytes, G::BM, p.m_tiles);
     const dim3 grid(static_cast<unsigned>(p.m_tiles) * static_cast<unsigned>(p.n_tiles));
     bs_gemm_kernel<KIND, BN, STAGES><<<grid, 192, G::SMEM_ALLOC, s>>>(ta, tb, p);
     count_launch();
@@ -450,12 +464,13 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 //                 the MMA thread: issuing a copy costs the issuing thread tens
 //                 of cycles, which on the MMA thread left the tensor pipe idle.
 // Scale factors live in one TMEM slot per pipeline stage.
-template <int KIND, int STAGES_>
+template <int KIND, int STAGES_, int BKB_ = 128>
 struct CfgPair {
     static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
     static constexpr int BN = 256;  // pair tile N; each CTA stages BN / 2 rows of B
     static constexpr int STAGES = STAGES_;
-    static constexpr int BKB = 128;
+    static constexpr int BKB = BKB_;
+    static constexpr int SUB = BKB / 128;  // 128-byte-wide swizzled sub-tiles per operand per stage
     static constexpr int EPB = KIND == 0 ? 1 : 2;
     static constexpr int BK = BKB * EPB;
     static constexpr int BLOCK = KIND == 2 ? 16 : 32;
@@ -523,13 +538,13 @@ __device__ __forceinline__ void grouped_tile(int tile, int m_tiles, int n_tiles,
     nt = r / gm;
 }
 
-template <int KIND, int STAGES>
-__global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
+template <int KIND, int STAGES, int BKB_ = 128>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
     bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const PairParams p)
 {
-    using G = CfgPair<KIND, STAGES>;
+    using G = CfgPair<KIND, STAGES, BKB_>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(smem);
@@ -597,8 +612,13 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
                     }
                     const uint32_t fb = full0_r0 + 8u * s;
                     mbar_arrive_expect_tx_cluster(fb, G::TX);
-                    tma_load_2d_pair(s0 + G::OFF_A + s * G::A_BYTES, &tmA, fb, kt * G::BKB, arow);
-                    tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES, &tmB, fb, kt * G::BKB, brow);
+#pragma unroll
+                    for (int sub = 0; sub < G::SUB; ++sub) {
+                        tma_load_2d_pair(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128), &tmA, fb,
+                                         kt * G::BKB + sub * 128, arow);
+                        tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128), &tmB, fb,
+                                         kt * G::BKB + sub * 128, brow);
+                    }
                     tma_load_2d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0,
                                      static_cast<int>(((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK) * 4));
 #pragma unroll
@@ -649,15 +669,17 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + G::TM_SFA + slot * G::SFA_COLS;
                     const uint32_t sfb_t = tmem + G::TM_SFB + slot * G::SFB_COLS;
-                    const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES);
-                    const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES);
 #pragma unroll
                     for (int i = 0; i < G::MMAS; ++i) {
+                        constexpr int PER_SUB = 128 / G::MMA_K_BYTES;
+                        const int sub = i / PER_SUB;
+                        const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128));
+                        const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128));
                         const int fb = i * G::BPM;
                         const int chunk = fb / 4;
                         const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
                         const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, 256, G::BN, sf_id, sf_id);
-                        const uint64_t koff = static_cast<uint64_t>((i * G::MMA_K_BYTES) >> 4);
+                        const uint64_t koff = static_cast<uint64_t>(((i % PER_SUB) * G::MMA_K_BYTES) >> 4);
                         mma_bs_pair<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk, sfb_t + 8 * chunk,
                                           (kt > 0 || i > 0) ? 1u : 0u);
                     }
@@ -785,12 +807,12 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND, int STAGES>
+template <int KIND, int STAGES, int BKB_ = 128>
 int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s)
 {
-    using G = CfgPair<KIND, STAGES>;
-    auto kernel = bs_gemm_pair_kernel<KIND, STAGES>;
+    using G = CfgPair<KIND, STAGES, BKB_>;
+    auto kernel = bs_gemm_pair_kernel<KIND, STAGES, BKB_>;
     static int configured_device = -1;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -837,8 +859,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.m_tiles = static_cast<int>((M + 255) / 256);
     p.n_tiles = static_cast<int>((N + 255) / 256);
-    const int64_t a_tile_bytes = 256 * kbytes;
-    p.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+    p.group_m = raster_group_m(M, N, kbytes, 256, p.m_tiles);
     p.status = d.status;
     p.wait_ns = kWaitLimitNs;
     const int tiles = p.m_tiles * p.n_tiles;
@@ -886,8 +907,17 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         return MX_ERR_INVALID_ARG;
     if (v == 3) {
         switch (kind) {
-        case 0: return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        case 1: return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        // MXFP8 / MXFP4: three stages of 256 K-bytes (eight MMAs per stage halve
+        // the per-stage synchronisation); NVFP4's scale tiles do not fit three such
+        // stages, and K not a multiple of 256 bytes takes five stages of 128.
+        case 0:
+            if (A->k % 256 == 0)
+                return launch_pair<0, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        case 1:
+            if (A->k % 512 == 0)
+                return launch_pair<1, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         default: return launch_pair<2, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         }
     }

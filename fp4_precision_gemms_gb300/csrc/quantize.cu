@@ -720,7 +720,9 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     static_assert(kColGroups * (kTR / BLOCK) == kThreads, "one colwise task per encoding thread");
     constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // 32-bit code words per colwise block
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    // 128-byte aligned stage base, by pointer arithmetic on the shared array so
+    // that the tile reads stay shared-memory loads
+    uint8_t* base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const uint32_t sbase = smem_u32(base);
     const uint32_t full0 = sbase + kTStages * kTileBytes;
     __shared__ float2 nv_tab[128];

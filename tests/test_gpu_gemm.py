@@ -196,3 +196,18 @@ def test_gemm_quantized_rejects(mx):
         mx.gemm_quantized(q, q, "nvfp4")
     assert e.value.code == mx.MX_ERR_UNSUPPORTED
     assert mx.last_device_status() == mx.MX_OK
+
+
+@pytest.mark.parametrize("fmt,K", [("mxfp8", 384), ("mxfp8", 1280), ("mxfp4", 768), ("mxfp4", 1536)])
+def test_pair_kernel_both_stage_depths(mx, fmt, K):
+    """K a multiple of 256 bytes takes the three-stage ring of 256-byte K-stages,
+    otherwise the five-stage ring of 128-byte stages: both against the oracle."""
+    mx.set_gemm_variant("pair")
+    M, N = 512 + 64, 768 + 32
+    a = workloads.draw("student_t3", (M, K), 101)
+    b = workloads.draw("normal", (N, K), 102, 0.02)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    c = mx.gemm(qa, qb)
+    ref, cabs = orc.gemm(ra, rb)
+    assert_gemm_close(c, ref, cabs, f"{fmt} K={K}")
+    mx.set_gemm_variant("auto")
