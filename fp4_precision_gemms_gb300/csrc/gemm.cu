@@ -463,7 +463,14 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 //                 TMEM (tcgen05.cp) as soon as the stage is full and signals
 //                 the MMA thread: issuing a copy costs the issuing thread tens
 //                 of cycles, which on the MMA thread left the tensor pipe idle.
-// Scale factors live in one TMEM slot per pipeline stage.
+// Scale factors live in one TMEM slot per pipeline stage.  Each copy also holds
+// the tensor pipe for tens of cycles whatever its size, so where shared memory
+// allows, a scale operand is staged "replicated": every 512-byte chunk (32
+// lines of 16 bytes, the rows r, r + 32, r + 64, r + 96 of one line) stored four
+// times over, which is what one 128x256b copy needs to fill the same TMEM
+// columns as two 32x128b.warpx4 copies.  The TMA load repeats the chunk through
+// a zero-stride dimension of its tensor map.  B pairs its two 128-row tiles in
+// one copy; A (NVFP4) pairs consecutive chunks.
 template <int KIND, int STAGES_, int BKB_ = 128>
 struct CfgPair {
     static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
@@ -483,8 +490,12 @@ struct CfgPair {
     static constexpr int SFB_RT = 2;
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = (BN / 2) * BKB;
-    static constexpr int SFA_BYTES = NCHUNK * 512;
-    static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512;
+    // Replicated staging where it fits: NVFP4 (four stages) both operands,
+    // the 8-bit and MXFP4 kinds B only, and not MXFP4 with 256-byte stages.
+    static constexpr bool SFA_REP = KIND == 2 && NCHUNK % 2 == 0;
+    static constexpr bool SFB_REP = !(KIND == 1 && BKB == 256);
+    static constexpr int SFA_BYTES = NCHUNK * 512 * (SFA_REP ? 4 : 1);
+    static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512 * (SFB_REP ? 4 : 1);
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -619,13 +630,19 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
                         tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128), &tmB, fb,
                                          kt * G::BKB + sub * 128, brow);
                     }
-                    tma_load_2d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0,
-                                     static_cast<int>(((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK) * 4));
+                    const int cha = static_cast<int>((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK);
+                    if constexpr (G::SFA_REP)
+                        tma_load_4d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0, 0, 0, cha);
+                    else
+                        tma_load_2d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0, cha * 4);
 #pragma unroll
                     for (int r = 0; r < G::SFB_RT; ++r) {
-                        const int rt = nt * 2 + r;
-                        tma_load_2d_pair(s0 + G::OFF_SFB + s * G::SFB_BYTES + r * G::NCHUNK * 512, &tmSFB, fb, 0,
-                                         static_cast<int>((rt * p.kgroups + kt * G::NCHUNK) * 4));
+                        const int chb = static_cast<int>((nt * 2 + r) * p.kgroups + kt * G::NCHUNK);
+                        const uint32_t dst = s0 + G::OFF_SFB + s * G::SFB_BYTES + r * (G::SFB_BYTES / G::SFB_RT);
+                        if constexpr (G::SFB_REP)
+                            tma_load_4d_pair(dst, &tmSFB, fb, 0, 0, 0, chb);
+                        else
+                            tma_load_2d_pair(dst, &tmSFB, fb, 0, chb * 4);
                     }
                 }
             }
@@ -710,15 +727,30 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
                     const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
+                    const uint32_t sfa_s = s0 + G::OFF_SFA + s * G::SFA_BYTES;
+                    const uint32_t sfb_s = s0 + G::OFF_SFB + s * G::SFB_BYTES;
+                    if constexpr (G::SFA_REP) {
+                        // chunks 2c and 2c + 1 (2048 bytes apart) into columns 8c .. 8c + 7
 #pragma unroll
-                    for (int c = 0; c < G::NCHUNK; ++c)
-                        tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(s0 + G::OFF_SFA + s * G::SFA_BYTES + c * 512));
-#pragma unroll
-                    for (int r = 0; r < G::SFB_RT; ++r)
+                        for (int c = 0; c < G::NCHUNK / 2; ++c)
+                            tc_cp_sf2_pair(sfa_t + 8 * c, sdesc_sf_rep(sfa_s + c * 4096, 2048));
+                    } else {
 #pragma unroll
                         for (int c = 0; c < G::NCHUNK; ++c)
-                            tc_cp_sf_pair(sfb_t + 8 * c + 4 * r,
-                                          sdesc_sf(s0 + G::OFF_SFB + s * G::SFB_BYTES + (r * G::NCHUNK + c) * 512));
+                            tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(sfa_s + c * 512));
+                    }
+                    if constexpr (G::SFB_REP) {
+                        // chunk c of both 128-row tiles into columns 8c .. 8c + 7
+#pragma unroll
+                        for (int c = 0; c < G::NCHUNK; ++c)
+                            tc_cp_sf2_pair(sfb_t + 8 * c, sdesc_sf_rep(sfb_s + c * 2048, G::NCHUNK * 2048));
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < G::SFB_RT; ++r)
+#pragma unroll
+                            for (int c = 0; c < G::NCHUNK; ++c)
+                                tc_cp_sf_pair(sfb_t + 8 * c + 4 * r, sdesc_sf(sfb_s + (r * G::NCHUNK + c) * 512));
+                    }
                     tc_commit_pair(s0 + G::OFF_SFBAR + 8u * s, 0x1);  // to the MMA thread's CTA
                 }
             }
@@ -807,6 +839,28 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map that stages `chunks` consecutive 512-byte chunks replicated: shared
+// memory receives [chunk][copy 0..3][half][256 bytes], the copy dimension
+// having global stride zero.  Boxes past the end read zeros.
+bool make_sf_rep_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[4] = {256u, 2u, 4u, static_cast<cuuint64_t>(bytes / 512)};
+    const cuuint64_t strides[3] = {256u, 0u, 512u};
+    const cuuint32_t box[4] = {256u, 2u, 4u, static_cast<cuuint32_t>(chunks)};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_sf_map_for(bool replicated, CUtensorMap* m, const void* base, int64_t bytes, int chunks)
+{
+    return replicated ? make_sf_rep_map(m, base, bytes, chunks) : make_sf_map(m, base, bytes, chunks);
+}
+
 template <int KIND, int STAGES, int BKB_ = 128>
 int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s)
@@ -841,7 +895,8 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     CUtensorMap ta, tb, tsa, tsb;
     const int64_t sfa_bytes = sf_layout_bytes(M, K / G::BLOCK), sfb_bytes = sf_layout_bytes(N, K / G::BLOCK);
     if (!make_code_map(&ta, A->codes, M, kbytes, 128) || !make_code_map(&tb, B->codes, N, kbytes, 128) ||
-        !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
+        !make_sf_map_for(G::SFA_REP, &tsa, A->sf, sfa_bytes, G::NCHUNK) ||
+        !make_sf_map_for(G::SFB_REP, &tsb, B->sf, sfb_bytes, G::NCHUNK))
         return MX_ERR_CUDA;
     PairParams p;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
@@ -908,8 +963,9 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
     if (v == 3) {
         switch (kind) {
         // MXFP8 / MXFP4: three stages of 256 K-bytes (eight MMAs per stage halve
-        // the per-stage synchronisation); NVFP4's scale tiles do not fit three such
-        // stages, and K not a multiple of 256 bytes takes five stages of 128.
+        // the per-stage synchronisation); K not a multiple of 256 bytes takes five
+        // stages of 128.  NVFP4's replicated scale tiles leave room for four
+        // stages of 128.
         case 0:
             if (A->k % 256 == 0)
                 return launch_pair<0, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
@@ -918,7 +974,7 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
             if (A->k % 512 == 0)
                 return launch_pair<1, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
             return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        default: return launch_pair<2, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        default: return launch_pair<2, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         }
     }
     const int bn = v == 1 ? 128 : 256;
