@@ -460,18 +460,22 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 //                 rows from TMEM into registers, release the accumulator to the
 //                 next tile's MMAs, then scale and store.
 //   warp 10       in rank 0 one thread copies each stage's scale factors into
-//                 TMEM (tcgen05.cp) as soon as the stage is full and signals
-//                 the MMA thread: issuing a copy costs the issuing thread tens
-//                 of cycles, which on the MMA thread left the tensor pipe idle.
-// Scale factors live in one TMEM slot per pipeline stage.  Each copy also holds
-// the tensor pipe for tens of cycles whatever its size, so where shared memory
-// allows, a scale operand is staged "replicated": every 512-byte chunk (32
-// lines of 16 bytes, the rows r, r + 32, r + 64, r + 96 of one line) stored four
-// times over, which is what one 128x256b copy needs to fill the same TMEM
-// columns as two 32x128b.warpx4 copies.  The TMA load repeats the chunk through
-// a zero-stride dimension of its tensor map.  B pairs its two 128-row tiles in
-// one copy; A (NVFP4) pairs consecutive chunks.
-template <int KIND, int STAGES_, int BKB_ = 128>
+//                 TMEM (tcgen05.cp) and signals the MMA thread: issuing a copy
+//                 costs the issuing thread tens of cycles, which on the MMA
+//                 thread left the tensor pipe idle.
+//   warp 11       scale-factor TMA producer (both CTAs).
+// Scale factors live in one TMEM slot per pipeline stage, but in shared memory
+// they have a ring of their own (SFS slots): a slot is free again as soon as
+// its copies into TMEM have completed, well before the stage's MMAs have, so
+// the scale tiles need not be held for the code tiles' whole ring.  Each copy
+// also holds the tensor pipe for tens of cycles whatever its size, so where
+// shared memory allows, a scale operand is staged "replicated": every 512-byte
+// chunk (32 lines of 16 bytes, the rows r, r + 32, r + 64, r + 96 of one line)
+// stored four times over, which is what one 128x256b copy needs to fill the
+// same TMEM columns as two 32x128b.warpx4 copies.  The TMA load repeats the
+// chunk through a zero-stride dimension of its tensor map.  B pairs its two
+// 128-row tiles in one copy; A pairs consecutive chunks.
+template <int KIND, int STAGES_, int BKB_ = 128, int SFS_ = 2>
 struct CfgPair {
     static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
     static constexpr int BN = 256;  // pair tile N; each CTA stages BN / 2 rows of B
@@ -490,19 +494,27 @@ struct CfgPair {
     static constexpr int SFB_RT = 2;
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = (BN / 2) * BKB;
-    // Replicated staging where it fits: NVFP4 (four stages) both operands,
-    // the 8-bit and MXFP4 kinds B only, and not MXFP4 with 256-byte stages.
-    static constexpr bool SFA_REP = KIND == 2 && NCHUNK % 2 == 0;
-    static constexpr bool SFB_REP = !(KIND == 1 && BKB == 256);
+    static constexpr int SFS = SFS_;  // scale-factor slots in shared memory
+    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16 + STAGES * 8 + 2 * SFS * 8;
+    static constexpr int smem_need(bool rep_a, bool rep_b)
+    {
+        return STAGES * (A_BYTES + B_BYTES) +
+               SFS * (NCHUNK * 512 * (rep_a ? 4 : 1) + SFB_RT * NCHUNK * 512 * (rep_b ? 4 : 1)) + BAR_BYTES + 1024;
+    }
+    // Replicated staging of both operands where it fits, else of B only, else none.
+    static constexpr bool SFA_REP = NCHUNK % 2 == 0 && smem_need(true, true) <= 232448;
+    static constexpr bool SFB_REP = smem_need(SFA_REP, true) <= 232448;
     static constexpr int SFA_BYTES = NCHUNK * 512 * (SFA_REP ? 4 : 1);
     static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512 * (SFB_REP ? 4 : 1);
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int OFF_SFBAR = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // scale slot s copied
-    static constexpr int SMEM_BYTES = OFF_SFBAR + STAGES * 8;
+    static constexpr int OFF_SFB = OFF_SFA + SFS * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + SFS * SFB_BYTES;
+    static constexpr int OFF_SFBAR = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // TMEM scale slot s filled
+    static constexpr int OFF_SFFULL = OFF_SFBAR + STAGES * 8;            // shared scale slot q loaded
+    static constexpr int OFF_SFEMPTY = OFF_SFFULL + SFS * 8;             // shared scale slot q copied out
+    static constexpr int SMEM_BYTES = OFF_SFEMPTY + SFS * 8;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
     static constexpr int SFT = STAGES;  // one scale slot per pipeline stage
     static constexpr int SFA_COLS = 4 * NCHUNK;
@@ -512,11 +524,14 @@ struct CfgPair {
     static constexpr int TM_USED = TM_SFB + SFT * SFB_COLS;
     static constexpr int TM_ALLOC = 512;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int SF_WARP = 2 + EPI_WARPS;             // the scale-copy warp
-    static constexpr int THREADS = 64 + EPI_WARPS * 32 + 32;
+    static constexpr int SF_WARP = 2 + EPI_WARPS;   // the scale-copy warp
+    static constexpr int SF_LOAD_WARP = SF_WARP + 1;  // the scale-factor TMA producer
+    static constexpr int THREADS = 64 + EPI_WARPS * 32 + 64;
     static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;
     static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
-    static constexpr uint32_t TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;  // per CTA per stage
+    static constexpr uint32_t TX = A_BYTES + B_BYTES;         // code bytes per CTA per stage
+    static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;  // scale bytes per CTA per stage
+    static_assert(SMEM_BYTES + 1024 == smem_need(SFA_REP, SFB_REP), "shared memory layout");
     static_assert(TM_USED <= TM_ALLOC, "TMEM budget");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -549,13 +564,13 @@ __device__ __forceinline__ void grouped_tile(int tile, int m_tiles, int n_tiles,
     nt = r / gm;
 }
 
-template <int KIND, int STAGES, int BKB_ = 128>
-__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
+template <int KIND, int STAGES, int BKB_ = 128, int SFS_ = 2>
+__global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
     bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const PairParams p)
 {
-    using G = CfgPair<KIND, STAGES, BKB_>;
+    using G = CfgPair<KIND, STAGES, BKB_, SFS_>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s0 = smem_u32(smem);
@@ -565,6 +580,9 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
     const uint32_t accf = bar0 + 8u * (2 * STAGES);
     const uint32_t acce = accf + 8u;
     const uint32_t tdone = acce + 8u;  // this CTA's epilogue warps have read the accumulator
+    auto sfbar = [&](int s) { return s0 + G::OFF_SFBAR + 8u * s; };
+    auto sffull = [&](int q) { return s0 + G::OFF_SFFULL + 8u * q; };
+    auto sfempty = [&](int q) { return s0 + G::OFF_SFEMPTY + 8u * q; };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_BAR + 8 * (2 * STAGES + 3));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -583,7 +601,11 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
         mbar_init(acce, 2);  // one arrival from each CTA's epilogue
         mbar_init(tdone, G::EPI_WARPS);
         for (int st = 0; st < STAGES; ++st)
-            mbar_init(s0 + G::OFF_SFBAR + 8u * st, 1);
+            mbar_init(sfbar(st), 1);
+        for (int q = 0; q < G::SFS; ++q) {
+            mbar_init(sffull(q), 2);   // one arrive.expect_tx from each CTA's scale producer
+            mbar_init(sfempty(q), 1);  // rank 0's multicast commit after the slot's copies
+        }
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
@@ -599,6 +621,36 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
     cluster_sync();  // barrier initialisation and the joint TMEM allocation seen by both CTAs
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // tcgen05.cp of shared scale slot q into TMEM scale slot s
+    auto copy_sf = [&](uint32_t tm, int s, int q) {
+        const uint32_t sfa_t = tm + G::TM_SFA + s * G::SFA_COLS;
+        const uint32_t sfb_t = tm + G::TM_SFB + s * G::SFB_COLS;
+        const uint32_t sfa_s = s0 + G::OFF_SFA + q * G::SFA_BYTES;
+        const uint32_t sfb_s = s0 + G::OFF_SFB + q * G::SFB_BYTES;
+        if constexpr (G::SFA_REP) {
+            // chunks 2c and 2c + 1 (2048 bytes apart) into columns 8c .. 8c + 7
+#pragma unroll
+            for (int c = 0; c < G::NCHUNK / 2; ++c)
+                tc_cp_sf2_pair(sfa_t + 8 * c, sdesc_sf_rep(sfa_s + c * 4096, 2048));
+        } else {
+#pragma unroll
+            for (int c = 0; c < G::NCHUNK; ++c)
+                tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(sfa_s + c * 512));
+        }
+        if constexpr (G::SFB_REP) {
+            // chunk c of both 128-row tiles into columns 8c .. 8c + 7
+#pragma unroll
+            for (int c = 0; c < G::NCHUNK; ++c)
+                tc_cp_sf2_pair(sfb_t + 8 * c, sdesc_sf_rep(sfb_s + c * 2048, G::NCHUNK * 2048));
+        } else {
+#pragma unroll
+            for (int r = 0; r < G::SFB_RT; ++r)
+#pragma unroll
+                for (int c = 0; c < G::NCHUNK; ++c)
+                    tc_cp_sf_pair(sfb_t + 8 * c + 4 * r, sdesc_sf(sfb_s + (r * G::NCHUNK + c) * 512));
+        }
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -629,20 +681,6 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
                                          kt * G::BKB + sub * 128, arow);
                         tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128), &tmB, fb,
                                          kt * G::BKB + sub * 128, brow);
-                    }
-                    const int cha = static_cast<int>((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK);
-                    if constexpr (G::SFA_REP)
-                        tma_load_4d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0, 0, 0, cha);
-                    else
-                        tma_load_2d_pair(s0 + G::OFF_SFA + s * G::SFA_BYTES, &tmSFA, fb, 0, cha * 4);
-#pragma unroll
-                    for (int r = 0; r < G::SFB_RT; ++r) {
-                        const int chb = static_cast<int>((nt * 2 + r) * p.kgroups + kt * G::NCHUNK);
-                        const uint32_t dst = s0 + G::OFF_SFB + s * G::SFB_BYTES + r * (G::SFB_BYTES / G::SFB_RT);
-                        if constexpr (G::SFB_REP)
-                            tma_load_4d_pair(dst, &tmSFB, fb, 0, 0, 0, chb);
-                        else
-                            tma_load_2d_pair(dst, &tmSFB, fb, 0, chb * 4);
                     }
                 }
             }
@@ -677,7 +715,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
                         break;
                     }
                     // the scale-copy warp has put this stage's scale factors in its slot
-                    if (!mbar_wait_bounded(s0 + G::OFF_SFBAR + 8u * s, round & 1u, p.wait_ns)) {
+                    if (!mbar_wait_bounded(sfbar(s), round & 1u, p.wait_ns)) {
                         atomicExch(p.status, MX_ERR_TIMEOUT);
                         *abort_flag = 1;
                         stop = true;
@@ -706,62 +744,91 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_>::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (warp == G::SF_LOAD_WARP) {
+        // Scale-factor producer (both CTAs): slot q of the shared ring is refilled
+        // once rank 0's copies out of it have completed.
+        if (lane == 0) {
+            const uint32_t sffull0_r0 = mapa_shared(sffull(0), 0);
+            int it = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
+                int mt, nt;
+                grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int q = it % G::SFS;
+                    const uint32_t round = static_cast<uint32_t>(it / G::SFS);
+                    if (it >= G::SFS && !mbar_wait_bounded(sfempty(q), (round - 1) & 1u, p.wait_ns)) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = sffull0_r0 + 8u * q;
+                    mbar_arrive_expect_tx_cluster(fb, G::SF_TX);
+                    const int cha = static_cast<int>((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK);
+                    if constexpr (G::SFA_REP)
+                        tma_load_4d_pair(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fb, 0, 0, 0, cha);
+                    else
+                        tma_load_2d_pair(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fb, 0, cha * 4);
+#pragma unroll
+                    for (int r = 0; r < G::SFB_RT; ++r) {
+                        const int chb = static_cast<int>((nt * 2 + r) * p.kgroups + kt * G::NCHUNK);
+                        const uint32_t dst = s0 + G::OFF_SFB + q * G::SFB_BYTES + r * (G::SFB_BYTES / G::SFB_RT);
+                        if constexpr (G::SFB_REP)
+                            tma_load_4d_pair(dst, &tmSFB, fb, 0, 0, 0, chb);
+                        else
+                            tma_load_2d_pair(dst, &tmSFB, fb, 0, chb * 4);
+                    }
+                }
+            }
+            if (stop) {  // give copies already issued time to land before the CTA can exit
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            } else {
+                // the last slots' release arrivals (multicast from rank 0) land
+                // in this CTA before it may exit
+                for (int l = it - G::SFS < 0 ? 0 : it - G::SFS; l < it; ++l)
+                    (void)mbar_wait_bounded(sfempty(l % G::SFS), static_cast<uint32_t>(l / G::SFS) & 1u, p.wait_ns);
+            }
+        }
+        __syncwarp();
     } else if (warp == G::SF_WARP) {
-        // Scale-factor copies (tcgen05.cp) into each stage's TMEM slot, issued
-        // from their own thread so that the MMA thread issues only MMAs.  A
-        // slot is free once its stage is full again: the producer refilled the
-        // stage only after the MMAs that read the slot had completed.
+        // Scale-factor copies (tcgen05.cp) from shared slot q into TMEM slot s,
+        // issued from their own thread so that the MMA thread issues only MMAs.
+        // TMEM slot s is free once the MMAs of the stage's previous round have
+        // completed (its empty barrier).
         if (lane == 0 && rank == 0) {
             int it = 0;
             bool stop = false;
             for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
                 for (int kt = 0; kt < num_kt; ++kt, ++it) {
                     const int s = it % STAGES;
-                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
-                    if (!mbar_wait_bounded(full(s), round & 1u, p.wait_ns) || *abort_flag) {
+                    const int q = it % G::SFS;
+                    const bool ok = mbar_wait_bounded(sffull(q), static_cast<uint32_t>(it / G::SFS) & 1u, p.wait_ns) &&
+                                    (it < STAGES || mbar_wait_bounded(empty(s), static_cast<uint32_t>(it / STAGES - 1) & 1u,
+                                                                      p.wait_ns));
+                    if (!ok || *abort_flag) {
                         atomicExch(p.status, MX_ERR_TIMEOUT);
                         *abort_flag = 1;
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
-                    const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
-                    const uint32_t sfa_s = s0 + G::OFF_SFA + s * G::SFA_BYTES;
-                    const uint32_t sfb_s = s0 + G::OFF_SFB + s * G::SFB_BYTES;
-                    if constexpr (G::SFA_REP) {
-                        // chunks 2c and 2c + 1 (2048 bytes apart) into columns 8c .. 8c + 7
-#pragma unroll
-                        for (int c = 0; c < G::NCHUNK / 2; ++c)
-                            tc_cp_sf2_pair(sfa_t + 8 * c, sdesc_sf_rep(sfa_s + c * 4096, 2048));
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < G::NCHUNK; ++c)
-                            tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(sfa_s + c * 512));
-                    }
-                    if constexpr (G::SFB_REP) {
-                        // chunk c of both 128-row tiles into columns 8c .. 8c + 7
-#pragma unroll
-                        for (int c = 0; c < G::NCHUNK; ++c)
-                            tc_cp_sf2_pair(sfb_t + 8 * c, sdesc_sf_rep(sfb_s + c * 2048, G::NCHUNK * 2048));
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < G::SFB_RT; ++r)
-#pragma unroll
-                            for (int c = 0; c < G::NCHUNK; ++c)
-                                tc_cp_sf_pair(sfb_t + 8 * c + 4 * r, sdesc_sf(sfb_s + (r * G::NCHUNK + c) * 512));
-                    }
-                    tc_commit_pair(s0 + G::OFF_SFBAR + 8u * s, 0x1);  // to the MMA thread's CTA
+                    copy_sf(tmem, s, q);
+                    tc_commit_pair(sfbar(s), 0x1);    // to the MMA thread's CTA
+                    tc_commit_pair(sfempty(q), 0x3);  // the shared slot, to both scale producers
                 }
             }
             if (stop && it > 0) {  // the last copies must finish before TMEM is released
                 const int l = it - 1;
-                (void)mbar_wait_bounded(s0 + G::OFF_SFBAR + 8u * (l % STAGES), static_cast<uint32_t>(l / STAGES) & 1u,
-                                        kWaitLimitNs);
+                (void)mbar_wait_bounded(sfbar(l % STAGES), static_cast<uint32_t>(l / STAGES) & 1u, kWaitLimitNs);
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < G::SF_WARP) {
         const int ew = warp - 2;        // 0 .. 7
         const int q = warp & 3;         // TMEM lane quarter this warp may read
         const int half = ew >> 2;       // accumulator columns half*128 .. +127
@@ -861,12 +928,12 @@ bool make_sf_map_for(bool replicated, CUtensorMap* m, const void* base, int64_t 
     return replicated ? make_sf_rep_map(m, base, bytes, chunks) : make_sf_map(m, base, bytes, chunks);
 }
 
-template <int KIND, int STAGES, int BKB_ = 128>
+template <int KIND, int STAGES, int BKB_ = 128, int SFS = 2>
 int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s)
 {
-    using G = CfgPair<KIND, STAGES, BKB_>;
-    auto kernel = bs_gemm_pair_kernel<KIND, STAGES, BKB_>;
+    using G = CfgPair<KIND, STAGES, BKB_, SFS>;
+    auto kernel = bs_gemm_pair_kernel<KIND, STAGES, BKB_, SFS>;
     static int configured_device = -1;
     static int max_clusters = 0;
     cudaLaunchConfig_t cfg = {};
@@ -964,8 +1031,9 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         switch (kind) {
         // MXFP8 / MXFP4: three stages of 256 K-bytes (eight MMAs per stage halve
         // the per-stage synchronisation); K not a multiple of 256 bytes takes five
-        // stages of 128.  NVFP4's replicated scale tiles leave room for four
-        // stages of 128.
+        // stages of 128.  NVFP4 (stages of eight MMAs do not fit) has four stages
+        // of 128 and four scale slots: a slot is held until its copies have run,
+        // behind the MMAs queued before them, so slots matter more than stages.
         case 0:
             if (A->k % 256 == 0)
                 return launch_pair<0, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
@@ -974,7 +1042,7 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
             if (A->k % 512 == 0)
                 return launch_pair<1, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
             return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        default: return launch_pair<2, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        default: return launch_pair<2, 4, 128, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         }
     }
     const int bn = v == 1 ? 128 : 256;
