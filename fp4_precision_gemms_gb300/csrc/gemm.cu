@@ -451,31 +451,26 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 // scale-factor traffic per flop is two thirds of the single-CTA 128 x 256 tile.
 // The kernel is persistent: cluster c walks tiles c, c + clusters, ... in the
 // grouped order.  Roles per CTA:
-//   warp 0        TMA producer (both CTAs): code and scale tiles, completing on
-//                 the rank-0 CTA's stage barrier (two arrivals per stage).
+//   warp 0        TMA producer (both CTAs): code tiles, completing on the
+//                 rank-0 CTA's stage barrier (two arrivals per stage).
 //   warp 1        TMEM allocation (both CTAs, jointly); in rank 0 one thread
 //                 issues the MMAs for the pair and frees stages and the
 //                 accumulator with multicast commits.
 //   warps 2-9     epilogue (both CTAs): pull this CTA's 128 x 256 accumulator
 //                 rows from TMEM into registers, release the accumulator to the
-//                 next tile's MMAs, then scale and store.
-//   warp 10       in rank 0 one thread copies each stage's scale factors into
-//                 TMEM (tcgen05.cp) and signals the MMA thread: issuing a copy
-//                 costs the issuing thread tens of cycles, which on the MMA
-//                 thread left the tensor pipe idle.
-//   warp 11       scale-factor TMA producer (both CTAs).
-// Scale factors live in one TMEM slot per pipeline stage, but in shared memory
-// they have a ring of their own (SFS slots): a slot is free again as soon as
-// its copies into TMEM have completed, well before the stage's MMAs have, so
-// the scale tiles need not be held for the code tiles' whole ring.  Each copy
-// also holds the tensor pipe for tens of cycles whatever its size, so where
-// shared memory allows, a scale operand is staged "replicated": every 512-byte
-// chunk (32 lines of 16 bytes, the rows r, r + 32, r + 64, r + 96 of one line)
-// stored four times over, which is what one 128x256b copy needs to fill the
-// same TMEM columns as two 32x128b.warpx4 copies.  The TMA load repeats the
-// chunk through a zero-stride dimension of its tensor map.  B pairs its two
-// 128-row tiles in one copy; A pairs consecutive chunks.
-template <int KIND, int STAGES_, int BKB_ = 128, int SFS_ = 2>
+//                 next tile's MMAs, then scale and store.  Between tiles they
+//                 also write each stage's scale factors into TMEM (below).
+//   warp 10       scale-factor TMA producer (both CTAs).
+// Scale factors have a shared-memory ring of their own (SFS slots, compact
+// 512-byte chunks as the tensor-core layout stores them) and one TMEM slot per
+// pipeline stage.  The epilogue warps move them from shared memory to TMEM with
+// tcgen05.st, each warp into its own lane quarter: lane l of every quarter
+// gets chunk line l (the scales of rows l, l + 32, l + 64, l + 96), the layout
+// a 32x128b.warpx4 copy of the chunk leaves.  A tcgen05.cp copy would hold the
+// tensor pipe for tens of cycles per instruction, whatever its size (NVFP4
+// needs 1.5 copies per MMA); the warp stores do not touch the MMA's pipe, and
+// the epilogue warps are otherwise idle during the main loop.
+template <int KIND, int STAGES_, int BKB_ = 128, int SFS_ = 4>
 struct CfgPair {
     static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
     static constexpr int BN = 256;  // pair tile N; each CTA stages BN / 2 rows of B
@@ -495,17 +490,9 @@ struct CfgPair {
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = (BN / 2) * BKB;
     static constexpr int SFS = SFS_;  // scale-factor slots in shared memory
-    static constexpr int BAR_BYTES = (2 * STAGES + 3) * 8 + 16 + STAGES * 8 + 2 * SFS * 8;
-    static constexpr int smem_need(bool rep_a, bool rep_b)
-    {
-        return STAGES * (A_BYTES + B_BYTES) +
-               SFS * (NCHUNK * 512 * (rep_a ? 4 : 1) + SFB_RT * NCHUNK * 512 * (rep_b ? 4 : 1)) + BAR_BYTES + 1024;
-    }
-    // Replicated staging of both operands where it fits, else of B only, else none.
-    static constexpr bool SFA_REP = NCHUNK % 2 == 0 && smem_need(true, true) <= 232448;
-    static constexpr bool SFB_REP = smem_need(SFA_REP, true) <= 232448;
-    static constexpr int SFA_BYTES = NCHUNK * 512 * (SFA_REP ? 4 : 1);
-    static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512 * (SFB_REP ? 4 : 1);
+    static constexpr int SFA_BYTES = NCHUNK * 512;
+    static constexpr int SFB_BYTES = SFB_RT * NCHUNK * 512;
+    static constexpr int SF_UNITS = NCHUNK * (1 + SFB_RT);  // 512-byte chunks (4 TMEM columns) per stage
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -513,25 +500,22 @@ struct CfgPair {
     static constexpr int OFF_BAR = OFF_SFB + SFS * SFB_BYTES;
     static constexpr int OFF_SFBAR = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // TMEM scale slot s filled
     static constexpr int OFF_SFFULL = OFF_SFBAR + STAGES * 8;            // shared scale slot q loaded
-    static constexpr int OFF_SFEMPTY = OFF_SFFULL + SFS * 8;             // shared scale slot q copied out
+    static constexpr int OFF_SFEMPTY = OFF_SFFULL + SFS * 8;             // shared scale slot q read out
     static constexpr int SMEM_BYTES = OFF_SFEMPTY + SFS * 8;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
-    static constexpr int SFT = STAGES;  // one scale slot per pipeline stage
     static constexpr int SFA_COLS = 4 * NCHUNK;
     static constexpr int SFB_COLS = 8 * NCHUNK;
     static constexpr int TM_SFA = BN;
-    static constexpr int TM_SFB = TM_SFA + SFT * SFA_COLS;
-    static constexpr int TM_USED = TM_SFB + SFT * SFB_COLS;
+    static constexpr int TM_SFB = TM_SFA + STAGES * SFA_COLS;
+    static constexpr int TM_USED = TM_SFB + STAGES * SFB_COLS;
     static constexpr int TM_ALLOC = 512;
     static constexpr int EPI_WARPS = 8;
-    static constexpr int SF_WARP = 2 + EPI_WARPS;   // the scale-copy warp
-    static constexpr int SF_LOAD_WARP = SF_WARP + 1;  // the scale-factor TMA producer
-    static constexpr int THREADS = 64 + EPI_WARPS * 32 + 64;
+    static constexpr int SF_LOAD_WARP = 2 + EPI_WARPS;  // the scale-factor TMA producer
+    static constexpr int THREADS = 64 + EPI_WARPS * 32 + 32;
     static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;
     static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
     static constexpr uint32_t TX = A_BYTES + B_BYTES;         // code bytes per CTA per stage
     static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;  // scale bytes per CTA per stage
-    static_assert(SMEM_BYTES + 1024 == smem_need(SFA_REP, SFB_REP), "shared memory layout");
     static_assert(TM_USED <= TM_ALLOC, "TMEM budget");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -564,7 +548,7 @@ __device__ __forceinline__ void grouped_tile(int tile, int m_tiles, int n_tiles,
     nt = r / gm;
 }
 
-template <int KIND, int STAGES, int BKB_ = 128, int SFS_ = 2>
+template <int KIND, int STAGES, int BKB_ = 128, int SFS_ = 4>
 __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
     bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -594,17 +578,16 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full(s), 2);   // one arrive.expect_tx from each CTA's producer
-            mbar_init(empty(s), 1);  // rank 0's multicast commit
+            mbar_init(full(s), 2);                     // one arrive.expect_tx from each CTA's producer
+            mbar_init(empty(s), 1);                    // rank 0's multicast commit
+            mbar_init(sfbar(s), 2 * G::EPI_WARPS);     // the scale stores of every epilogue warp of both CTAs
         }
         mbar_init(accf, 1);
         mbar_init(acce, 2);  // one arrival from each CTA's epilogue
         mbar_init(tdone, G::EPI_WARPS);
-        for (int st = 0; st < STAGES; ++st)
-            mbar_init(sfbar(st), 1);
         for (int q = 0; q < G::SFS; ++q) {
-            mbar_init(sffull(q), 2);   // one arrive.expect_tx from each CTA's scale producer
-            mbar_init(sfempty(q), 1);  // rank 0's multicast commit after the slot's copies
+            mbar_init(sffull(q), 1);              // this CTA's scale producer
+            mbar_init(sfempty(q), G::EPI_WARPS);  // this CTA's epilogue warps have read the slot
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -621,36 +604,6 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
     cluster_sync();  // barrier initialisation and the joint TMEM allocation seen by both CTAs
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    // tcgen05.cp of shared scale slot q into TMEM scale slot s
-    auto copy_sf = [&](uint32_t tm, int s, int q) {
-        const uint32_t sfa_t = tm + G::TM_SFA + s * G::SFA_COLS;
-        const uint32_t sfb_t = tm + G::TM_SFB + s * G::SFB_COLS;
-        const uint32_t sfa_s = s0 + G::OFF_SFA + q * G::SFA_BYTES;
-        const uint32_t sfb_s = s0 + G::OFF_SFB + q * G::SFB_BYTES;
-        if constexpr (G::SFA_REP) {
-            // chunks 2c and 2c + 1 (2048 bytes apart) into columns 8c .. 8c + 7
-#pragma unroll
-            for (int c = 0; c < G::NCHUNK / 2; ++c)
-                tc_cp_sf2_pair(sfa_t + 8 * c, sdesc_sf_rep(sfa_s + c * 4096, 2048));
-        } else {
-#pragma unroll
-            for (int c = 0; c < G::NCHUNK; ++c)
-                tc_cp_sf_pair(sfa_t + 4 * c, sdesc_sf(sfa_s + c * 512));
-        }
-        if constexpr (G::SFB_REP) {
-            // chunk c of both 128-row tiles into columns 8c .. 8c + 7
-#pragma unroll
-            for (int c = 0; c < G::NCHUNK; ++c)
-                tc_cp_sf2_pair(sfb_t + 8 * c, sdesc_sf_rep(sfb_s + c * 2048, G::NCHUNK * 2048));
-        } else {
-#pragma unroll
-            for (int r = 0; r < G::SFB_RT; ++r)
-#pragma unroll
-                for (int c = 0; c < G::NCHUNK; ++c)
-                    tc_cp_sf_pair(sfb_t + 8 * c + 4 * r, sdesc_sf(sfb_s + (r * G::NCHUNK + c) * 512));
-        }
-    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -704,26 +657,18 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                 for (int kt = 0; kt < num_kt; ++kt, ++it) {
                     const int s = it % STAGES;
                     const uint32_t round = static_cast<uint32_t>(it / STAGES);
-                    // A full stage implies both producers saw this stage's previous MMAs
-                    // complete, so the stage's scale slot is free to overwrite.
-                    const bool ok = mbar_wait_bounded(full(s), round & 1u, p.wait_ns);
-                    const int slot = s;
-                    if (!ok) {
-                        atomicExch(p.status, MX_ERR_TIMEOUT);
-                        *abort_flag = 1;
-                        stop = true;
-                        break;
-                    }
-                    // the scale-copy warp has put this stage's scale factors in its slot
-                    if (!mbar_wait_bounded(sfbar(s), round & 1u, p.wait_ns)) {
+                    // the stage's code tiles have landed and every epilogue warp of
+                    // both CTAs has stored its share of the stage's scale factors
+                    if (!mbar_wait_bounded(full(s), round & 1u, p.wait_ns) ||
+                        !mbar_wait_bounded(sfbar(s), round & 1u, p.wait_ns)) {
                         atomicExch(p.status, MX_ERR_TIMEOUT);
                         *abort_flag = 1;
                         stop = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem + G::TM_SFA + slot * G::SFA_COLS;
-                    const uint32_t sfb_t = tmem + G::TM_SFB + slot * G::SFB_COLS;
+                    const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
+                    const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
 #pragma unroll
                     for (int i = 0; i < G::MMAS; ++i) {
                         constexpr int PER_SUB = 128 / G::MMA_K_BYTES;
@@ -746,9 +691,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         __syncwarp();
     } else if (warp == G::SF_LOAD_WARP) {
         // Scale-factor producer (both CTAs): slot q of the shared ring is refilled
-        // once rank 0's copies out of it have completed.
+        // once this CTA's epilogue warps have read it.
         if (lane == 0) {
-            const uint32_t sffull0_r0 = mapa_shared(sffull(0), 0);
             int it = 0;
             bool stop = false;
             for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
@@ -765,21 +709,15 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                         stop = true;
                         break;
                     }
-                    const uint32_t fb = sffull0_r0 + 8u * q;
-                    mbar_arrive_expect_tx_cluster(fb, G::SF_TX);
                     const int cha = static_cast<int>((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK);
-                    if constexpr (G::SFA_REP)
-                        tma_load_4d_pair(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fb, 0, 0, 0, cha);
-                    else
-                        tma_load_2d_pair(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fb, 0, cha * 4);
+                    const uint32_t fl = sffull(q);
+                    mbar_arrive_expect_tx(fl, G::SF_TX);
+                    tma_load_2d(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fl, 0, cha * 4);
 #pragma unroll
                     for (int r = 0; r < G::SFB_RT; ++r) {
                         const int chb = static_cast<int>((nt * 2 + r) * p.kgroups + kt * G::NCHUNK);
-                        const uint32_t dst = s0 + G::OFF_SFB + q * G::SFB_BYTES + r * (G::SFB_BYTES / G::SFB_RT);
-                        if constexpr (G::SFB_REP)
-                            tma_load_4d_pair(dst, &tmSFB, fb, 0, 0, 0, chb);
-                        else
-                            tma_load_2d_pair(dst, &tmSFB, fb, 0, chb * 4);
+                        tma_load_2d(s0 + G::OFF_SFB + q * G::SFB_BYTES + r * (G::SFB_BYTES / G::SFB_RT), &tmSFB, fl, 0,
+                                    chb * 4);
                     }
                 }
             }
@@ -787,61 +725,86 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                 const uint64_t t0 = globaltimer_ns();
                 while (globaltimer_ns() - t0 < 2000000ull) {
                 }
-            } else {
-                // the last slots' release arrivals (multicast from rank 0) land
-                // in this CTA before it may exit
-                for (int l = it - G::SFS < 0 ? 0 : it - G::SFS; l < it; ++l)
-                    (void)mbar_wait_bounded(sfempty(l % G::SFS), static_cast<uint32_t>(l / G::SFS) & 1u, p.wait_ns);
             }
         }
         __syncwarp();
-    } else if (warp == G::SF_WARP) {
-        // Scale-factor copies (tcgen05.cp) from shared slot q into TMEM slot s,
-        // issued from their own thread so that the MMA thread issues only MMAs.
-        // TMEM slot s is free once the MMAs of the stage's previous round have
-        // completed (its empty barrier).
-        if (lane == 0 && rank == 0) {
-            int it = 0;
-            bool stop = false;
-            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
-                for (int kt = 0; kt < num_kt; ++kt, ++it) {
-                    const int s = it % STAGES;
-                    const int q = it % G::SFS;
-                    const bool ok = mbar_wait_bounded(sffull(q), static_cast<uint32_t>(it / G::SFS) & 1u, p.wait_ns) &&
-                                    (it < STAGES || mbar_wait_bounded(empty(s), static_cast<uint32_t>(it / STAGES - 1) & 1u,
-                                                                      p.wait_ns));
-                    if (!ok || *abort_flag) {
-                        atomicExch(p.status, MX_ERR_TIMEOUT);
-                        *abort_flag = 1;
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    copy_sf(tmem, s, q);
-                    tc_commit_pair(sfbar(s), 0x1);    // to the MMA thread's CTA
-                    tc_commit_pair(sfempty(q), 0x3);  // the shared slot, to both scale producers
-                }
-            }
-            if (stop && it > 0) {  // the last copies must finish before TMEM is released
-                const int l = it - 1;
-                (void)mbar_wait_bounded(sfbar(l % STAGES), static_cast<uint32_t>(l / STAGES) & 1u, kWaitLimitNs);
-            }
-        }
-        __syncwarp();
-    } else if (warp < G::SF_WARP) {
+    } else {
         const int ew = warp - 2;        // 0 .. 7
-        const int q = warp & 3;         // TMEM lane quarter this warp may read
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
         const int half = ew >> 2;       // accumulator columns half*128 .. +127
         const uint32_t acce_r0 = mapa_shared(acce, 0);
         const float ta = p.tsa ? *p.tsa : 1.0f, tb = p.tsb ? *p.tsb : 1.0f;
         const float alpha = __fmul_rn(__fmul_rn(ta, tb), p.extra);
+        // This warp stores scale chunks u0 .. u1 - 1 of every stage (A's chunks,
+        // then B's (tile, chunk) pairs) into its lane quarter of the stage's TMEM
+        // slot; the other warp on the same quarter stores the rest.
+        const int u0 = half * G::SF_UNITS / 2, u1 = (half + 1) * G::SF_UNITS / 2;
+        const int my_tiles = cluster_id < tiles ? (tiles - cluster_id + nclusters - 1) / nclusters : 0;
+        const int total_it = my_tiles * num_kt;
+        const uint32_t sfbar0_r0 = mapa_shared(sfbar(0), 0);
+        int sf_it = 0;
+        auto store_sf = [&](int it) -> bool {
+            const int s = it % STAGES;
+            const int qs = it % G::SFS;
+            // the slot has landed and the MMAs that read TMEM slot s last have
+            // completed; every lane waits (and so sees the slot), then the warp
+            // decides as one, since the stores below are warp-collective
+            bool ok = mbar_wait_bounded(sffull(qs), static_cast<uint32_t>(it / G::SFS) & 1u, p.wait_ns) &&
+                      (it < STAGES ||
+                       mbar_wait_bounded(empty(s), static_cast<uint32_t>(it / STAGES - 1) & 1u, p.wait_ns));
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || *abort_flag) {
+                if (lane == 0) {
+                    atomicExch(p.status, MX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                return false;
+            }
+            tc_fence_after();
+            const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+            const uint32_t sfa_t = tmem + lanes + G::TM_SFA + s * G::SFA_COLS;
+            const uint32_t sfb_t = tmem + lanes + G::TM_SFB + s * G::SFB_COLS;
+            const uint32_t sfa_s = s0 + G::OFF_SFA + qs * G::SFA_BYTES + lane * 16;
+            const uint32_t sfb_s = s0 + G::OFF_SFB + qs * G::SFB_BYTES + lane * 16;
+#pragma unroll
+            for (int u = 0; u < G::SF_UNITS; ++u) {
+                if (u < u0 || u >= u1)
+                    continue;
+                if (u < G::NCHUNK) {
+                    tmem_st4(sfa_t + 4 * u, lds128(sfa_s + u * 512));
+                } else {
+                    const int r = (u - G::NCHUNK) / G::NCHUNK, c = (u - G::NCHUNK) % G::NCHUNK;
+                    tmem_st4(sfb_t + 8 * c + 4 * r, lds128(sfb_s + (r * G::NCHUNK + c) * 512));
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sfempty(qs));                 // the shared slot is read
+                mbar_arrive_cluster(sfbar0_r0 + 8u * s);  // TMEM slot s holds this warp's share
+            }
+            return true;
+        };
         int titer = 0;
         for (int tile = cluster_id; tile < tiles; tile += nclusters, ++titer) {
             int mt, nt;
             grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
-            if (!mbar_wait_bounded(accf, static_cast<uint32_t>(titer) & 1u, p.wait_ns)) {
-                atomicExch(p.status, MX_ERR_TIMEOUT);
-                *abort_flag = 1;
+            // this tile's scales and the next tile's first STAGES stages: those
+            // wait only on MMAs of this tile, which need nothing more from here
+            const int upto = min((titer + 1) * num_kt + STAGES, total_it);
+            bool good = true;
+            while (sf_it < upto && good)
+                good = store_sf(sf_it++);
+            if (!good)
+                break;
+            const bool acc_ok =
+                __all_sync(0xffffffffu, mbar_wait_bounded(accf, static_cast<uint32_t>(titer) & 1u, p.wait_ns));
+            if (!acc_ok) {
+                if (lane == 0) {
+                    atomicExch(p.status, MX_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
                 break;
             }
             tc_fence_after();
@@ -906,29 +869,7 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map that stages `chunks` consecutive 512-byte chunks replicated: shared
-// memory receives [chunk][copy 0..3][half][256 bytes], the copy dimension
-// having global stride zero.  Boxes past the end read zeros.
-bool make_sf_rep_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
-{
-    EncodeTiledFn enc = encode_fn();
-    if (!enc)
-        return false;
-    const cuuint64_t dims[4] = {256u, 2u, 4u, static_cast<cuuint64_t>(bytes / 512)};
-    const cuuint64_t strides[3] = {256u, 0u, 512u};
-    const cuuint32_t box[4] = {256u, 2u, 4u, static_cast<cuuint32_t>(chunks)};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool make_sf_map_for(bool replicated, CUtensorMap* m, const void* base, int64_t bytes, int chunks)
-{
-    return replicated ? make_sf_rep_map(m, base, bytes, chunks) : make_sf_map(m, base, bytes, chunks);
-}
-
-template <int KIND, int STAGES, int BKB_ = 128, int SFS = 2>
+template <int KIND, int STAGES, int BKB_ = 128, int SFS = 4>
 int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s)
 {
@@ -962,8 +903,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     CUtensorMap ta, tb, tsa, tsb;
     const int64_t sfa_bytes = sf_layout_bytes(M, K / G::BLOCK), sfb_bytes = sf_layout_bytes(N, K / G::BLOCK);
     if (!make_code_map(&ta, A->codes, M, kbytes, 128) || !make_code_map(&tb, B->codes, N, kbytes, 128) ||
-        !make_sf_map_for(G::SFA_REP, &tsa, A->sf, sfa_bytes, G::NCHUNK) ||
-        !make_sf_map_for(G::SFB_REP, &tsb, B->sf, sfb_bytes, G::NCHUNK))
+        !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
         return MX_ERR_CUDA;
     PairParams p;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
@@ -1030,19 +970,17 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
     if (v == 3) {
         switch (kind) {
         // MXFP8 / MXFP4: three stages of 256 K-bytes (eight MMAs per stage halve
-        // the per-stage synchronisation); K not a multiple of 256 bytes takes five
-        // stages of 128.  NVFP4 (stages of eight MMAs do not fit) has four stages
-        // of 128 and four scale slots: a slot is held until its copies have run,
-        // behind the MMAs queued before them, so slots matter more than stages.
+        // the per-stage synchronisation); K not a multiple of 256 bytes, and
+        // NVFP4, whose stages of eight MMAs do not fit, take five stages of 128.
         case 0:
             if (A->k % 256 == 0)
-                return launch_pair<0, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_pair<0, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_pair<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_pair<0, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         case 1:
             if (A->k % 512 == 0)
-                return launch_pair<1, 3, 256>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_pair<1, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        default: return launch_pair<2, 4, 128, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_pair<1, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_pair<1, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        default: return launch_pair<2, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
         }
     }
     const int bn = v == 1 ? 128 : 256;

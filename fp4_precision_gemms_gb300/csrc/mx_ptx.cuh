@@ -183,6 +183,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
+// Each thread of the warp writes 4 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, K-major operand tile with the 128-byte
@@ -202,16 +220,6 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr)
 {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 32) |
            (static_cast<uint64_t>(1) << 46);
-}
-
-// Descriptor of two replicated scale-factor chunks for a 128x256b copy: 128
-// rows x 2 columns of 16 bytes, no swizzle; 8-row core matrices 128 bytes
-// apart (rows 32 .. 127 repeat rows 0 .. 31 through the four stored copies),
-// the second 16-byte column `lbo` bytes after the first.
-__device__ __forceinline__ uint64_t sdesc_sf_rep(uint32_t saddr, uint32_t lbo)
-{
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>(128 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
 // Instruction descriptor of the block-scaled MMA kinds: B scale id [4,6),
@@ -280,16 +288,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, uint32_t bar_cluster, int32_t x,
-                                                 int32_t y, int32_t z, int32_t w)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "r"(w)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols)
 {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
@@ -315,17 +313,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask)
             bar),
         "h"(cta_mask)
         : "memory");
-}
-
-__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
-// 128 lanes x 256 bits: eight TMEM columns from the descriptor's 128 x 32 bytes.
-__device__ __forceinline__ void tc_cp_sf2_pair(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 template <int KIND>
