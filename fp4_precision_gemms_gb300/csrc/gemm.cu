@@ -452,10 +452,10 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 // The kernel is persistent: cluster c walks tiles c, c + clusters, ... in the
 // grouped order.  Roles per CTA:
 //   warp 0        TMA producer (both CTAs): code tiles, completing on the
-//                 rank-0 CTA's stage barrier (two arrivals per stage).
-//   warp 1        TMEM allocation (both CTAs, jointly); in rank 0 one thread
-//                 issues the MMAs for the pair and frees stages and the
-//                 accumulator with multicast commits.
+//                 rank-0 CTA's stage barrier.
+//   warp 1        TMEM allocation (both CTAs, jointly); in rank 0 the warp runs
+//                 the MMA loop, one elected lane issuing the MMAs for the pair
+//                 and freeing stages and the accumulator with multicast commits.
 //   warps 2-9     epilogue (both CTAs): pull this CTA's 128 x 256 accumulator
 //                 rows from TMEM into registers, release the accumulator to the
 //                 next tile's MMAs, then scale and store.  Between tiles they
@@ -469,7 +469,9 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 // a 32x128b.warpx4 copy of the chunk leaves.  A tcgen05.cp copy would hold the
 // tensor pipe for tens of cycles per instruction, whatever its size (NVFP4
 // needs 1.5 copies per MMA); the warp stores do not touch the MMA's pipe, and
-// the epilogue warps are otherwise idle during the main loop.
+// the epilogue warps are otherwise idle during the main loop.  A stage's
+// barrier counts the code-tile bytes of both CTAs and the scale stores of all
+// sixteen epilogue warps, so the MMA loop waits on one barrier per stage.
 template <int KIND, int STAGES_, int BKB_ = 128, int SFS_ = 4>
 struct CfgPair {
     static constexpr int BM = 128;  // rows per CTA; the pair tile has 256
@@ -498,8 +500,7 @@ struct CfgPair {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + SFS * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + SFS * SFB_BYTES;
-    static constexpr int OFF_SFBAR = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // TMEM scale slot s filled
-    static constexpr int OFF_SFFULL = OFF_SFBAR + STAGES * 8;            // shared scale slot q loaded
+    static constexpr int OFF_SFFULL = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // shared scale slot q loaded
     static constexpr int OFF_SFEMPTY = OFF_SFFULL + SFS * 8;             // shared scale slot q read out
     static constexpr int SMEM_BYTES = OFF_SFEMPTY + SFS * 8;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
@@ -564,7 +565,6 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
     const uint32_t accf = bar0 + 8u * (2 * STAGES);
     const uint32_t acce = accf + 8u;
     const uint32_t tdone = acce + 8u;  // this CTA's epilogue warps have read the accumulator
-    auto sfbar = [&](int s) { return s0 + G::OFF_SFBAR + 8u * s; };
     auto sffull = [&](int q) { return s0 + G::OFF_SFFULL + 8u * q; };
     auto sfempty = [&](int q) { return s0 + G::OFF_SFEMPTY + 8u * q; };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_BAR + 8 * (2 * STAGES + 3));
@@ -578,9 +578,10 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full(s), 2);                     // one arrive.expect_tx from each CTA's producer
-            mbar_init(empty(s), 1);                    // rank 0's multicast commit
-            mbar_init(sfbar(s), 2 * G::EPI_WARPS);     // the scale stores of every epilogue warp of both CTAs
+            // one arrive.expect_tx from each CTA's code producer and one arrival from
+            // each epilogue warp of both CTAs once its scale stores for the stage are done
+            mbar_init(full(s), 2 + 2 * G::EPI_WARPS);
+            mbar_init(empty(s), 1);  // rank 0's multicast commit
         }
         mbar_init(accf, 1);
         mbar_init(acce, 2);  // one arrival from each CTA's epilogue
@@ -644,13 +645,19 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
+        if (rank == 0) {
+            // The whole warp runs the loop (so descriptors are warp-uniform); one
+            // elected lane issues.  Waits are taken by every lane and decided as one.
+            const bool leader = elect_one();
             int it = 0, titer = 0;
             bool stop = false;
             for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters, ++titer) {
-                if (titer > 0 && !mbar_wait_bounded(acce, static_cast<uint32_t>(titer - 1) & 1u, p.wait_ns)) {
-                    atomicExch(p.status, MX_ERR_TIMEOUT);
-                    *abort_flag = 1;
+                if (titer > 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait_bounded(acce, static_cast<uint32_t>(titer - 1) & 1u, p.wait_ns))) {
+                    if (leader) {
+                        atomicExch(p.status, MX_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
                     break;
                 }
                 tc_fence_after();
@@ -659,33 +666,41 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                     const uint32_t round = static_cast<uint32_t>(it / STAGES);
                     // the stage's code tiles have landed and every epilogue warp of
                     // both CTAs has stored its share of the stage's scale factors
-                    if (!mbar_wait_bounded(full(s), round & 1u, p.wait_ns) ||
-                        !mbar_wait_bounded(sfbar(s), round & 1u, p.wait_ns)) {
-                        atomicExch(p.status, MX_ERR_TIMEOUT);
-                        *abort_flag = 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(s), round & 1u, p.wait_ns))) {
+                        if (leader) {
+                            atomicExch(p.status, MX_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
                         stop = true;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
                     const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
+                    if (leader) {
 #pragma unroll
-                    for (int i = 0; i < G::MMAS; ++i) {
-                        constexpr int PER_SUB = 128 / G::MMA_K_BYTES;
-                        const int sub = i / PER_SUB;
-                        const uint64_t adesc = sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128));
-                        const uint64_t bdesc = sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128));
-                        const int fb = i * G::BPM;
-                        const int chunk = fb / 4;
-                        const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
-                        const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, 256, G::BN, sf_id, sf_id);
-                        const uint64_t koff = static_cast<uint64_t>(((i % PER_SUB) * G::MMA_K_BYTES) >> 4);
-                        mma_bs_pair<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk, sfb_t + 8 * chunk,
-                                          (kt > 0 || i > 0) ? 1u : 0u);
+                        for (int i = 0; i < G::MMAS; ++i) {
+                            constexpr int PER_SUB = 128 / G::MMA_K_BYTES;
+                            const int sub = i / PER_SUB;
+                            const uint64_t adesc =
+                                sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128));
+                            const uint64_t bdesc =
+                                sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128));
+                            const int fb = i * G::BPM;
+                            const int chunk = fb / 4;
+                            const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
+                            const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, 256, G::BN, sf_id, sf_id);
+                            const uint64_t koff = static_cast<uint64_t>(((i % PER_SUB) * G::MMA_K_BYTES) >> 4);
+                            mma_bs_pair<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk,
+                                              sfb_t + 8 * chunk, (kt > 0 || i > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair(empty(s), 0x3);
                     }
-                    tc_commit_pair(empty(s), 0x3);
+                    __syncwarp();
                 }
-                tc_commit_pair(accf, 0x3);  // this tile's accumulator is complete in both CTAs
+                if (leader)
+                    tc_commit_pair(accf, 0x3);  // this tile's accumulator is complete in both CTAs
+                __syncwarp();
             }
         }
         __syncwarp();
@@ -741,7 +756,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         const int u0 = half * G::SF_UNITS / 2, u1 = (half + 1) * G::SF_UNITS / 2;
         const int my_tiles = cluster_id < tiles ? (tiles - cluster_id + nclusters - 1) / nclusters : 0;
         const int total_it = my_tiles * num_kt;
-        const uint32_t sfbar0_r0 = mapa_shared(sfbar(0), 0);
+        const uint32_t full0_r0 = mapa_shared(full(0), 0);
         int sf_it = 0;
         auto store_sf = [&](int it) -> bool {
             const int s = it % STAGES;
@@ -782,7 +797,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(sfempty(qs));                 // the shared slot is read
-                mbar_arrive_cluster(sfbar0_r0 + 8u * s);  // TMEM slot s holds this warp's share
+                mbar_arrive_cluster(full0_r0 + 8u * s);  // TMEM slot s holds this warp's share
             }
             return true;
         };
