@@ -801,8 +801,29 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
             }
             return true;
         };
+        // Between output chunks: store the next stages' scales while they are
+        // ready without waiting, at most two at a time; false on a failed store.
+        // With three stages the output stores outlast the stages the TMEM slots
+        // hold; with five they do not, and polling only lengthens the epilogue.
+        auto poll_sf = [&]() -> bool {
+            if constexpr (STAGES <= 3) {
+                for (int n = 0; n < 2 && sf_it < total_it; ++n) {
+                    const int s = sf_it % STAGES;
+                    const int qs = sf_it % G::SFS;
+                    const bool ready =
+                        mbar_try_wait(sffull(qs), static_cast<uint32_t>(sf_it / G::SFS) & 1u) &&
+                        (sf_it < STAGES || mbar_try_wait(empty(s), static_cast<uint32_t>(sf_it / STAGES - 1) & 1u));
+                    if (!__all_sync(0xffffffffu, ready))
+                        return true;
+                    if (!store_sf(sf_it++))
+                        return false;
+                }
+            }
+            return true;
+        };
         int titer = 0;
-        for (int tile = cluster_id; tile < tiles; tile += nclusters, ++titer) {
+        bool sf_good = true;
+        for (int tile = cluster_id; tile < tiles && sf_good; tile += nclusters, ++titer) {
             int mt, nt;
             grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
             // this tile's scales and the next tile's first STAGES stages: those
@@ -840,18 +861,32 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                     atomicExch(p.status, MX_ERR_TIMEOUT);
             }
             const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
-            if (row < p.M) {
+            auto out_chunk = [&](int j, int col0) {
+                const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
+                store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
+            };
+            if constexpr (STAGES <= 3) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int col0 = nt * 256 + half * 128 + j * 32;
                     if (col0 >= p.N)
                         break;
-                    const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
-                    float v[32];
+                    if (row < p.M)
+                        out_chunk(j, col0);
+                    __syncwarp();
+                    sf_good = sf_good && poll_sf();
+                }
+            } else if (row < p.M) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
-                    store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
+                for (int j = 0; j < 4; ++j) {
+                    const int col0 = nt * 256 + half * 128 + j * 32;
+                    if (col0 >= p.N)
+                        break;
+                    out_chunk(j, col0);
                 }
             }
         }
