@@ -499,7 +499,13 @@ struct CfgPair {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + SFS * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + SFS * SFB_BYTES;
+    // bf16 / fp32 output leaves through TMA stores from one 2 KB staging box
+    // per epilogue warp, where shared memory allows
+    static constexpr int STG_BOX = 2048;
+    static constexpr int BASE_BYTES = OFF_SFB + SFS * SFB_BYTES + (2 * STAGES + 3) * 8 + 16 + 2 * SFS * 8 + 1024;
+    static constexpr bool TMA_OUT = BASE_BYTES + 8 * STG_BOX <= 232448;
+    static constexpr int OFF_STG = OFF_SFB + SFS * SFB_BYTES;
+    static constexpr int OFF_BAR = OFF_STG + (TMA_OUT ? 8 * STG_BOX : 0);
     static constexpr int OFF_SFFULL = OFF_BAR + (2 * STAGES + 3) * 8 + 16;  // shared scale slot q loaded
     static constexpr int OFF_SFEMPTY = OFF_SFFULL + SFS * 8;             // shared scale slot q read out
     static constexpr int SMEM_BYTES = OFF_SFEMPTY + SFS * 8;
@@ -553,7 +559,7 @@ template <int KIND, int STAGES, int BKB_ = 128, int SFS_ = 4>
 __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
     bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                        const PairParams p)
+                        const __grid_constant__ CUtensorMap tmC, const PairParams p)
 {
     using G = CfgPair<KIND, STAGES, BKB_, SFS_>;
     extern __shared__ uint8_t smem_raw[];
@@ -596,6 +602,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         prefetch_tmap(&tmB);
         prefetch_tmap(&tmSFA);
         prefetch_tmap(&tmSFB);
+        if (G::TMA_OUT && p.out_mode <= EPI_BF16)
+            prefetch_tmap(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), G::TM_ALLOC);
@@ -823,6 +831,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         };
         int titer = 0;
         bool sf_good = true;
+        const bool tma_out = G::TMA_OUT && p.out_mode <= EPI_BF16;
+        bool stg_busy = false;  // this warp's staging box may still be read by a TMA store
         for (int tile = cluster_id; tile < tiles && sf_good; tile += nclusters, ++titer) {
             int mt, nt;
             grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
@@ -860,36 +870,96 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                 else
                     atomicExch(p.status, MX_ERR_TIMEOUT);
             }
-            const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
-            auto out_chunk = [&](int j, int col0) {
-                const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
-                float v[32];
+            const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
+            const int row = row0 + lane;
+            if (tma_out) {
+                // 32 rows x 64 bytes per box: 32 bf16 columns, or 16 fp32 columns;
+                // the store clips rows >= M and columns >= N
+                auto emit = [&](const uint32_t (&pk)[16], int col) {
+                    if (row0 >= p.M)  // all of this warp's rows lie past the output
+                        return;
+                    if (stg_busy) {  // the previous box has been read out of the buffer
+                        if (lane == 0)
+                            bulk_wait_read_all();
+                        __syncwarp();
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(smem + G::OFF_STG + ew * G::STG_BOX + lane * 64);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
-                store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
-            };
-            if constexpr (STAGES <= 3) {
+                    for (int w = 0; w < 4; ++w)
+                        dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, s0 + G::OFF_STG + ew * G::STG_BOX, col, row0);
+                        bulk_commit();
+                    }
+                    stg_busy = true;
+                };
+                const bool bf16 = p.out_mode == EPI_BF16;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int col0 = nt * 256 + half * 128 + j * 32;
                     if (col0 >= p.N)
                         break;
-                    if (row < p.M)
-                        out_chunk(j, col0);
-                    __syncwarp();
+                    const float al =
+                        (p.ts_region && row < p.M) ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    uint32_t pk[16];
+                    if (bf16) {
+#pragma unroll
+                        for (int h = 0; h < 16; ++h) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j][2 * h]), al),
+                                                                            __fmul_rn(__uint_as_float(r[j][2 * h + 1]), al));
+                            pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        emit(pk, col0);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 16; ++h)
+                            pk[h] = __float_as_uint(__fmul_rn(__uint_as_float(r[j][h]), al));
+                        emit(pk, col0);
+                        if (col0 + 16 < p.N) {
+#pragma unroll
+                            for (int h = 0; h < 16; ++h)
+                                pk[h] = __float_as_uint(__fmul_rn(__uint_as_float(r[j][16 + h]), al));
+                            emit(pk, col0 + 16);
+                        }
+                    }
                     sf_good = sf_good && poll_sf();
                 }
-            } else if (row < p.M) {
+            } else {
+                auto out_chunk = [&](int j, int col0) {
+                    const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    float v[32];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int col0 = nt * 256 + half * 128 + j * 32;
-                    if (col0 >= p.N)
-                        break;
-                    out_chunk(j, col0);
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
+                    store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
+                };
+                if constexpr (STAGES <= 3) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col0 = nt * 256 + half * 128 + j * 32;
+                        if (col0 >= p.N)
+                            break;
+                        if (row < p.M)
+                            out_chunk(j, col0);
+                        __syncwarp();
+                        sf_good = sf_good && poll_sf();
+                    }
+                } else if (row < p.M) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col0 = nt * 256 + half * 128 + j * 32;
+                        if (col0 >= p.N)
+                            break;
+                        out_chunk(j, col0);
+                    }
                 }
             }
         }
+        if (stg_busy && lane == 0)
+            bulk_wait_all();  // this warp's output stores have completed
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -916,6 +986,24 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t bytes, int chunks)
     const cuuint32_t estr[2] = {1u, 1u};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D map over the bf16 / fp32 output (row stride ldc elements) for TMA stores
+// of 32-row boxes 64 bytes wide; the store clips rows >= M and columns >= N.
+bool make_out_map(CUtensorMap* m, void* c, int64_t M, int64_t N, int64_t ldc, int out_mode)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const bool bf16 = out_mode == EPI_BF16;
+    const cuuint64_t esz = bf16 ? 2u : 4u;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * esz};
+    const cuuint32_t box[2] = {bf16 ? 32u : 16u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -955,6 +1043,9 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     if (!make_code_map(&ta, A->codes, M, kbytes, 128) || !make_code_map(&tb, B->codes, N, kbytes, 128) ||
         !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
         return MX_ERR_CUDA;
+    CUtensorMap tc = ta;  // unused unless the output leaves through TMA stores
+    if (G::TMA_OUT && out_mode <= EPI_BF16 && !make_out_map(&tc, C, M, N, ldc, out_mode))
+        return MX_ERR_CUDA;
     PairParams p;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
     p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
@@ -976,7 +1067,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.wait_ns = kWaitLimitNs;
     const int tiles = p.m_tiles * p.n_tiles;
     cfg.gridDim = dim3(2 * std::min(tiles, max_clusters));
-    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, tc, p) != cudaSuccess)
         return MX_ERR_CUDA;
     count_launch();
     return MX_OK;
