@@ -189,6 +189,52 @@ def test_philox_statistics_and_counter_sensitivity():
         assert 30 < flips < 98
 
 
+def _curand_host():
+    """cuRAND's host-side (CPU) generator library, if the toolkit ships it."""
+    import ctypes
+
+    for name in ("libcurand.so", "libcurand.so.10", "/usr/local/cuda/lib64/libcurand.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    return None
+
+
+def test_philox_matches_curand_host_generator():
+    """The oracle's Philox4x32-10 against a library implementation of the same
+    published generator: cuRAND's host Philox4_32_10 generator, which runs on the
+    CPU.  With a 64-bit seed s it emits output block j (four words) as
+    Philox4x32-10 with key (s mod 2^32, s div 2^32) and counter
+    (j div 65536, 0, j mod 65536, 0).  That covers both key words and counter
+    words 0 and 2, the words the stochastic-rounding counter uses."""
+    import ctypes
+
+    L = _curand_host()
+    if L is None:
+        pytest.skip("cuRAND is not installed")
+    gen = ctypes.c_void_p()
+    if L.curandCreateGeneratorHost(ctypes.byref(gen), 161) != 0:  # CURAND_RNG_PSEUDO_PHILOX4_32_10
+        pytest.skip("cuRAND host generator unavailable")
+    try:
+        n_blocks = 65536 + 1024
+        for seed in (0x0123456789ABCDEF, 42, 2 ** 64 - 1):
+            assert L.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+            assert L.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(0)) == 0  # restart the stream
+            out = np.zeros(4 * n_blocks, dtype=np.uint32)
+            assert L.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(out.size)) == 0
+            blocks = out.reshape(-1, 4)
+            key = [seed & 0xFFFFFFFF, seed >> 32]
+            rng = np.random.default_rng(seed & 0xFFFF)
+            picks = list(range(64)) + list(range(65536, 65536 + 64)) + list(rng.integers(0, n_blocks, 64))
+            for j in picks:
+                j = int(j)
+                want = orc.philox4x32_10([j // 65536, 0, j % 65536, 0], key)
+                assert np.array_equal(blocks[j], want), (seed, j)
+    finally:
+        L.curandDestroyGenerator(gen)
+
+
 def test_sr_unbiased_and_probability():
     grid = [orc.decode("e2m1", c) for c in range(8)]
     rng = np.random.default_rng(11)
