@@ -70,3 +70,20 @@ def test_calls_without_a_gpu_fail_loudly(lib):
     assert lib.mx_last_device_status(None) == mx.MX_ERR_NO_DEVICE
     with pytest.raises(mx.MXError):
         mx.quantize(torch.zeros(32, 32, dtype=torch.bfloat16), "mxfp8")
+
+
+def test_size_queries_agree_with_the_oracle_layout(lib):
+    """The library's buffer sizes against the oracle's independently written
+    layout (512-byte tiles of 128 rows x 4 scale blocks) on many shapes, and the
+    tensor-scale entry counts against the format table."""
+    import oracle as orc
+
+    fmts = {"mxfp8": (0, 32, 1.0), "mxfp4": (1, 32, 0.5), "nvfp4": (2, 16, 0.5), "moss": (3, 32, 1.0),
+            "nvfp4_local": (4, 16, 0.5)}
+    for name, (f, block, code_bytes) in fmts.items():
+        for rows in (1, 31, 127, 128, 129, 300, 4096, 14336):
+            for k in (block, 2 * block, 4 * block, 5 * block, 256, 4160, 14336):
+                assert lib.mx_codes_bytes(f, rows, k) == int(rows * k * code_bytes), (name, rows, k)
+                assert lib.mx_sf_bytes(f, rows, k) == orc.sf_bytes(rows, k // block), (name, rows, k)
+            want = {"nvfp4": 1, "moss": 1, "nvfp4_local": max(1, -(-rows // 128))}.get(name, 0)
+            assert lib.mx_scale_count(f, rows) == want, (name, rows)
