@@ -211,3 +211,29 @@ def test_pair_kernel_both_stage_depths(mx, fmt, K):
     ref, cabs = orc.gemm(ra, rb)
     assert_gemm_close(c, ref, cabs, f"{fmt} K={K}")
     mx.set_gemm_variant("auto")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mnk", [(33, 40, 256), (300, 1000, 512), (257, 264, 1024)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_pair_output_stays_inside_a_strided_view(mx, fmt, mnk, out_dtype):
+    """The CTA-pair kernel writes its bf16 / fp32 output (TMA stores of 32-row
+    boxes, clipped at M and N) into a view of a wider, taller buffer: every
+    element of the view matches the oracle and nothing past column N or row M
+    is touched."""
+    M, N, K = mnk
+    a = workloads.draw("student_t3", (M, K), 90 + M)
+    b = workloads.draw("normal", (N, K), 91 + N, 0.02)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    ld = ((N + 24 + 7) // 8) * 8
+    buf = torch.full((M + 16, ld), float("nan"), dtype=out_dtype, device="cuda")
+    out = buf[:M, :N]
+    mx.set_gemm_variant("pair")
+    try:
+        mx.gemm(qa, qb, out=out)
+    finally:
+        mx.set_gemm_variant("auto")
+    ref, cabs = orc.gemm(ra, rb)
+    assert_gemm_close(out, ref, cabs, f"pair strided {fmt} {mnk}")
+    assert torch.isnan(buf[:M, N:]).all()
+    assert torch.isnan(buf[M:, :]).all()
