@@ -237,3 +237,24 @@ def test_pair_output_stays_inside_a_strided_view(mx, fmt, mnk, out_dtype):
     assert_gemm_close(out, ref, cabs, f"pair strided {fmt} {mnk}")
     assert torch.isnan(buf[:M, N:]).all()
     assert torch.isnan(buf[M:, :]).all()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("K", [256, 512])
+def test_pair_kernel_short_k_many_tiles(mx, fmt, K):
+    """Every cluster runs several tiles of one or two K-stages, so the
+    epilogue warps' scale stores run ahead across several future tiles and the
+    accumulator changes hands every stage or two."""
+    M, N = 4096 + 40, 4096
+    a = workloads.draw("student_t3", (M, K), 95 + K)
+    b = workloads.draw("normal", (N, K), 96 + K, 0.02)
+    qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
+    rows = np.r_[0:32, 2048:2080, M - 64:M]
+    mx.set_gemm_variant("pair")
+    try:
+        for out_dtype in (torch.float32, torch.bfloat16):
+            c = mx.gemm(qa, qb, out_dtype=out_dtype)
+            ref, cabs = orc.gemm(ra, rb, rows=rows)
+            assert_gemm_close(c[torch.as_tensor(rows, device=c.device)], ref, cabs, f"pair short K {fmt} {K}")
+    finally:
+        mx.set_gemm_variant("auto")
