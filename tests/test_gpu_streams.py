@@ -44,3 +44,33 @@ def test_gemm_on_side_stream_and_in_a_graph(mx, fmt):
     torch.cuda.synchronize()
     assert torch.equal(out2, ref)
     assert mx.last_device_status() == mx.MX_OK
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_linear_layer_captured_in_a_graph(mx, fmt):
+    """The whole layer (quantize producers, amax, GEMMs) for forward and backward,
+    captured on a side stream with caller-owned workspace and outputs, replays
+    to the eagerly computed result bit for bit."""
+    T, Kin, Nout = 1024, 1024, 1536
+    X = workloads.draw("student_t3", (T, Kin), 21).cuda()
+    W = workloads.draw("normal", (Nout, Kin), 22, 0.02).cuda()
+    dY = workloads.draw("student_t3", (T, Nout), 23, 1e-3).cuda()
+    ws = torch.empty(max(mx.workspace_bytes(T, Kin, Nout, fmt, "fwd"), mx.workspace_bytes(T, Kin, Nout, fmt, "bwd")),
+                     dtype=torch.uint8, device="cuda")
+    Y_ref = mx.linear_fwd(X, W, fmt, workspace=ws)
+    dX_ref, dW_ref = mx.linear_bwd(dY, X, W, fmt, workspace=ws)
+    torch.cuda.synchronize()
+
+    s = torch.cuda.Stream()
+    Y = torch.zeros_like(Y_ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        mx.linear_fwd(X, W, fmt, workspace=ws, out=Y, stream=s)
+        dX, dW = mx.linear_bwd(dY, X, W, fmt, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y_ref)
+    assert torch.equal(dX, dX_ref)
+    assert torch.equal(dW, dW_ref)
+    assert mx.last_device_status() == mx.MX_OK
