@@ -184,6 +184,7 @@ class MXTensor:
 
     def _c(self) -> _CTensor:
         t = _CTensor()
+        _on_gpu(self.codes, self.sf, self.scalars)  # the library only reads and writes device memory
         t.codes = self.codes.data_ptr()
         t.sf = self.sf.data_ptr()
         t.amax = self.scalars.data_ptr()
@@ -195,7 +196,7 @@ class MXTensor:
 
 def amax(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
-    _on_gpu(x)
+    _on_gpu(x, out)
     out = out if out is not None else torch.empty(1, dtype=torch.float32, device=x.device)
     _check(lib().mx_amax(_ptr(x), x.shape[0], x.shape[1], x.stride(0), _ptr(out), _stream(stream)),
            "mx_amax")
@@ -259,6 +260,7 @@ def dequantize(q: MXTensor, stream=None) -> torch.Tensor:
 def gemm(a: MXTensor, b: MXTensor, extra_alpha: float = 1.0, out_dtype=torch.float32,
          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """C[M, N] = alpha * dq(a) dq(b)^T on the tensor cores."""
+    _on_gpu(out)
     out = out if out is not None else torch.empty((a.rows, b.rows), dtype=out_dtype,
                                                   device=a.codes.device)
     ca, cb = a._c(), b._c()
@@ -287,7 +289,7 @@ def linear_fwd(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloa
                workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
                stream=None) -> torch.Tensor:
     """Y = X W^T with X [T, Kin], W [Nout, Kin] (bf16, contiguous)."""
-    _on_gpu(X, W)
+    _on_gpu(X, W, workspace, out)
     T, Kin = X.shape
     Nout = W.shape[0]
     n = workspace_bytes(T, Kin, Nout, fmt, "fwd")
@@ -303,7 +305,7 @@ def linear_fwd_noalloc(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=tor
                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """linear_fwd without a workspace: the library's fixed device array holds the
     quantized operands (for callers that cannot allocate; up to 32 MiB)."""
-    _on_gpu(X, W)
+    _on_gpu(X, W, out)
     T, Kin = X.shape
     Nout = W.shape[0]
     Y = out if out is not None else torch.empty((T, Nout), dtype=out_dtype, device=X.device)
@@ -319,7 +321,7 @@ def linear_bwd(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor, fmt: str,
                need_dx: bool = True, need_dw: bool = True, workspace: torch.Tensor | None = None,
                dX: torch.Tensor | None = None, dW: torch.Tensor | None = None, stream=None):
     """dX = dY W and dW = dY^T X for the layer Y = X W^T."""
-    _on_gpu(dY, X, W)
+    _on_gpu(dY, X, W, workspace, dX, dW)
     T, Kin = X.shape
     Nout = W.shape[0]
     n = workspace_bytes(T, Kin, Nout, fmt, "bwd")

@@ -87,3 +87,16 @@ def test_size_queries_agree_with_the_oracle_layout(lib):
                 assert lib.mx_sf_bytes(f, rows, k) == orc.sf_bytes(rows, k // block), (name, rows, k)
             want = {"nvfp4": 1, "moss": 1, "nvfp4_local": max(1, -(-rows // 128))}.get(name, 0)
             assert lib.mx_scale_count(f, rows) == want, (name, rows)
+
+
+def test_host_memory_is_refused_before_the_library_is_called():
+    """The library reads and writes device memory only: operands, outputs and
+    workspaces in host memory are refused by the binding (no launch happens)."""
+    q = mx.MXTensor("mxfp8", 128, 64, "cpu")  # allocated in host memory
+    with pytest.raises(mx.MXError):
+        mx.gemm(q, q)
+    with pytest.raises(mx.MXError):
+        mx.dequantize(q)
+    x = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(mx.MXError):
+        mx.linear_fwd(x, x, "mxfp8", out=torch.zeros(64, 64, dtype=torch.bfloat16))
