@@ -194,8 +194,10 @@ int mx_dequantize(const mx_tensor* A, float* out, void* stream);
  * both operands carry the Hadamard transform ((H a)^T (H b) = 32 a^T b)
  * ([MOSS] GEMM Kernel 优化: dequantise once in the epilogue).
  * C is fp32 or bf16 (RNE), row stride ldc elements (ldc >= N, ldc % 8 == 0,
- * C 16-byte aligned).  K % 128 == 0 for FP8 formats, K % 256 == 0 for FP4.
- * A->hadamard must equal B->hadamard. */
+ * C 16-byte aligned); nothing outside the M x N view (columns N .. ldc - 1 of a
+ * row, rows past M) is written.  K % 128 == 0 for FP8 formats, K % 256 == 0 for
+ * FP4.  A->hadamard must equal B->hadamard.  Asynchronous on `stream`; the
+ * call allocates nothing and may be captured into a CUDA graph. */
 int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
             int out_dtype, void* stream);
 
