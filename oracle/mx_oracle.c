@@ -16,7 +16,9 @@
  *     comparison made here is exact.
  *   - Codes are found by searching the enumerated value grid, not by bit tricks.
  *
- * Parity pins for every function live in tests/test_oracle_pins.py.
+ * Parity pins for every function live in tests/test_oracle_pins.py; the
+ * quotients by the tensor scale (NVFP4 block-scale byte and element divisor,
+ * MOSS level 1) also in tests/test_oracle_quotient_pins.py.
  */
 #include "mx_oracle.h"
 
