@@ -159,7 +159,8 @@ class ClockSampler:
 
 GEMM_KERNEL_NAME = {"cta_n128": "bs_gemm_kernel<{fmt}, 128x128 tiles>",
                     "cta_n256": "bs_gemm_kernel<{fmt}, 128x256 tiles>",
-                    "pair": "bs_gemm_pair_kernel<{fmt}, 256x256 tiles, CTA pair>"}
+                    "pair": "bs_gemm_pair_kernel<{fmt}, 256x256 tiles, CTA pair>",
+                    "pair_ws": "bs_gemm_ws_kernel<{fmt}, 256x256 tiles, CTA pair, warp-specialised>"}
 
 
 def quant_bytes(fmt: str, elems: int, amax_pass: bool) -> float:

@@ -361,7 +361,7 @@ def debug_divide(v: torch.Tensor, d: torch.Tensor):
     return fast, ieee
 
 
-GEMM_VARIANTS = {"auto": 0, "cta_n128": 1, "cta_n256": 2, "pair": 3}
+GEMM_VARIANTS = {"auto": 0, "cta_n128": 1, "cta_n256": 2, "pair": 3, "pair_ws": 4}
 
 
 def set_gemm_variant(variant: str) -> None:

@@ -1073,6 +1073,516 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     return MX_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised CTA-pair kernel.  Same tiles, operand rings, scale-factor
+// layout and MMA loop as bs_gemm_pair_kernel, with the two jobs of that
+// kernel's epilogue warps given to separate warps, so that neither waits for
+// the other:
+//   warp 0        code-tile TMA producer (both CTAs).
+//   warp 1        TMEM allocation (both CTAs); in rank 0 the MMA loop.
+//   warp 2        scale-factor TMA producer (both CTAs).
+//   warp 3        idle.
+//   warps 4-7     scale-factor stores: warp 4 + q copies every stage's scale
+//                 chunks from the shared ring into lane quarter q of the
+//                 stage's TMEM slot with wide tcgen05.st, as soon as the MMAs
+//                 that last read that slot have completed.
+//   warps 8-15    epilogue: pull this CTA's 128 x 256 accumulator rows into
+//                 registers, release the accumulator, scale by alpha and write
+//                 the output.  bf16 / fp32 chunks are transposed through a
+//                 padded 32-row staging box per warp, so that each store
+//                 instruction writes eight rows of 64 contiguous bytes.
+// A stage's barrier counts the code bytes of both CTAs and one arrival from
+// each of the eight scale-store warps.  Warpgroups 0 and 1 hand registers to
+// the epilogue warpgroups (setmaxnreg), whose threads hold 128 accumulator
+// values each.
+template <int KIND, int STAGES_, int BKB_ = 128, int SFS_ = 5>
+struct CfgWs {
+    static constexpr int BM = 128, BN = 256;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int BKB = BKB_;
+    static constexpr int SUB = BKB / 128;
+    static constexpr int EPB = KIND == 0 ? 1 : 2;
+    static constexpr int BK = BKB * EPB;
+    static constexpr int BLOCK = KIND == 2 ? 16 : 32;
+    static constexpr int MMA_K_BYTES = 32;
+    static constexpr int MMAS = BKB / MMA_K_BYTES;
+    static constexpr int BPM = MMA_K_BYTES * EPB / BLOCK;
+    static constexpr int NCHUNK = MMAS * BPM / 4;  // 512-byte scale chunks per 128 rows per stage
+    static constexpr int A_BYTES = BM * BKB;
+    static constexpr int B_BYTES = (BN / 2) * BKB;
+    static constexpr int SFS = SFS_;
+    static constexpr int SFA_BYTES = NCHUNK * 512;
+    static constexpr int SFB_BYTES = 2 * NCHUNK * 512;
+    static constexpr int STG_PITCH = 80;  // 64 data bytes per staged row + 16 of padding (no bank conflicts)
+    static constexpr int STG_BOX = 32 * STG_PITCH;
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + SFS * SFA_BYTES;
+    static constexpr int OFF_STG = OFF_SFB + SFS * SFB_BYTES;
+    static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_BOX;
+    static constexpr int NBAR = 2 * STAGES + 3 + 2 * SFS;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+    static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+    static constexpr int SFA_COLS = 4 * NCHUNK;
+    static constexpr int SFB_COLS = 8 * NCHUNK;
+    static constexpr int TM_SFA = BN;
+    static constexpr int TM_SFB = TM_SFA + STAGES * SFA_COLS;
+    static constexpr int TM_USED = TM_SFB + STAGES * SFB_COLS;
+    static constexpr int TM_ALLOC = 512;
+    static constexpr int THREADS = 512;
+    static constexpr int REGS_LOW = 64;    // warpgroups 0 and 1
+    static constexpr int REGS_HIGH = 192;  // epilogue warpgroups 2 and 3
+    static constexpr uint32_t AB_TYPE = KIND == 0 ? 0u : 1u;
+    static constexpr uint32_t SF_E8M0 = KIND == 2 ? 0u : 1u;
+    static constexpr uint32_t TX = A_BYTES + B_BYTES;
+    static constexpr uint32_t SF_TX = SFA_BYTES + SFB_BYTES;
+    static_assert(TM_USED <= TM_ALLOC, "TMEM budget");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(NCHUNK == 1 || NCHUNK == 2 || NCHUNK == 4, "scale chunks per stage");
+    // the register pool the block launches with (128 per thread) covers the split
+    static_assert(128 * (REGS_LOW + REGS_LOW) + 256 * REGS_HIGH <= THREADS * 128, "register split");
+};
+
+template <int KIND, int STAGES, int BKB_ = 128, int SFS_ = 5>
+__global__ void __launch_bounds__(512, 1)
+    bs_gemm_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                      const PairParams p)
+{
+    using G = CfgWs<KIND, STAGES, BKB_, SFS_>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s0 = smem_u32(smem);
+    const uint32_t bar0 = s0 + G::OFF_BAR;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t accf = bar0 + 8u * (2 * STAGES);
+    const uint32_t acce = accf + 8u;
+    const uint32_t tdone = acce + 8u;
+    auto sffull = [&](int q) { return bar0 + 8u * (2 * STAGES + 3 + q); };
+    auto sfempty = [&](int q) { return bar0 + 8u * (2 * STAGES + 3 + G::SFS + q); };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + G::OFF_BAR + 8 * G::NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_ctarank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int num_kt = p.K / G::BK;
+    const int my_tiles = cluster_id < tiles ? (tiles - cluster_id + nclusters - 1) / nclusters : 0;
+    const int total_it = my_tiles * num_kt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 2 + 8);  // both code producers + four scale-store warps per CTA
+            mbar_init(empty(s), 1);     // rank 0's multicast commit
+        }
+        mbar_init(accf, 1);
+        mbar_init(acce, 2);
+        mbar_init(tdone, G::EPI_WARPS);
+        for (int q = 0; q < G::SFS; ++q) {
+            mbar_init(sffull(q), 1);   // this CTA's scale producer
+            mbar_init(sfempty(q), 4);  // this CTA's four scale-store warps
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmSFA);
+        prefetch_tmap(&tmSFB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), G::TM_ALLOC);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() {
+        atomicExch(p.status, MX_ERR_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    // Each warpgroup changes its register allotment at one point, before its
+    // warps take their roles.
+    if (warp < 8) {
+    regs_dec<G::REGS_LOW>();
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t full0_r0 = mapa_shared(full(0), 0);
+            int it = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
+                int mt, nt;
+                grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                const int arow = mt * 256 + static_cast<int>(rank) * 128;
+                const int brow = nt * 256 + static_cast<int>(rank) * 128;
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
+                    if (it >= STAGES && !mbar_wait_bounded(empty(s), (round - 1) & 1u, p.wait_ns))
+                        fail();
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = full0_r0 + 8u * s;
+                    mbar_arrive_expect_tx_cluster(fb, G::TX);
+#pragma unroll
+                    for (int sub = 0; sub < G::SUB; ++sub) {
+                        tma_load_2d_pair(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128), &tmA, fb,
+                                         kt * G::BKB + sub * 128, arow);
+                        tma_load_2d_pair(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128), &tmB, fb,
+                                         kt * G::BKB + sub * 128, brow);
+                    }
+                }
+            }
+            if (stop) {  // give copies already issued time to land before the CTA can exit
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (rank == 0) {
+            const bool leader = elect_one();
+            int it = 0, titer = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters, ++titer) {
+                if (titer > 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait_bounded(acce, static_cast<uint32_t>(titer - 1) & 1u, p.wait_ns))) {
+                    if (leader)
+                        fail();
+                    break;
+                }
+                tc_fence_after();
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t round = static_cast<uint32_t>(it / STAGES);
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(full(s), round & 1u, p.wait_ns))) {
+                        if (leader)
+                            fail();
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem + G::TM_SFA + s * G::SFA_COLS;
+                    const uint32_t sfb_t = tmem + G::TM_SFB + s * G::SFB_COLS;
+                    if (leader) {
+#pragma unroll
+                        for (int i = 0; i < G::MMAS; ++i) {
+                            constexpr int PER_SUB = 128 / G::MMA_K_BYTES;
+                            const int sub = i / PER_SUB;
+                            const uint64_t adesc =
+                                sdesc_kmajor_sw128(s0 + G::OFF_A + s * G::A_BYTES + sub * (G::BM * 128));
+                            const uint64_t bdesc =
+                                sdesc_kmajor_sw128(s0 + G::OFF_B + s * G::B_BYTES + sub * ((G::BN / 2) * 128));
+                            const int fb = i * G::BPM;
+                            const int chunk = fb / 4;
+                            const uint32_t sf_id = static_cast<uint32_t>(fb % 4);
+                            const uint32_t idesc = idesc_block_scaled(G::AB_TYPE, G::SF_E8M0, 256, G::BN, sf_id, sf_id);
+                            const uint64_t koff = static_cast<uint64_t>(((i % PER_SUB) * G::MMA_K_BYTES) >> 4);
+                            mma_bs_pair<KIND>(tmem, adesc + koff, bdesc + koff, idesc, sfa_t + 4 * chunk,
+                                              sfb_t + 8 * chunk, (kt > 0 || i > 0) ? 1u : 0u);
+                        }
+                        tc_commit_pair(empty(s), 0x3);
+                    }
+                    __syncwarp();
+                }
+                if (leader)
+                    tc_commit_pair(accf, 0x3);
+                __syncwarp();
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0) {
+            int it = 0;
+            bool stop = false;
+            for (int tile = cluster_id; tile < tiles && !stop; tile += nclusters) {
+                int mt, nt;
+                grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+                for (int kt = 0; kt < num_kt; ++kt, ++it) {
+                    const int q = it % G::SFS;
+                    const uint32_t round = static_cast<uint32_t>(it / G::SFS);
+                    if (it >= G::SFS && !mbar_wait_bounded(sfempty(q), (round - 1) & 1u, p.wait_ns))
+                        fail();
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const int cha = static_cast<int>((mt * 2 + static_cast<int>(rank)) * p.kgroups + kt * G::NCHUNK);
+                    const uint32_t fl = sffull(q);
+                    mbar_arrive_expect_tx(fl, G::SF_TX);
+                    tma_load_2d(s0 + G::OFF_SFA + q * G::SFA_BYTES, &tmSFA, fl, 0, cha * 4);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int chb = static_cast<int>((nt * 2 + r) * p.kgroups + kt * G::NCHUNK);
+                        tma_load_2d(s0 + G::OFF_SFB + q * G::SFB_BYTES + r * (G::SFB_BYTES / 2), &tmSFB, fl, 0,
+                                    chb * 4);
+                    }
+                }
+            }
+            if (stop) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // Scale-factor stores into lane quarter q.  Lane l of the quarter gets
+        // line l of every 512-byte chunk (the scales of rows l, l + 32, l + 64,
+        // l + 96); A's chunks fill the slot's SFA columns in order, B's chunk c
+        // of row tile r fills columns 8c + 4r .. 8c + 4r + 3 of its SFB columns.
+        const int q = warp & 3;
+        const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t full0_r0 = mapa_shared(full(0), 0);
+        for (int it = 0; it < total_it; ++it) {
+            const int s = it % STAGES;
+            const int qs = it % G::SFS;
+            bool ok = mbar_wait_bounded(sffull(qs), static_cast<uint32_t>(it / G::SFS) & 1u, p.wait_ns) &&
+                      (it < STAGES ||
+                       mbar_wait_bounded(empty(s), static_cast<uint32_t>(it / STAGES - 1) & 1u, p.wait_ns));
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok || *abort_flag) {
+                if (lane == 0 && !ok)
+                    fail();
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sfa_s = s0 + G::OFF_SFA + qs * G::SFA_BYTES + lane * 16;
+            const uint32_t sfb_s = s0 + G::OFF_SFB + qs * G::SFB_BYTES + lane * 16;
+            uint4 va[G::NCHUNK];
+#pragma unroll
+            for (int c = 0; c < G::NCHUNK; ++c)
+                va[c] = lds128(sfa_s + c * 512);
+            uint4 vb[2 * G::NCHUNK];
+#pragma unroll
+            for (int c = 0; c < G::NCHUNK; ++c)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    vb[2 * c + r] = lds128(sfb_s + (r * G::NCHUNK + c) * 512);
+            tmem_st_wide<G::NCHUNK>(tmem + lanes + G::TM_SFA + s * G::SFA_COLS, va);
+            tmem_st_wide<2 * G::NCHUNK>(tmem + lanes + G::TM_SFB + s * G::SFB_COLS, vb);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(sfempty(qs));
+                mbar_arrive_cluster(full0_r0 + 8u * s);
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        regs_inc<G::REGS_HIGH>();
+        const int ew = warp - 8;   // 0 .. 7
+        const int q = warp & 3;    // TMEM lane quarter this warp may access
+        const int half = ew >> 2;  // accumulator columns half*128 .. +127
+        const uint32_t acce_r0 = mapa_shared(acce, 0);
+        const float ta = p.tsa ? *p.tsa : 1.0f, tb = p.tsb ? *p.tsb : 1.0f;
+        const float alpha = __fmul_rn(__fmul_rn(ta, tb), p.extra);
+        uint8_t* stg = smem + G::OFF_STG + ew * G::STG_BOX;
+        const bool bf16 = p.out_mode == EPI_BF16;
+        const int esz = bf16 ? 2 : 4;
+        int titer = 0;
+        for (int tile = cluster_id; tile < tiles; tile += nclusters, ++titer) {
+            int mt, nt;
+            grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+            const bool acc_ok =
+                __all_sync(0xffffffffu, mbar_wait_bounded(accf, static_cast<uint32_t>(titer) & 1u, p.wait_ns));
+            if (!acc_ok || *abort_flag) {
+                if (lane == 0 && !acc_ok)
+                    fail();
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * 128 + j * 32, r[j]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(tdone);
+            if (ew == 0 && lane == 0) {
+                if (mbar_wait_bounded(tdone, static_cast<uint32_t>(titer) & 1u, p.wait_ns))
+                    mbar_arrive_cluster(acce_r0);
+                else
+                    fail();
+            }
+            const int row0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
+            const int row = row0 + lane;
+            if (row0 >= p.M)
+                continue;
+            if (p.out_mode <= EPI_BF16) {
+                // One 64-byte piece per row (32 bf16 or 16 fp32 columns) goes
+                // through the staging box: lane l writes row l, then lane l reads
+                // 16 bytes of row 8i + l/4 and stores them.
+                auto emit = [&](const uint32_t (&pk)[16], int col) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        *reinterpret_cast<uint4*>(stg + lane * G::STG_PITCH + w * 16) =
+                            make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    __syncwarp();
+                    const int piece = lane & 3;
+                    const int per_piece = 16 / esz;  // columns per 16 bytes
+                    const int c = col + piece * per_piece;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = 8 * i + (lane >> 2);
+                        const int grow = row0 + rr;
+                        const uint4 v = *reinterpret_cast<const uint4*>(stg + rr * G::STG_PITCH + piece * 16);
+                        if (grow < p.M && c < p.N) {
+                            uint8_t* dst = static_cast<uint8_t*>(p.c) + (static_cast<int64_t>(grow) * p.ldc + c) * esz;
+                            if (c + per_piece <= p.N) {
+                                st_global_v4(dst, v);
+                            } else {
+                                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                                for (int e = 0; e < per_piece && c + e < p.N; ++e) {
+                                    if (bf16)
+                                        reinterpret_cast<uint16_t*>(dst)[e] =
+                                            static_cast<uint16_t>(w4[e >> 1] >> (16 * (e & 1)));
+                                    else
+                                        reinterpret_cast<uint32_t*>(dst)[e] = w4[e];
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                };
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col0 = nt * 256 + half * 128 + j * 32;
+                    if (col0 >= p.N)
+                        break;
+                    const float al =
+                        (p.ts_region && row < p.M) ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    uint32_t pk[16];
+                    if (bf16) {
+#pragma unroll
+                        for (int h = 0; h < 16; ++h) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[j][2 * h]), al),
+                                                                            __fmul_rn(__uint_as_float(r[j][2 * h + 1]), al));
+                            pk[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                        emit(pk, col0);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 16; ++h)
+                            pk[h] = __float_as_uint(__fmul_rn(__uint_as_float(r[j][h]), al));
+                        emit(pk, col0);
+                        if (col0 + 16 < p.N) {
+#pragma unroll
+                            for (int h = 0; h < 16; ++h)
+                                pk[h] = __float_as_uint(__fmul_rn(__uint_as_float(r[j][16 + h]), al));
+                            emit(pk, col0 + 16);
+                        }
+                    }
+                }
+            } else if (row < p.M) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int col0 = nt * 256 + half * 128 + j * 32;
+                    if (col0 >= p.N)
+                        break;
+                    const float al = p.ts_region ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
+                    store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // remote arrivals and the peer's TMEM reads are finished
+    if (warp == 1) {
+        if (*abort_flag && lane == 0 && rank == 0)
+            (void)mbar_wait_bounded(accf, 0, kWaitLimitNs);
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, G::TM_ALLOC);
+    }
+}
+
+template <int KIND, int STAGES, int BKB_ = 128, int SFS = 5>
+int launch_ws(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
+              uint8_t* q_sf, const Device& d, cudaStream_t s)
+{
+    using G = CfgWs<KIND, STAGES, BKB_, SFS>;
+    auto kernel = bs_gemm_ws_kernel<KIND, STAGES, BKB_, SFS>;
+    static int configured_device = -1;
+    static int max_clusters = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(G::THREADS);
+    cfg.dynamicSmemBytes = G::SMEM_ALLOC;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (configured_device != d.id) {
+        // The register split (setmaxnreg) assumes the kernel launches with 128
+        // registers per thread: with fewer, the epilogue's increase could not be
+        // met, so such a build is refused instead of launched.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.numRegs != 128)
+            return MX_ERR_UNSUPPORTED;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM_ALLOC) != cudaSuccess)
+            return MX_ERR_CUDA;
+        cfg.gridDim = dim3(2 * (d.sms / 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1)
+            return MX_ERR_CUDA;
+        max_clusters = n;
+        configured_device = d.id;
+    }
+    const int64_t M = A->rows, N = B->rows, K = A->k;
+    const int64_t kbytes = K / G::EPB;
+    CUtensorMap ta, tb, tsa, tsb;
+    const int64_t sfa_bytes = sf_layout_bytes(M, K / G::BLOCK), sfb_bytes = sf_layout_bytes(N, K / G::BLOCK);
+    if (!make_code_map(&ta, A->codes, M, kbytes, 128) || !make_code_map(&tb, B->codes, N, kbytes, 128) ||
+        !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
+        return MX_ERR_CUDA;
+    PairParams p;
+    p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
+    p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
+    p.extra = extra;
+    p.c = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.out_mode = out_mode;
+    p.ts_region = fmt_is_local(A->fmt) ? 1 : 0;
+    p.q_sf = q_sf;
+    p.q_kgroups = sf_kgroups(N / 32);
+    p.kgroups = sf_kgroups(K / G::BLOCK);
+    p.m_tiles = static_cast<int>((M + 255) / 256);
+    p.n_tiles = static_cast<int>((N + 255) / 256);
+    p.group_m = raster_group_m(M, N, kbytes, 256, p.m_tiles);
+    p.status = d.status;
+    p.wait_ns = kWaitLimitNs;
+    const int tiles = p.m_tiles * p.n_tiles;
+    cfg.gridDim = dim3(2 * std::min(tiles, max_clusters));
+    if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, p) != cudaSuccess)
+        return MX_ERR_CUDA;
+    count_launch();
+    return MX_OK;
+}
+
 template <int KIND>
 int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
                 uint8_t* q_sf, const Device& d, cudaStream_t s, int bn)
@@ -1085,7 +1595,8 @@ int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 }  // namespace
 
 // Kernel override for tests: 0 = automatic, 1 = single CTA with N = 128,
-// 2 = single CTA with N = 256, 3 = CTA pair (256 x 256 tiles).
+// 2 = single CTA with N = 256, 3 = CTA pair (256 x 256 tiles), 4 = the
+// warp-specialised CTA pair.
 static int g_variant = 0;
 static int g_last_variant = 0;  // the variant the last launch_gemm chose
 
@@ -1096,10 +1607,10 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         return MX_OK;
     int v = g_variant;
     if (v == 0) {
-        // CTA pairs once there are enough 256 x 256 tiles to fill the GPU;
+        // warp-specialised CTA pairs once there are enough 256 x 256 tiles to fill the GPU;
         // single-CTA tiles for small problems, where more, smaller tiles win.
         const int64_t pair_tiles = ((A->rows + 255) / 256) * ((B->rows + 255) / 256);
-        v = pair_tiles >= d.sms / 2 ? 3 : (B->rows > 128 ? 2 : 1);
+        v = pair_tiles >= d.sms / 2 ? 4 : (B->rows > 128 ? 2 : 1);
     }
     g_last_variant = v;
     const int kind = (A->fmt == MX_FMT_MXFP8_E4M3 || A->fmt == MX_FMT_MOSS_FP8) ? 0
@@ -1108,6 +1619,19 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
                                                                                 : -1;
     if (kind < 0)
         return MX_ERR_INVALID_ARG;
+    if (v == 4) {
+        switch (kind) {
+        case 0:
+            if (A->k % 256 == 0)
+                return launch_ws<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_ws<0, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        case 1:
+            if (A->k % 512 == 0)
+                return launch_ws<1, 3, 256, 2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+            return launch_ws<1, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        default: return launch_ws<2, 5, 128, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+        }
+    }
     if (v == 3) {
         switch (kind) {
         // MXFP8 / MXFP4: three stages of 256 K-bytes (eight MMAs per stage halve
@@ -1132,7 +1656,7 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
     }
 }
 
-void set_gemm_variant(int v) { g_variant = (v >= 0 && v <= 3) ? v : 0; }
+void set_gemm_variant(int v) { g_variant = (v >= 0 && v <= 4) ? v : 0; }
 int last_gemm_variant() { return g_last_variant; }
 
 }  // namespace mx

@@ -217,7 +217,61 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v)
                  : "memory");
 }
 
+// Each thread of the warp writes 4*N consecutive 32-bit columns of its TMEM
+// lane from N 16-byte values (v[0] to the first four columns).
+template <int N>
+__device__ __forceinline__ void tmem_st_wide(uint32_t taddr, const uint4 (&v)[N])
+{
+    static_assert(N == 1 || N == 2 || N == 4 || N == 8, "4, 8, 16 or 32 columns");
+    if constexpr (N == 1) {
+        tmem_st4(taddr, v[0]);
+    } else if constexpr (N == 2) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                     "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+                     "r"(v[1].w)
+                     : "memory");
+    } else if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15, %16};" ::"r"(taddr),
+                     "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+                     "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y),
+                     "r"(v[3].z), "r"(v[3].w)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+                     "%31, %32};" ::"r"(taddr),
+                     "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+                     "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y),
+                     "r"(v[3].z), "r"(v[3].w), "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x),
+                     "r"(v[5].y), "r"(v[5].z), "r"(v[5].w), "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w),
+                     "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w)
+                     : "memory");
+    }
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Warpgroup register reallocation: every thread of the warpgroup executes the
+// same instruction.  The block's register pool is its threads x the registers
+// per thread it was launched with; the increases must fit in what the
+// decreases return, or the increasing warps wait.
+template <int R>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t saddr)
 {

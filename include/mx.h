@@ -292,7 +292,9 @@ void mx_debug_set_quant_impl(int impl);
 
 /* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
  * calls, process-wide: 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA
- * 128 x 256 tiles, 3 CTA-pair (cluster of two) 256 x 256 tiles. */
+ * 128 x 256 tiles, 3 CTA-pair (cluster of two) 256 x 256 tiles, 4 the
+ * warp-specialised CTA pair (scale-factor stores and the epilogue in separate
+ * warps; the automatic choice for large shapes). */
 void mx_debug_set_gemm_variant(int variant);
 
 /* Test/benchmark hook: the GEMM variant (numbered as above, never 0) that the

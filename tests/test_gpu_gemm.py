@@ -29,7 +29,7 @@ def quant_pair(mx, a, b, fmt, **kw):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
-@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair", "pair_ws"])
 def test_exact_small_integers(mx, fmt, variant):
     """Small-integer codes with power-of-two scales: every partial sum is exact in
     fp32, so the tensor core must reproduce the fp64 oracle bit for bit."""
@@ -46,7 +46,7 @@ def test_exact_small_integers(mx, fmt, variant):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair", "pair_ws"])
 def test_scale_factor_layout_one_hot(mx, fmt, variant):
     """Pins the swizzled scale layout against the hardware: with all-ones inputs,
     raise single scale bytes of A and of B in the GPU buffers (at the offsets the
@@ -83,7 +83,7 @@ def test_random_gemm(mx, fmt, mnk, out_dtype):
     a = workloads.draw("student_t3", (M, K), 40 + M)
     b = workloads.draw("normal", (N, K), 41 + N, 0.02)
     qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
-    for variant in ("cta_n128", "cta_n256", "pair"):
+    for variant in ("cta_n128", "cta_n256", "pair", "pair_ws"):
         mx.set_gemm_variant(variant)
         c = mx.gemm(qa, qb, out_dtype=out_dtype)
         ref, cabs = orc.gemm(ra, rb)
@@ -124,10 +124,11 @@ def test_gemm_k_alignment_rejected(mx):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_pair_kernel_many_tiles_and_tails(mx, fmt):
+@pytest.mark.parametrize("pv", ["pair", "pair_ws"])
+def test_pair_kernel_many_tiles_and_tails(mx, pv, fmt):
     """Enough 256 x 256 tiles that every cluster runs several (persistent
     loop, accumulator hand-off between tiles), with ragged M and N tails."""
-    mx.set_gemm_variant("pair")
+    mx.set_gemm_variant(pv)
     M, N, K = 1280 + 72, 1536 + 40, 512
     a = workloads.draw("student_t3", (M, K), 77)
     b = workloads.draw("normal", (N, K), 78, 0.02)
@@ -143,7 +144,7 @@ def test_pair_kernel_many_tiles_and_tails(mx, fmt):
 # ------------------------------------------------ quantized epilogue (next layer)
 @pytest.mark.parametrize("in_fmt", FMTS)
 @pytest.mark.parametrize("out_fmt", ["mxfp8", "mxfp4"])
-@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair"])
+@pytest.mark.parametrize("variant", ["cta_n128", "cta_n256", "pair", "pair_ws"])
 def test_gemm_quantized_epilogue(mx, in_fmt, out_fmt, variant):
     """The operand the epilogue writes equals the oracle's rowwise MX quantization
     of the same kernel's fp32 output, bit for bit: both runs issue the same MMAs
@@ -152,21 +153,25 @@ def test_gemm_quantized_epilogue(mx, in_fmt, out_fmt, variant):
     M, N, K = 424, 640, 512
     a = workloads.draw("student_t3", (M, K), 91)
     b = workloads.draw("normal", (N, K), 92, 0.02)
-    qa, qb, _, _ = quant_pair(mx, a, b, in_fmt)
+    qa, qb, ra, rb = quant_pair(mx, a, b, in_fmt)
     c32 = mx.gemm(qa, qb, extra_alpha=0.75, out_dtype=torch.float32)
     q = mx.gemm_quantized(qa, qb, out_fmt, extra_alpha=0.75)
     torch.cuda.synchronize()
     assert (q.rows, q.k) == (M, N)
+    # the fp32 result the epilogue quantizes is itself the oracle GEMM within 1e-3
+    ref, cabs = orc.gemm(ra, rb, extra_alpha=0.75)
+    assert_gemm_close(c32, ref, cabs, f"{in_fmt} fp32 before the epilogue quantizer {variant}")
     assert_quant_equal(q, orc.quantize_rows_f32(c32.cpu().numpy(), out_fmt), f"{in_fmt}->{out_fmt} {variant}")
     mx.set_gemm_variant("auto")
 
 
 @pytest.mark.parametrize("out_fmt", ["mxfp8", "mxfp4"])
-def test_gemm_quantized_many_tiles_feeds_next_gemm(mx, out_fmt):
+@pytest.mark.parametrize("pv", ["pair", "pair_ws"])
+def test_gemm_quantized_many_tiles_feeds_next_gemm(mx, pv, out_fmt):
     """Pair kernel over many 256 x 256 tiles with a ragged M tail; the result is a
     valid operand: a second GEMM consuming it matches the oracle GEMM of the
     oracle-quantized first result."""
-    mx.set_gemm_variant("pair")
+    mx.set_gemm_variant(pv)
     # N is the next GEMM's K (a multiple of 128 / 256); 1408 leaves a ragged 256-column tile
     M, N, K = 1280 + 72, (1408 if out_fmt == "mxfp8" else 1792), 512
     a = workloads.draw("student_t3", (M, K), 93)
@@ -199,10 +204,11 @@ def test_gemm_quantized_rejects(mx):
 
 
 @pytest.mark.parametrize("fmt,K", [("mxfp8", 384), ("mxfp8", 1280), ("mxfp4", 768), ("mxfp4", 1536)])
-def test_pair_kernel_both_stage_depths(mx, fmt, K):
+@pytest.mark.parametrize("pv", ["pair", "pair_ws"])
+def test_pair_kernel_both_stage_depths(mx, pv, fmt, K):
     """K a multiple of 256 bytes takes the three-stage ring of 256-byte K-stages,
     otherwise the five-stage ring of 128-byte stages: both against the oracle."""
-    mx.set_gemm_variant("pair")
+    mx.set_gemm_variant(pv)
     M, N = 512 + 64, 768 + 32
     a = workloads.draw("student_t3", (M, K), 101)
     b = workloads.draw("normal", (N, K), 102, 0.02)
@@ -216,7 +222,8 @@ def test_pair_kernel_both_stage_depths(mx, fmt, K):
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("mnk", [(33, 40, 256), (300, 1000, 512), (257, 264, 1024)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_pair_output_stays_inside_a_strided_view(mx, fmt, mnk, out_dtype):
+@pytest.mark.parametrize("pv", ["pair", "pair_ws"])
+def test_pair_output_stays_inside_a_strided_view(mx, pv, fmt, mnk, out_dtype):
     """The CTA-pair kernel writes its bf16 / fp32 output (TMA stores of 32-row
     boxes, clipped at M and N) into a view of a wider, taller buffer: every
     element of the view matches the oracle and nothing past column N or row M
@@ -228,7 +235,7 @@ def test_pair_output_stays_inside_a_strided_view(mx, fmt, mnk, out_dtype):
     ld = ((N + 24 + 7) // 8) * 8
     buf = torch.full((M + 16, ld), float("nan"), dtype=out_dtype, device="cuda")
     out = buf[:M, :N]
-    mx.set_gemm_variant("pair")
+    mx.set_gemm_variant(pv)
     try:
         mx.gemm(qa, qb, out=out)
     finally:
@@ -241,7 +248,8 @@ def test_pair_output_stays_inside_a_strided_view(mx, fmt, mnk, out_dtype):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("K", [256, 512])
-def test_pair_kernel_short_k_many_tiles(mx, fmt, K):
+@pytest.mark.parametrize("pv", ["pair", "pair_ws"])
+def test_pair_kernel_short_k_many_tiles(mx, pv, fmt, K):
     """Every cluster runs several tiles of one or two K-stages, so the
     epilogue warps' scale stores run ahead across several future tiles and the
     accumulator changes hands every stage or two."""
@@ -250,7 +258,7 @@ def test_pair_kernel_short_k_many_tiles(mx, fmt, K):
     b = workloads.draw("normal", (N, K), 96 + K, 0.02)
     qa, qb, ra, rb = quant_pair(mx, a, b, fmt)
     rows = np.r_[0:32, 2048:2080, M - 64:M]
-    mx.set_gemm_variant("pair")
+    mx.set_gemm_variant(pv)
     try:
         for out_dtype in (torch.float32, torch.bfloat16):
             c = mx.gemm(qa, qb, out_dtype=out_dtype)
