@@ -30,7 +30,8 @@ MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_scale_count", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
             "mx_gemm_quantized",
-            "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd", "mx_strerror",
+            "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd",
+            "mx_linear_saved_bytes", "mx_linear_fwd_save", "mx_linear_bwd_saved", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
             "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_gemm_variant",
             "mx_debug_last_gemm_variant")
@@ -105,6 +106,14 @@ def lib():
             L.mx_linear_bwd.restype = i32
             L.mx_linear_bwd.argtypes = [p, p, p, i64, i64, i64, i32, C.POINTER(_CBwdOpts), p, i32, p,
                                         i32, p, sz, p]
+            L.mx_linear_saved_bytes.restype = sz
+            L.mx_linear_saved_bytes.argtypes = [i64, i64, i64, i32]
+            L.mx_linear_fwd_save.restype = i32
+            L.mx_linear_fwd_save.argtypes = [p, p, i64, i64, i64, i32, p, p, C.POINTER(_CBwdOpts), p, i32, p, sz,
+                                             p, sz, p]
+            L.mx_linear_bwd_saved.restype = i32
+            L.mx_linear_bwd_saved.argtypes = [p, i64, i64, i64, i32, p, C.POINTER(_CBwdOpts), p, sz, p, i32, p, i32,
+                                              p, sz, p]
             L.mx_strerror.restype = C.c_char_p
             L.mx_strerror.argtypes = [i32]
             L.mx_last_device_status.restype = i32
@@ -281,8 +290,16 @@ def gemm_quantized(a: MXTensor, b: MXTensor, fmt: str = "mxfp8", extra_alpha: fl
     return out
 
 
+PASSES = {"fwd": 0, "bwd": 1, "bwd_saved": 2}
+
+
 def workspace_bytes(T: int, Kin: int, Nout: int, fmt: str, pass_: str = "fwd") -> int:
-    return int(lib().mx_linear_workspace_bytes(T, Kin, Nout, FORMATS[fmt], 0 if pass_ == "fwd" else 1))
+    return int(lib().mx_linear_workspace_bytes(T, Kin, Nout, FORMATS[fmt], PASSES[pass_]))
+
+
+def saved_bytes(T: int, Kin: int, Nout: int, fmt: str) -> int:
+    """Bytes of one layer's saved backward state (X^T and W^T operands)."""
+    return int(lib().mx_linear_saved_bytes(T, Kin, Nout, FORMATS[fmt]))
 
 
 def linear_fwd(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloat16,
@@ -336,6 +353,57 @@ def linear_bwd(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor, fmt: str,
                              _ptr(dW) if need_dw else None, OUT[dW.dtype] if need_dw else 0,
                              _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "mx_linear_bwd")
+    return dX, dW
+
+
+def _bwd_opts(wgrad_hadamard, wgrad_dy_rounding, seed, stream_id):
+    return _CBwdOpts(int(bool(wgrad_hadamard)), ROUNDING[wgrad_dy_rounding], seed, stream_id, 0)
+
+
+def linear_fwd_save(X: torch.Tensor, W: torch.Tensor, fmt: str, out_dtype=torch.bfloat16,
+                    wgrad_hadamard: bool = False, wgrad_dy_rounding: str = "rne", seed: int = 0,
+                    stream_id: int = 0, x_amax: torch.Tensor | None = None, w_amax: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, saved: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None, stream=None):
+    """Y = X W^T plus the layer's saved backward state (one read each of X and W).
+    Returns (Y, saved); pass `saved` and the same backward options to linear_bwd_saved."""
+    _on_gpu(X, W, x_amax, w_amax, workspace, saved, out)
+    T, Kin = X.shape
+    Nout = W.shape[0]
+    ws = workspace if workspace is not None else torch.empty(workspace_bytes(T, Kin, Nout, fmt, "fwd"),
+                                                             dtype=torch.uint8, device=X.device)
+    sv = saved if saved is not None else torch.empty(saved_bytes(T, Kin, Nout, fmt), dtype=torch.uint8,
+                                                     device=X.device)
+    Y = out if out is not None else torch.empty((T, Nout), dtype=out_dtype, device=X.device)
+    o = _bwd_opts(wgrad_hadamard, wgrad_dy_rounding, seed, stream_id)
+    rc = lib().mx_linear_fwd_save(_ptr(X), _ptr(W), T, Kin, Nout, FORMATS[fmt], _ptr(x_amax), _ptr(w_amax),
+                                  C.byref(o), _ptr(Y), OUT[Y.dtype], _ptr(ws), ws.numel(), _ptr(sv), sv.numel(),
+                                  _stream(stream))
+    _check(rc, "mx_linear_fwd_save")
+    return Y, sv
+
+
+def linear_bwd_saved(dY: torch.Tensor, saved: torch.Tensor, Kin: int, fmt: str,
+                     wgrad_hadamard: bool = False, wgrad_dy_rounding: str = "rne", seed: int = 0,
+                     stream_id: int = 0, dy_amax: torch.Tensor | None = None, dx_dtype=torch.bfloat16,
+                     dw_dtype=torch.float32, need_dx: bool = True, need_dw: bool = True,
+                     workspace: torch.Tensor | None = None, dX: torch.Tensor | None = None,
+                     dW: torch.Tensor | None = None, stream=None):
+    """dX = dY W and dW = dY^T X from the state linear_fwd_save kept (one read of dY)."""
+    _on_gpu(dY, saved, dy_amax, workspace, dX, dW)
+    T, Nout = dY.shape
+    ws = workspace if workspace is not None else torch.empty(workspace_bytes(T, Kin, Nout, fmt, "bwd_saved"),
+                                                             dtype=torch.uint8, device=dY.device)
+    if need_dx and dX is None:
+        dX = torch.empty((T, Kin), dtype=dx_dtype, device=dY.device)
+    if need_dw and dW is None:
+        dW = torch.empty((Nout, Kin), dtype=dw_dtype, device=dY.device)
+    o = _bwd_opts(wgrad_hadamard, wgrad_dy_rounding, seed, stream_id)
+    rc = lib().mx_linear_bwd_saved(_ptr(dY), T, Kin, Nout, FORMATS[fmt], _ptr(dy_amax), C.byref(o), _ptr(saved),
+                                   saved.numel(), _ptr(dX) if need_dx else None, OUT[dX.dtype] if need_dx else 0,
+                                   _ptr(dW) if need_dw else None, OUT[dW.dtype] if need_dw else 0,
+                                   _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "mx_linear_bwd_saved")
     return dX, dW
 
 

@@ -1597,8 +1597,10 @@ int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
 // Kernel override for tests: 0 = automatic, 1 = single CTA with N = 128,
 // 2 = single CTA with N = 256, 3 = CTA pair (256 x 256 tiles), 4 = the
 // warp-specialised CTA pair.
-static int g_variant = 0;
-static int g_last_variant = 0;  // the variant the last launch_gemm chose
+// Both are per host thread, so a test or tuning run that forces a variant
+// changes nothing for the library's other callers.
+static thread_local int g_variant = 0;
+static thread_local int g_last_variant = 0;  // the variant this thread's last launch_gemm chose
 
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_mode,
                 const Device& d, cudaStream_t s, uint8_t* q_sf)

@@ -105,8 +105,9 @@ size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
 }
 
 // Producer implementation for tests and tuning: 0 automatic (direct loads
-// rowwise, tile producer colwise), 1 direct loads, 2 tile producer.
-int g_quant_impl = 0;
+// rowwise, tile producer colwise), 1 direct loads, 2 tile producer.  Per host
+// thread, like the GEMM variant override.
+thread_local int g_quant_impl = 0;
 
 // Shared argument checks of the single and dual producers.
 int check_quantize_args(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int rule)
@@ -500,6 +501,10 @@ size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, 
         return 0;
     if (pass == 0)
         return carve(nullptr, fmt, T, Kin, nullptr) + carve(nullptr, fmt, Nout, Kin, nullptr);
+    if (pass == 2)  // mx_linear_bwd_saved: dY rowwise [T, Nout] and dY^T [Nout, T]
+        return carve(nullptr, fmt, T, Nout, nullptr) + carve(nullptr, fmt, Nout, T, nullptr);
+    if (pass != 1)
+        return 0;
     // dgrad: dY rowwise [T, Nout], W^T [Kin, Nout]; wgrad: dY^T [Nout, T], X^T [Kin, T]
     return carve(nullptr, fmt, T, Nout, nullptr) + carve(nullptr, fmt, Kin, Nout, nullptr) +
            carve(nullptr, fmt, Nout, T, nullptr) + carve(nullptr, fmt, Kin, T, nullptr);
@@ -592,6 +597,113 @@ int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64
             return rc;
         rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s);
     }
+    return rc;
+}
+
+size_t mx_linear_saved_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return 0;
+    return carve(nullptr, fmt, Kin, T, nullptr) + carve(nullptr, fmt, Kin, Nout, nullptr);  // X^T, W^T
+}
+
+namespace {
+
+// The saved backward state of one layer: the colwise operands X^T [Kin, T]
+// (for the weight gradient) and W^T [Kin, Nout] (for the data gradient), in
+// that order, carved like a workspace.
+void carve_saved(uint8_t* saved, int64_t T, int64_t Kin, int64_t Nout, int fmt, int wgrad_hadamard, mx_tensor* xt,
+                 mx_tensor* wt)
+{
+    const size_t off = carve(saved, fmt, Kin, T, xt);
+    carve(saved + off, fmt, Kin, Nout, wt);
+    fill_meta(xt, Kin, T, fmt, wgrad_hadamard);
+    fill_meta(wt, Kin, Nout, fmt, 0);
+}
+
+}  // namespace
+
+int mx_linear_fwd_save(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt,
+                       const float* x_amax, const float* w_amax, const mx_bwd_opts* opts, void* Y, int out_dtype,
+                       void* workspace, size_t ws_bytes, void* saved, size_t saved_bytes, void* stream)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return MX_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < mx_linear_workspace_bytes(T, Kin, Nout, fmt, 0) || !saved ||
+        saved_bytes < mx_linear_saved_bytes(T, Kin, Nout, fmt))
+        return MX_ERR_WORKSPACE;
+    if (fmt_is_local(fmt) && (x_amax || w_amax))
+        return MX_ERR_UNSUPPORTED;  // the region maxima of both directions come from the pass itself
+    mx_bwd_opts o;
+    std::memset(&o, 0, sizeof o);
+    if (opts)
+        o = *opts;
+    Device d;
+    int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mx_tensor xq, wq, xt, wt;
+    const size_t off = carve(ws, fmt, T, Kin, &xq);
+    carve(ws + off, fmt, Nout, Kin, &wq);
+    carve_saved(static_cast<uint8_t*>(saved), T, Kin, Nout, fmt, o.wgrad_hadamard, &xt, &wt);
+    const int block = fmt_block(fmt);
+    // one read of X: the forward operand and X^T, transformed as the weight gradient will want it
+    rc = quantize_dual_impl(X, T, Kin, Kin, fmt, block, MX_SCALE_DEFAULT, 0, 0, MX_ROUND_RNE, 0, MX_ROUND_RNE,
+                            o.wgrad_hadamard, x_amax, &xq, &xt, d, s);
+    if (rc != MX_OK)
+        return rc;
+    // one read of W: the forward operand and W^T for the data gradient
+    rc = quantize_dual_impl(W, Nout, Kin, Kin, fmt, block, MX_SCALE_DEFAULT, 0, 0, MX_ROUND_RNE, 0, MX_ROUND_RNE, 0,
+                            w_amax, &wq, &wt, d, s);
+    if (rc != MX_OK)
+        return rc;
+    return gemm_impl(&xq, &wq, 1.0f, Y, Nout, out_dtype, d, s);
+}
+
+int mx_linear_bwd_saved(const void* dY, int64_t T, int64_t Kin, int64_t Nout, int fmt, const float* dy_amax,
+                        const mx_bwd_opts* opts, const void* saved, size_t saved_bytes, void* dX, int dx_dtype,
+                        void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream)
+{
+    if (!valid_fmt(fmt) || T < 0 || Kin < 0 || Nout < 0)
+        return MX_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < mx_linear_workspace_bytes(T, Kin, Nout, fmt, 2) || !saved ||
+        saved_bytes < mx_linear_saved_bytes(T, Kin, Nout, fmt))
+        return MX_ERR_WORKSPACE;
+    if (fmt_is_local(fmt) && dy_amax)
+        return MX_ERR_UNSUPPORTED;
+    mx_bwd_opts o;
+    std::memset(&o, 0, sizeof o);
+    if (opts)
+        o = *opts;
+    Device d;
+    int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    mx_tensor dyr, dyt, xt, wt;
+    const size_t off = carve(ws, fmt, T, Nout, &dyr);
+    carve(ws + off, fmt, Nout, T, &dyt);
+    carve_saved(static_cast<uint8_t*>(const_cast<void*>(saved)), T, Kin, Nout, fmt, o.wgrad_hadamard, &xt, &wt);
+    const int block = fmt_block(fmt);
+    if (dX && dW) {
+        rc = quantize_dual_impl(dY, T, Nout, Nout, fmt, block, MX_SCALE_DEFAULT, o.seed, o.stream_id, MX_ROUND_RNE, 0,
+                                o.wgrad_dy_rounding, o.wgrad_hadamard, dy_amax, &dyr, &dyt, d, s);
+    } else if (dX) {
+        rc = quantize_impl(dY, T, Nout, Nout, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0, dy_amax,
+                           &dyr, d, s);
+    } else if (dW) {
+        rc = quantize_impl(dY, T, Nout, Nout, MX_COLWISE, fmt, block, o.wgrad_dy_rounding, MX_SCALE_DEFAULT, o.seed,
+                           o.stream_id, o.wgrad_hadamard, dy_amax, &dyt, d, s);
+    }
+    if (rc != MX_OK)
+        return rc;
+    if (dX && (rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s)) != MX_OK)
+        return rc;
+    if (dW)
+        rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s);
     return rc;
 }
 

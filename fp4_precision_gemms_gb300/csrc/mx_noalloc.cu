@@ -49,7 +49,7 @@ int scratch_address(int device, void** out)
 extern "C" int mx_linear_fwd_noalloc(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout,
                                      int fmt, void* Y, int out_dtype, void* stream)
 {
-    if (fmt < MX_FMT_MXFP8_E4M3 || fmt > MX_FMT_MOSS_FP8 || T < 0 || Kin < 0 || Nout < 0)
+    if (fmt < MX_FMT_MXFP8_E4M3 || fmt > MX_FMT_NVFP4_LOCAL || T < 0 || Kin < 0 || Nout < 0)
         return MX_ERR_INVALID_ARG;
     const size_t need = mx_linear_workspace_bytes(T, Kin, Nout, fmt, 0);
     if (need == 0 || need > kNoAllocScratchBytes)
@@ -63,8 +63,8 @@ extern "C" int mx_linear_fwd_noalloc(const void* X, const void* W, int64_t T, in
     if (rc != MX_OK)
         return rc;
     // The forward rewrites every workspace byte it later reads (codes, scale
-    // bytes of real rows, tensor scales) and clears the amax words on the
-    // stream before reducing into them, so the previous call's contents do not
-    // leak into this one.
+    // bytes of real rows, tensor scales) and clears the amax words (the tensor
+    // amax, or the region maxima of NVFP4_LOCAL) on the stream before reducing
+    // into them, so the previous call's contents do not leak into this one.
     return mx_linear_fwd(X, W, T, Kin, Nout, fmt, Y, out_dtype, ws, kNoAllocScratchBytes, stream);
 }

@@ -217,7 +217,9 @@ int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, 
  * for N % 32 != 0 or misaligned buffers, MX_ERR_INVALID_ARG otherwise. */
 int mx_gemm_quantized(const mx_tensor* A, const mx_tensor* B, float extra_alpha, mx_tensor* out, void* stream);
 
-/* Workspace bytes for mx_linear_fwd (pass 0) and mx_linear_bwd (pass 1). */
+/* Workspace bytes for mx_linear_fwd and mx_linear_fwd_save (pass 0),
+ * mx_linear_bwd (pass 1) and mx_linear_bwd_saved (pass 2); 0 for another pass
+ * or invalid arguments. */
 size_t mx_linear_workspace_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt, int pass);
 
 /* Forward of a linear layer: Y[T, Nout] = X[T, Kin] W[Nout, Kin]^T, both
@@ -263,6 +265,47 @@ int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64
                   int64_t Nout, int fmt, const mx_bwd_opts* opts, void* dX, int dx_dtype,
                   void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of the saved backward state of one layer (mx_linear_fwd_save ->
+ * mx_linear_bwd_saved): the colwise operands X^T [Kin, T] and W^T [Kin, Nout]
+ * with their scale bytes and tensor scales; 0 for invalid arguments. */
+size_t mx_linear_saved_bytes(int64_t T, int64_t Kin, int64_t Nout, int fmt);
+
+/* Forward of a linear layer that also keeps what its backward pass needs
+ * ([FAF] FP4加速为何常常"纸上富贵": saving backward state is one of the costs
+ * around the GEMM; 格式感知融合的设计思路: each producer writes its consumer's
+ * layout).  One read of X emits the forward operand X (rowwise) and X^T
+ * (colwise, for the weight gradient); one read of W emits W and W^T (for the
+ * data gradient).  Y[T, Nout] = X W^T exactly as mx_linear_fwd computes it;
+ * X^T and W^T go to `saved` (device, mx_linear_saved_bytes bytes, caller-owned,
+ * to be passed unchanged to mx_linear_bwd_saved).
+ *   x_amax, w_amax  optional device floats holding max |X|, max |W| (NVFP4,
+ *                   MOSS): the tensor amax then needs no pass of its own
+ *                   (e.g. taken from the operation that produced X, or from a
+ *                   weight-scale predictor).  NULL = reduce it from the tensor.
+ *                   NVFP4_LOCAL takes NULL only (MX_ERR_UNSUPPORTED else).
+ *   opts            the options the backward pass will use (NULL = RNE, no
+ *                   Hadamard); wgrad_hadamard decides whether X^T carries the
+ *                   Hadamard transform.
+ *   workspace       device, >= mx_linear_workspace_bytes(.., pass 0).
+ * Requires T % 32 == 0 and Nout % 32 == 0 (the colwise operands' K) besides
+ * the rules of mx_quantize and mx_gemm.  Errors: MX_ERR_WORKSPACE for a missing
+ * or short workspace or saved buffer, otherwise as mx_quantize_dual/mx_gemm. */
+int mx_linear_fwd_save(const void* X, const void* W, int64_t T, int64_t Kin, int64_t Nout, int fmt,
+                       const float* x_amax, const float* w_amax, const mx_bwd_opts* opts, void* Y, int out_dtype,
+                       void* workspace, size_t ws_bytes, void* saved, size_t saved_bytes, void* stream);
+
+/* Backward of the layer from its saved state: one read of dY emits dY
+ * (rowwise, RNE) and dY^T (colwise, opts' rounding and Hadamard), then
+ *   dgrad dX[T, Kin] = dY W (against the saved W^T),
+ *   wgrad dW[Nout, Kin] = dY^T X (against the saved X^T).
+ * Results are bit-identical to mx_linear_bwd with the same opts.  `saved` is
+ * the buffer mx_linear_fwd_save filled (read only), `opts` must be the ones
+ * given to it.  dy_amax as x_amax above.  dX or dW may be NULL to skip that
+ * GEMM.  workspace: device, >= mx_linear_workspace_bytes(.., pass 2). */
+int mx_linear_bwd_saved(const void* dY, int64_t T, int64_t Kin, int64_t Nout, int fmt, const float* dy_amax,
+                        const mx_bwd_opts* opts, const void* saved, size_t saved_bytes, void* dX, int dx_dtype,
+                        void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream);
+
 /* Human-readable text of an mx_status. */
 const char* mx_strerror(int status);
 
@@ -285,20 +328,23 @@ uint64_t mx_launch_count(void);
  * next to CUDA's IEEE division (q_ieee), for n device pairs v[i] / d[i]. */
 int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, float* q_ieee, void* stream);
 
-/* Test hook: choose the producer implementation for later calls, process-wide:
+/* Test hook: choose the producer implementation for later calls made by the
+ * calling host thread (other threads keep their own choice, initially 0):
  * 0 automatic, 1 direct-load row/col kernels, 2 the shared-memory tile producer
  * for both directions.  Outputs are identical; only the speed differs. */
 void mx_debug_set_quant_impl(int impl);
 
 /* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
- * calls, process-wide: 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA
+ * calls made by the calling host thread (other threads keep their own choice,
+ * initially 0): 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA
  * 128 x 256 tiles, 3 CTA-pair (cluster of two) 256 x 256 tiles, 4 the
  * warp-specialised CTA pair (scale-factor stores and the epilogue in separate
  * warps; the automatic choice for large shapes). */
 void mx_debug_set_gemm_variant(int variant);
 
 /* Test/benchmark hook: the GEMM variant (numbered as above, never 0) that the
- * most recent mx_gemm / mx_linear_* call launched, process-wide; 0 before any. */
+ * calling host thread's most recent mx_gemm / mx_linear_* call launched; 0
+ * before any. */
 int mx_debug_last_gemm_variant(void);
 
 #ifdef __cplusplus

@@ -100,3 +100,19 @@ def test_host_memory_is_refused_before_the_library_is_called():
     x = torch.zeros(64, 64, dtype=torch.bfloat16)
     with pytest.raises(mx.MXError):
         mx.linear_fwd(x, x, "mxfp8", out=torch.zeros(64, 64, dtype=torch.bfloat16))
+
+
+def test_saved_state_sizes(lib):
+    """The saved backward state is the colwise operands X^T [Kin, T] and W^T
+    [Kin, Nout]; the saved-state backward's workspace is dY and dY^T.  Each
+    operand is its codes, scale bytes and two scalar arrays, each padded."""
+    def operand(f, rows, k):
+        pad = lambda v, a: -(-v // a) * a  # noqa: E731
+        n = max(1, lib.mx_scale_count(f, rows))
+        return pad(lib.mx_codes_bytes(f, rows, k), 256) + pad(lib.mx_sf_bytes(f, rows, k), 256) + 2 * pad(4 * n, 128)
+    for f in range(5):
+        for T, Kin, Nout in ((8192, 4096, 6144), (256, 512, 384), (4096, 14336, 4096)):
+            assert lib.mx_linear_saved_bytes(T, Kin, Nout, f) == operand(f, Kin, T) + operand(f, Kin, Nout)
+            assert lib.mx_linear_workspace_bytes(T, Kin, Nout, f, 2) == operand(f, T, Nout) + operand(f, Nout, T)
+            assert lib.mx_linear_workspace_bytes(T, Kin, Nout, f, 3) == 0
+    assert lib.mx_linear_saved_bytes(256, 256, 256, 9) == 0

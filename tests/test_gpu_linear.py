@@ -87,3 +87,64 @@ def test_e4m3_wgrad_stochastic_rounding(mx, fmt):
     rb = orc.quantize(bits(X), fmt, "col")
     ref, cabs = orc.gemm(ra, rb)
     assert_gemm_close(dW, ref, cabs, f"wgrad {fmt} SR")
+
+
+# --------------------------------------------- saved backward state (one read per tensor)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("hadamard,rounding", [(False, "rne"), (True, "sr")])
+def test_saved_state_path_equals_the_plain_layer(mx, fmt, hadamard, rounding):
+    """mx_linear_fwd_save + mx_linear_bwd_saved read X, W and dY once each and
+    give bit for bit what mx_linear_fwd + mx_linear_bwd give, and the oracle's
+    composition of the same quantizations and GEMMs."""
+    if hadamard and fmt not in ("mxfp8", "mxfp4"):
+        pytest.skip("the Hadamard transform is offered on the MX formats")
+    T, Kin, Nout = 512, 256, 768
+    X = workloads.draw("student_t3", (T, Kin), 171).cuda()
+    W = workloads.draw("normal", (Nout, Kin), 172, 0.02).cuda()
+    dY = workloads.draw("student_t3", (T, Nout), 173, 1e-3).cuda()
+    kw = dict(wgrad_hadamard=hadamard, wgrad_dy_rounding=rounding, seed=42, stream_id=3)
+    Y0 = mx.linear_fwd(X, W, fmt, out_dtype=torch.float32)
+    dX0, dW0 = mx.linear_bwd(dY, X, W, fmt, dx_dtype=torch.float32, **kw)
+    Y1, saved = mx.linear_fwd_save(X, W, fmt, out_dtype=torch.float32, **kw)
+    dX1, dW1 = mx.linear_bwd_saved(dY, saved, Kin, fmt, dx_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    assert mx.last_device_status() == mx.MX_OK
+    assert torch.equal(Y0, Y1) and torch.equal(dX0, dX1) and torch.equal(dW0, dW1)
+    # one of the three against the oracle (the others are checked by the plain-layer tests)
+    ra = orc.quantize(bits(dY.cpu()), fmt, "col", rounding=rounding, seed=42, stream_id=3, hadamard=hadamard)
+    rb = orc.quantize(bits(X.cpu()), fmt, "col", hadamard=hadamard)
+    ref, cabs = orc.gemm(ra, rb, extra_alpha=(1.0 / 32 if hadamard else 1.0))
+    assert_gemm_close(dW1, ref, cabs, f"wgrad from saved state {fmt}")
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "moss"])
+def test_saved_state_path_with_caller_amax(mx, fmt):
+    """A caller-supplied tensor amax skips the amax passes: with the true maxima
+    the results are those of the plain layer; with a larger amax they are the
+    oracle's quantization at that amax."""
+    T, Kin, Nout = 256, 512, 512  # every GEMM's K a multiple of 256, as FP4 requires
+    X = workloads.draw("student_t3", (T, Kin), 181).cuda()
+    W = workloads.draw("normal", (Nout, Kin), 182, 0.02).cuda()
+    dY = workloads.draw("student_t3", (T, Nout), 183, 1e-3).cuda()
+    am = lambda t: t.float().abs().max().reshape(1)  # noqa: E731
+    Y0 = mx.linear_fwd(X, W, fmt, out_dtype=torch.float32)
+    dX0, dW0 = mx.linear_bwd(dY, X, W, fmt, dx_dtype=torch.float32)
+    Y1, saved = mx.linear_fwd_save(X, W, fmt, out_dtype=torch.float32, x_amax=am(X), w_amax=am(W))
+    dX1, dW1 = mx.linear_bwd_saved(dY, saved, Kin, fmt, dx_dtype=torch.float32, dy_amax=am(dY))
+    assert torch.equal(Y0, Y1) and torch.equal(dX0, dX1) and torch.equal(dW0, dW1)
+    big = am(X) * 4
+    Y2, _ = mx.linear_fwd_save(X, W, fmt, out_dtype=torch.float32, x_amax=big)
+    ref, cabs = orc.gemm(orc.quantize(bits(X.cpu()), fmt, amax_in=float(big)), orc.quantize(bits(W.cpu()), fmt))
+    assert_gemm_close(Y2, ref, cabs, f"fwd with caller amax {fmt}")
+
+
+def test_saved_state_buffers_too_small(mx):
+    X = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mx.MXError) as e:
+        mx.linear_fwd_save(X, W, "mxfp8", saved=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == mx.MX_ERR_WORKSPACE
+    _, sv = mx.linear_fwd_save(X, W, "mxfp8")
+    with pytest.raises(mx.MXError) as e:
+        mx.linear_bwd_saved(X, sv[:1024], 256, "mxfp8")
+    assert e.value.code == mx.MX_ERR_WORKSPACE

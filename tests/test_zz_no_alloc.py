@@ -23,7 +23,7 @@ def mx():
     return m
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4", "moss", "nvfp4_local"])
 def test_noalloc_forward_matches_linear_fwd_twice(mx, fmt):
     T, Kin, Nout = 512, 1024, 768
     X = workloads.draw("student_t3", (T, Kin), 91).cuda()
