@@ -188,64 +188,197 @@ def source_hash(kind: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kind: str, fmt: str):
-    """Mean DRAM bytes (read + write) per launch of one kernel class over one
-    step, from the committed ncu summary, if it was taken on the current
-    sources of that kernel; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+COUNTERS = os.path.join("profiles", "counters.json")
+
+
+def ncu_counters(kind: str, fmt: str, workload: int = 5):
+    """The committed ncu counters of one kernel class (per launch: DRAM bytes;
+    tensor-pipe, ALU/FMA-pipe and issue activity in percent), if they were taken
+    on the current sources of that kernel; else None.  Classes of the headline
+    workload are keyed '<kind>_<fmt>', those of another workload
+    '<kind>_<fmt>@<workload>'."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, COUNTERS)) as f:
             t = json.load(f)
     except Exception:
         return None
-    e = t.get("kernels", {}).get(f"{kind}_{fmt}")
+    key = f"{kind}_{fmt}" if workload == 5 else f"{kind}_{fmt}@{workload}"
+    e = t.get("kernels", {}).get(key)
     if e is None or e.get("source_hash") != source_hash(kind):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e
+
+
+def ncu_traffic(kind: str, fmt: str, workload: int = 5):
+    """DRAM bytes (read + write) per launch of one kernel class, or None."""
+    e = ncu_counters(kind, fmt, workload)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def tensor_peak(pk: dict, fmt: str) -> float:
+    """Dense tensor peak of a format (TFLOP/s): the measured bf16 burst figure
+    (cuBLAS) times the nominal FP8 / FP4 to bf16 ratio.  The timed region is
+    well under a second, so the burst (not the sustained) bf16 figure applies."""
+    return pk["bf16_tflops"] * NOMINAL_RATIO[fmt]
+
+
+def class_rates(per: dict, pk: dict, workload: int = 5) -> dict:
+    """Per (format, kind) class: ms per step, calls, rate, fraction of its roof,
+    and the committed ncu counters of the class when they match the sources."""
+    kernels = {}
+    for (f, k), a in sorted(per.items()):
+        ctr = ncu_counters(k, f, workload)
+        if k == "gemm":
+            tf = a["work"] / (a["ms"] * 1e-3) / 1e12
+            e = {"ms_per_step": round(a["ms"], 3), "calls": a["calls"], "TFLOP/s": round(tf, 1),
+                 "frac_of_tensor_peak": round(tf / tensor_peak(pk, f), 4)}
+            if ctr and "tensor_active_pct" in ctr:
+                e["tensor_active_pct"] = ctr["tensor_active_pct"]
+            kernels[f"{f}_gemm"] = e
+        else:
+            gb = a["work"] / (a["ms"] * 1e-3) / 1e9
+            e = {"ms_per_step": round(a["ms"], 3), "calls": a["calls"], "GB/s": round(gb, 1),
+                 "frac_of_hbm_peak": round(gb / pk["hbm_gbs"], 4)}
+            if ctr:
+                for n in ("alu_pipe_pct", "fma_pipe_pct", "issue_active_pct", "dram_throughput_pct"):
+                    if n in ctr:
+                        e[n] = ctr[n]
+            kernels[f"{f}_quantize"] = e
+    return kernels
+
+
+def fused_fraction(per: dict, pk: dict, ms: float) -> dict:
+    """The step's roofline fraction: the time every class would take at its own
+    roof (quantize bytes at the HBM peak, GEMM flops at the format's tensor
+    peak), summed since the kernels run one after another, over the measured
+    step time."""
+    ideal = 0.0
+    for (f, k), a in per.items():
+        ideal += a["work"] / (tensor_peak(pk, f) * 1e12) if k == "gemm" else a["work"] / (pk["hbm_gbs"] * 1e9)
+    ideal_ms = ideal * 1e3
+    return {"ideal_ms": round(ideal_ms, 3), "measured_ms": round(ms, 3), "frac": round(ideal_ms / ms, 4)}
 
 
 # ------------------------------------------------------------ our library
 class Plan:
-    """Preallocated device buffers for one step of the layer-linears workload."""
+    """Preallocated device buffers for one step of a workload under one format.
 
-    def __init__(self, mx, wl, fmt, device):
+    Each GEMM of the workload runs its passes: fwd Y = X W^T, dgrad dX = dY W,
+    wgrad dW = dY^T X.  fwd reads X and W rowwise; dgrad reads dY rowwise and
+    W colwise; wgrad reads dY and X colwise.  A tensor needed in both
+    directions is read once by the dual-direction producer.  `wgrad` holds the
+    weight-gradient options: Hadamard on both operands, rounding and seed of
+    dY^T."""
+
+    def __init__(self, mx, wl, fmt, device, wgrad=None):
         self.mx, self.fmt = mx, fmt
+        self.wgrad = dict(hadamard=False, rounding="rne", seed=0)
+        self.wgrad.update(wgrad or {})
         self.gemms = []
-        for i, g in enumerate(wl.gemms):
+        for g in wl.gemms:
             T, Kin, Nout = g.tokens, g.k_in, g.n_out
             e = dict(g=g, T=T, Kin=Kin, Nout=Nout)
-            e["xq"] = mx.MXTensor(fmt, T, Kin, device)       # X rowwise
-            e["wq"] = mx.MXTensor(fmt, Nout, Kin, device)    # W rowwise
-            e["dyq"] = mx.MXTensor(fmt, T, Nout, device)     # dY rowwise
-            e["wtq"] = mx.MXTensor(fmt, Kin, Nout, device)   # W^T (colwise)
-            e["dytq"] = mx.MXTensor(fmt, Nout, T, device)    # dY^T (colwise)
-            e["xtq"] = mx.MXTensor(fmt, Kin, T, device)      # X^T (colwise)
-            e["Y"] = torch.empty(T, Nout, dtype=torch.bfloat16, device=device)
-            e["dX"] = torch.empty(T, Kin, dtype=torch.bfloat16, device=device)
-            e["dW"] = torch.empty(Nout, Kin, dtype=torch.float32, device=device)
+            p = g.passes
+            if "fwd" in p:
+                e["xq"] = mx.MXTensor(fmt, T, Kin, device)       # X rowwise
+                e["wq"] = mx.MXTensor(fmt, Nout, Kin, device)    # W rowwise
+                e["Y"] = torch.empty(T, Nout, dtype=torch.bfloat16, device=device)
+            if "dgrad" in p:
+                e["dyq"] = mx.MXTensor(fmt, T, Nout, device)     # dY rowwise
+                e["wtq"] = mx.MXTensor(fmt, Kin, Nout, device)   # W^T (colwise)
+                e["dX"] = torch.empty(T, Kin, dtype=torch.bfloat16, device=device)
+            if "wgrad" in p:
+                e["dytq"] = mx.MXTensor(fmt, Nout, T, device)    # dY^T (colwise)
+                e["xtq"] = mx.MXTensor(fmt, Kin, T, device)      # X^T (colwise)
+                e["dW"] = torch.empty(Nout, Kin, dtype=torch.float32, device=device)
             self.gemms.append(e)
         self.has_ts = fmt in ("nvfp4", "moss")
 
+    def _quant(self, x, row_key, col_key, e, col_opts):
+        """(fn, algorithmic bytes) of the producer call(s) for one input tensor."""
+        mx, fmt, ts = self.mx, self.fmt, self.has_ts
+        if row_key in e and col_key in e:
+            fn = lambda: mx.quantize_dual(x, fmt, row_out=e[row_key], col_out=e[col_key], **col_opts)  # noqa: E731
+            return fn, dual_bytes(fmt, e[row_key].rows * e[row_key].k, ts)
+        if row_key in e:
+            return (lambda: mx.quantize(x, fmt, "row", out=e[row_key]),
+                    quant_bytes(fmt, e[row_key].rows * e[row_key].k, ts))
+        opts = {{"col_hadamard": "hadamard", "col_rounding": "rounding"}.get(k, k): v for k, v in col_opts.items()}
+        return (lambda: mx.quantize(x, fmt, "col", out=e[col_key], **opts),
+                quant_bytes(fmt, e[col_key].rows * e[col_key].k, ts))
+
     def calls(self, inputs):
-        """The step as a list of (kind, fn, flops_or_bytes) in issue order.  Each of
-        X, W and dY is read once by the dual-direction producer, which emits the
-        rowwise operand and the transposed operand the other pass needs."""
-        mx, fmt, out = self.mx, self.fmt, []
+        """The step as a list of (kind, fn, flops_or_bytes) in issue order."""
+        mx, out = self.mx, []
+        wg = self.wgrad
+        had = dict(col_hadamard=True) if wg["hadamard"] else {}
+        dy_col = dict(col_rounding=wg["rounding"], seed=wg["seed"], **had) if (wg["rounding"] != "rne" or had) else {}
         for e in self.gemms:
             g = e["g"]
-            X, W, dY = inputs[g.x.name], inputs[g.w.name], inputs[g.dy.name]
             T, Kin, Nout = e["T"], e["Kin"], e["Nout"]
-            ts = self.has_ts
-            out.append(("quant", lambda X=X, e=e: mx.quantize_dual(X, fmt, row_out=e["xq"], col_out=e["xtq"]),
-                        dual_bytes(fmt, T * Kin, ts)))
-            out.append(("quant", lambda W=W, e=e: mx.quantize_dual(W, fmt, row_out=e["wq"], col_out=e["wtq"]),
-                        dual_bytes(fmt, Nout * Kin, ts)))
-            out.append(("gemm", lambda e=e: mx.gemm(e["xq"], e["wq"], out=e["Y"]), 2.0 * T * Kin * Nout))
-            out.append(("quant", lambda dY=dY, e=e: mx.quantize_dual(dY, fmt, row_out=e["dyq"], col_out=e["dytq"]),
-                        dual_bytes(fmt, T * Nout, ts)))
-            out.append(("gemm", lambda e=e: mx.gemm(e["dyq"], e["wtq"], out=e["dX"]), 2.0 * T * Kin * Nout))
-            out.append(("gemm", lambda e=e: mx.gemm(e["dytq"], e["xtq"], out=e["dW"]), 2.0 * T * Kin * Nout))
+            flops = 2.0 * T * Kin * Nout
+            if g.x is not None and ("xq" in e or "xtq" in e):
+                fn, b = self._quant(inputs[g.x.name], "xq", "xtq", e, had)
+                out.append(("quant", fn, b))
+            if g.w is not None and ("wq" in e or "wtq" in e):
+                fn, b = self._quant(inputs[g.w.name], "wq", "wtq", e, {})
+                out.append(("quant", fn, b))
+            if "Y" in e:
+                out.append(("gemm", lambda e=e: mx.gemm(e["xq"], e["wq"], out=e["Y"]), flops))
+            if g.dy is not None and ("dyq" in e or "dytq" in e):
+                fn, b = self._quant(inputs[g.dy.name], "dyq", "dytq", e, dy_col)
+                out.append(("quant", fn, b))
+            if "dX" in e:
+                out.append(("gemm", lambda e=e: mx.gemm(e["dyq"], e["wtq"], out=e["dX"]), flops))
+            if "dW" in e:
+                out.append(("gemm", lambda e=e: mx.gemm(e["dytq"], e["xtq"], out=e["dW"]), flops))
         return out
+
+
+# The workloads timed next to the headline one, with their weight-gradient
+# options (workload 4: Hadamard-32 on both wgrad operands, stochastic rounding
+# of dY^T with Philox seed 42).
+SIDE_WORKLOADS = {2: {}, 3: {}, 4: dict(hadamard=True, rounding="sr", seed=42)}
+
+
+def time_calls(calls, steps, warmup, stream, clk=None, count=None):
+    """Runs warm-up steps, then `steps` timed steps of `calls` with CUDA events on
+    `stream` (one pair per call).  Returns (ms per step, per-class dict, the
+    increase of count() over the timed steps, or None)."""
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step(events=None):
+        for i, c in enumerate(calls):
+            if events is not None:
+                events[i][0].record(stream)
+            c[2]()
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    c0 = count() if count else None
+    if clk is not None:
+        clk.start_window()
+    t0.record(stream)
+    for s in range(steps):
+        step(ev[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.end_window()
+    counted = count() - c0 if count else None
+    per = {}
+    for i, (fmt, kind, fn, work) in enumerate(calls):
+        d = sum(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)) / steps
+        a = per.setdefault((fmt, kind), {"ms": 0.0, "work": 0.0, "calls": 0})
+        a["ms"] += d
+        a["work"] += work
+        a["calls"] += 1
+    return t0.elapsed_time(t1) / steps, per, counted
 
 
 def run_ours(args, world, rank, local):
@@ -262,14 +395,6 @@ def run_ours(args, world, rank, local):
     gemm_flops = sum(c[3] for c in calls if c[1] == "gemm")
     stream = torch.cuda.current_stream()
 
-    def step(events=None):
-        for i, (fmt, kind, fn, _) in enumerate(calls):
-            if events is not None:
-                events[i][0].record(stream)
-            fn()
-            if events is not None:
-                events[i][1].record(stream)
-
     # which GEMM kernel each scheme's launches use (named in the roofline)
     variants = {}
     for fmt, kind, fn, _ in calls:
@@ -277,42 +402,18 @@ def run_ours(args, world, rank, local):
         if kind == "gemm":
             variants.setdefault(fmt, set()).add(mx.last_gemm_variant())
     gemm_kernels = {f: " + ".join(GEMM_KERNEL_NAME[v].format(fmt=f) for v in sorted(vs)) for f, vs in variants.items()}
-    # per-call events for every timed step
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
-          for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index) as clk:
-        for _ in range(args.warmup):
-            step()
         torch.cuda.synchronize()
         assert mx.last_device_status() == mx.MX_OK
-        launches0 = mx.launch_count()
         barrier(world)
-        torch.cuda.synchronize()
-        clk.start_window()
-        t0.record(stream)
-        for s in range(args.steps):
-            step(ev[s])
-        t1.record(stream)
-        torch.cuda.synchronize()
-        clk.end_window()
+        ms, per, launches = time_calls(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count)
     barrier(world)
-    launches = mx.launch_count() - launches0
     status = mx.last_device_status()
-    ms = t0.elapsed_time(t1) / args.steps
     ms = reduce_max(ms, world)
-    # per-kernel-class durations (ms per step)
-    per = {}
-    for i, (fmt, kind, fn, work) in enumerate(calls):
-        d = sum(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)) / args.steps
-        k = (fmt, kind)
-        a = per.setdefault(k, {"ms": 0.0, "work": 0.0, "calls": 0})
-        a["ms"] += d
-        a["work"] += work
-        a["calls"] += 1
     result = dict(ms=ms, gemm_flops=gemm_flops, per=per, launches=launches, clocks=clk.summary(),
-                  gemm_kernels=gemm_kernels,
-                  status=status, calls_per_step=len(calls))
+                  gemm_kernels=gemm_kernels, status=status, calls_per_step=len(calls))
+    if not args.no_side:
+        result["side"] = run_side_workloads(mx, device, stream, args)
     if not args.no_e2e:
         result["e2e"] = run_e2e(mx, wl, inputs, device, args, world)
     result["wl"] = wl
@@ -320,11 +421,32 @@ def run_ours(args, world, rank, local):
     return result
 
 
+def run_side_workloads(mx, device, stream, args):
+    """The other single-GPU workloads (MOSS linear, NVFP4 MLP forward, MXFP4
+    wgrad with Hadamard-32 and SR), each timed on its own: ms per step and the
+    per-class (format, kind) durations."""
+    out = {}
+    for idx, wg in SIDE_WORKLOADS.items():
+        wl = workloads.workloads()[idx]
+        inputs = workloads.materialize(wl, device=device)
+        calls = []
+        for fmt in wl.formats:
+            calls += [(fmt,) + c for c in Plan(mx, wl, fmt, device, wgrad=wg).calls(inputs)]
+        flops = sum(c[3] for c in calls if c[1] == "gemm")
+        ms, per, _ = time_calls(calls, args.side_steps, args.warmup, stream)
+        out[wl.name] = dict(ms=ms, gemm_flops=flops, per=per, wgrad=wg, index=idx)
+        del inputs
+    torch.cuda.synchronize()
+    return out
+
+
 def run_e2e(mx, wl, dev_inputs, device, args, world):
     """The same step through the public linear-layer API with host buffers:
-    pinned-host -> device copies of every input, mx.linear_fwd / linear_bwd,
-    device -> pinned-host copies of every output, all inside the timed region
-    (copies overlap the compute of neighbouring layers on their own streams)."""
+    pinned-host -> device copies of every input, mx.linear_fwd_save (which keeps
+    X^T and W^T for the backward) and mx.linear_bwd_saved, so X, W and dY are
+    each read once on the device, as in the kernel-level step; device ->
+    pinned-host copies of every output; all inside the timed region (copies
+    overlap the compute of neighbouring layers on their own streams)."""
     host_in = {k: v.cpu().pin_memory() for k, v in dev_inputs.items()}
     bufs = []
     for fmt in wl.formats:
@@ -337,7 +459,9 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
             b["dX"] = torch.empty(T, Kin, dtype=torch.bfloat16, device=device)
             b["dW"] = torch.empty(Nout, Kin, dtype=torch.float32, device=device)
             b["wsf"] = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "fwd"), dtype=torch.uint8, device=device)
-            b["wsb"] = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "bwd"), dtype=torch.uint8, device=device)
+            b["wsb"] = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "bwd_saved"), dtype=torch.uint8,
+                                   device=device)
+            b["saved"] = torch.empty(mx.saved_bytes(T, Kin, Nout, fmt), dtype=torch.uint8, device=device)
             b["hY"] = torch.empty(b["Y"].shape, dtype=b["Y"].dtype).pin_memory()
             b["hdX"] = torch.empty(b["dX"].shape, dtype=b["dX"].dtype).pin_memory()
             b["hdW"] = torch.empty(b["dW"].shape, dtype=b["dW"].dtype).pin_memory()
@@ -371,8 +495,9 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
         for b in bufs:
             compute.wait_event(b["in_ready"])
             compute.wait_event(b["out_done"])  # the previous step's outputs have left
-            mx.linear_fwd(b["X"], b["W"], b["fmt"], workspace=b["wsf"], out=b["Y"])
-            mx.linear_bwd(b["dY"], b["X"], b["W"], b["fmt"], workspace=b["wsb"], dX=b["dX"], dW=b["dW"])
+            mx.linear_fwd_save(b["X"], b["W"], b["fmt"], workspace=b["wsf"], saved=b["saved"], out=b["Y"])
+            mx.linear_bwd_saved(b["dY"], b["saved"], b["g"].k_in, b["fmt"], workspace=b["wsb"], dX=b["dX"],
+                                dW=b["dW"])
             b["computed"].record(compute)
             d2h_s.wait_event(b["computed"])
             with torch.cuda.stream(d2h_s):
@@ -483,7 +608,9 @@ def run_reference(args, world, rank):
 def run_case(args):
     """One kernel on its own, for tuning and small ncu captures:
     gemm:<fmt>:MxNxK, gemmq:<fmt>:<out fmt>:MxNxK (quantized epilogue) or
-    quant:<fmt>:<row|col|dual>:RxC  (bf16 Student-t inputs)."""
+    quant:<fmt>:<row|col|dual>[+had][+sr]:RxC (bf16 Student-t inputs; +had
+    applies Hadamard-32, +sr stochastic rounding with seed 42, to the colwise
+    operand of a dual call)."""
     import fp4_precision_gemms_gb300 as mx
     mx.build()
     mx.set_gemm_variant(args.gemm_variant)
@@ -508,8 +635,14 @@ def run_case(args):
         q = mx.MXTensor(ofmt, M, N, dev)
         fn = lambda: mx.gemm_quantized(a, b, ofmt, out=q)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
-    else:
-        fmt, direction = parts[1], parts[2]
+    else:  # direction row, col or dual, optionally +had (Hadamard-32) and +sr (stochastic rounding)
+        fmt, dopts = parts[1], parts[2].split("+")
+        direction = dopts[0]
+        qo = {}
+        if "had" in dopts:
+            qo["hadamard"] = True
+        if "sr" in dopts:
+            qo.update(rounding="sr", seed=42)
         R, Cc = (int(v) for v in parts[3].split("x"))
         x = workloads.draw("student_t3", (R, Cc), 1, device=dev)
         rows, k = (R, Cc) if direction == "row" else (Cc, R)
@@ -520,10 +653,11 @@ def run_case(args):
         if direction == "dual":
             qc = mx.MXTensor(fmt, Cc, R, dev)
             q = mx.MXTensor(fmt, R, Cc, dev)
-            fn = lambda: mx.quantize_dual(x, fmt, row_out=q, col_out=qc, amax_in=amax_in)  # noqa: E731
+            do = {("col_" + k if k in ("hadamard", "rounding") else k): v for k, v in qo.items()}
+            fn = lambda: mx.quantize_dual(x, fmt, row_out=q, col_out=qc, amax_in=amax_in, **do)  # noqa: E731
             work = dual_bytes(fmt, R * Cc, False)
         else:
-            fn = lambda: mx.quantize(x, fmt, direction, out=q, amax_in=amax_in)  # noqa: E731
+            fn = lambda: mx.quantize(x, fmt, direction, out=q, amax_in=amax_in, **qo)  # noqa: E731
             work = quant_bytes(fmt, R * Cc, False)
         unit = "GB/s"
     for _ in range(args.warmup):
@@ -557,6 +691,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side", action="store_true", help="skip the other workloads' lines")
+    ap.add_argument("--side-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1024)
     ap.add_argument("--ref-sample", type=int, default=256)
@@ -587,35 +723,40 @@ def main():
     dom_key = max(r["per"], key=lambda k: r["per"][k]["ms"])
     d = r["per"][dom_key]
     fmt, kind = dom_key
+    ctr = ncu_counters(kind, fmt) or {}
     if kind == "gemm":
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e12
-        peak = pk["bf16_tflops_sustained"] * NOMINAL_RATIO[fmt]
+        peak = tensor_peak(pk, fmt)
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "kernel": r["gemm_kernels"][fmt],
-                "peak_source": f"{src}: bf16_tflops_sustained x {NOMINAL_RATIO[fmt]:g} (nominal {fmt} / bf16 ratio)",
-                "traffic": ncu_traffic("gemm", fmt)}
+                "peak_source": (f"derived from {src}: bf16_tflops (cuBLAS bf16 burst) x {NOMINAL_RATIO[fmt]:g}, "
+                                f"the nominal dense {fmt} / bf16 ratio"),
+                "traffic": ctr.get("dram_bytes_per_launch"),
+                "tensor_active_pct": ctr.get("tensor_active_pct")}
     else:
         achieved = d["work"] / (d["ms"] * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "kernel": f"quantize<{fmt}>", "peak_source": f"{src}: hbm_gbs",
-                "traffic": ncu_traffic("quant", fmt)}
-    kernels = {}
-    for (f, k), a in sorted(r["per"].items()):
-        if k == "gemm":
-            tf = a["work"] / (a["ms"] * 1e-3) / 1e12
-            pkk = pk["bf16_tflops_sustained"] * NOMINAL_RATIO[f]
-            kernels[f"{f}_gemm"] = {"ms_per_step": round(a["ms"], 3), "calls": a["calls"], "TFLOP/s": round(tf, 1),
-                                    "frac_of_tensor_peak": round(tf / pkk, 4)}
-        else:
-            gb = a["work"] / (a["ms"] * 1e-3) / 1e9
-            kernels[f"{f}_quantize"] = {"ms_per_step": round(a["ms"], 3), "calls": a["calls"],
-                                        "GB/s": round(gb, 1), "frac_of_hbm_peak": round(gb / pk["hbm_gbs"], 4)}
+                "traffic": ctr.get("dram_bytes_per_launch")}
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(r["ms"], 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3/e2m1 block-scaled MMA, f32 accumulate", "data": "synthetic",
-            "config": config_of(wl, args), "roofline": roof, "kernels": kernels,
+            "config": config_of(wl, args), "roofline": roof,
+            "fused_roofline": dict(fused_fraction(r["per"], pk, r["ms"]),
+                                   definition="(sum of quantize bytes / HBM peak + sum of GEMM flops / tensor peak) "
+                                              "/ measured step time"),
+            "kernels": class_rates(r["per"], pk),
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "device_status": int(r["status"])}
+    if "side" in r:
+        side = {}
+        for name, w in r["side"].items():
+            side[name] = {"TFLOP/s": round(w["gemm_flops"] / (w["ms"] * 1e-3) / 1e12, 1),
+                          "ms_per_step": round(w["ms"], 3), "gemm_tflop_per_step": round(w["gemm_flops"] / 1e12, 4),
+                          "wgrad_options": w["wgrad"],
+                          "fused_roofline": fused_fraction(w["per"], pk, w["ms"]),
+                          "kernels": class_rates(w["per"], pk, w["index"])}
+        line["workloads"] = side
     if "e2e" in r:
         line["e2e"] = r["e2e"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -53,9 +53,44 @@ def test_traffic_is_reported_only_for_the_profiled_sources(tmp_path, monkeypatch
         (csrc / f).write_text(f"// {f}\n")
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    entry = {"dram_bytes_per_launch": 123456, "source_hash": bench.source_hash("gemm")}
-    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"kernels": {"gemm_mxfp8": entry}}))
+    entry = {"dram_bytes_per_launch": 123456, "tensor_active_pct": 71.5, "source_hash": bench.source_hash("gemm")}
+    (tmp_path / "profiles" / "counters.json").write_text(json.dumps({"kernels": {"gemm_mxfp8": entry}}))
     assert bench.ncu_traffic("gemm", "mxfp8") == 123456
+    assert bench.ncu_counters("gemm", "mxfp8")["tensor_active_pct"] == 71.5
     assert bench.ncu_traffic("gemm", "nvfp4") is None  # no counters for that class
     (csrc / "gemm.cu").write_text("// gemm.cu, edited\n")
     assert bench.ncu_traffic("gemm", "mxfp8") is None  # the kernel changed since the capture
+
+
+@pytest.mark.parametrize("idx,kinds", [
+    (2, ["quant", "quant", "gemm", "quant", "gemm", "gemm"]),         # MOSS: X, W, dY dual; three passes
+    (3, ["quant", "quant", "gemm", "quant", "quant", "gemm"]),         # NVFP4 MLP fwd: rowwise only
+    (4, ["quant", "quant", "gemm"]),                                    # MXFP4 wgrad: X^T, dY^T, dW
+])
+def test_side_workload_plans(idx, kinds):
+    """The other workloads' steps: which producer calls and GEMMs run, their
+    flops and the bytes of each producer call (one direction or both)."""
+    wl = workloads.workloads()[idx]
+    inputs = {t.name: None for g in wl.gemms for t in (g.x, g.w, g.dy) if t is not None}
+    calls = bench.Plan(_StubMX, wl, wl.formats[0], torch.device("cpu"), wgrad=bench.SIDE_WORKLOADS[idx]).calls(inputs)
+    assert [c[0] for c in calls] == kinds
+    assert sum(c[2] for c in calls if c[0] == "gemm") == wl.flops()
+    fmt = wl.formats[0]
+    ts = fmt in ("nvfp4", "moss")
+    qbytes = [c[2] for c in calls if c[0] == "quant"]
+    if idx == 4:  # X^T and dY^T, one direction each, no tensor scale
+        assert qbytes == [bench.quant_bytes(fmt, 8192 * 4096, False), bench.quant_bytes(fmt, 8192 * 14336, False)]
+    if idx == 3:
+        assert qbytes[0] == bench.quant_bytes(fmt, 8192 * 4096, ts)
+    if idx == 2:
+        assert qbytes[0] == bench.dual_bytes(fmt, 4096 * 4096, ts)
+
+
+def test_fused_fraction_adds_each_class_at_its_roof():
+    pk = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    per = {("mxfp8", "gemm"): {"work": 4e12, "ms": 2.0}, ("nvfp4", "gemm"): {"work": 6e12, "ms": 1.0},
+           ("mxfp8", "quant"): {"work": 8e9, "ms": 2.0}}
+    f = bench.fused_fraction(per, pk, 8.0)
+    # 4e12 / 4000e12 s + 6e12 / 12000e12 s + 8e9 / 8000e9 s = 1 + 0.5 + 1 ms
+    assert f["ideal_ms"] == pytest.approx(2.5)
+    assert f["frac"] == pytest.approx(2.5 / 8.0)
