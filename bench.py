@@ -607,7 +607,9 @@ def run_reference(args, world, rank):
 
 def run_case(args):
     """One kernel on its own, for tuning and small ncu captures:
-    gemm:<fmt>:MxNxK, gemmq:<fmt>:<out fmt>:MxNxK (quantized epilogue) or
+    step:<fmt>:<gemm|quant>[:<workload>] (that class's calls of one step of a
+    workload, default the headline one, after one untimed pass of the whole
+    step), gemm:<fmt>:MxNxK, gemmq:<fmt>:<out fmt>:MxNxK (quantized epilogue) or
     quant:<fmt>:<row|col|dual>[+had][+sr]:RxC (bf16 Student-t inputs; +had
     applies Hadamard-32, +sr stochastic rounding with seed 42, to the colwise
     operand of a dual call)."""
@@ -619,7 +621,19 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if parts[0] == "gemm":
+    if parts[0] == "step":  # one kernel class of a workload's step: step:<fmt>:<gemm|quant>[:<workload>]
+        fmt, kind = parts[1], parts[2]
+        idx = int(parts[3]) if len(parts) > 3 else 5
+        wl = workloads.workloads()[idx]
+        inputs = workloads.materialize(wl, device=dev)
+        calls = Plan(mx, wl, fmt, dev, wgrad=SIDE_WORKLOADS.get(idx)).calls(inputs)
+        for c in calls:  # every operand the class reads exists before the timed calls
+            c[1]()
+        sel = [c for c in calls if c[0] == kind]
+        fn = lambda: [c[1]() for c in sel]  # noqa: E731
+        work = sum(c[2] for c in sel)
+        unit = "TFLOP/s" if kind == "gemm" else "GB/s"
+    elif parts[0] == "gemm":
         fmt = parts[1]
         M, N, K = (int(v) for v in parts[2].split("x"))
         a = mx.quantize(workloads.draw("student_t3", (M, K), 1, device=dev), fmt)
