@@ -368,7 +368,11 @@ static void put_code(uint8_t* codes, int64_t r, int64_t k, int64_t K, int elem, 
  *     [FAF] FP4加速为何常常"纸上富贵" and 格式感知融合的设计思路):
  *     s_t = fl32(amax / (448 * 6)); sb = UE4M3_rne(fl32(b / fl32(6 * s_t)));
  *     d = fl32(dec(sb) * s_t); code = E2M1(fl32(x / d)), or sign-kept zero
- *     when d == 0.
+ *     when d == 0.  With hadamard, every 32 consecutive operand elements
+ *     along K (two scale blocks) are first replaced by y = H32 x, and amax is
+ *     max |y| over the whole transformed operand ([FAF] 两个关键的数值技巧
+ *     puts the transform before quantization; the tensor scale must then
+ *     cover the transformed values, which can exceed max |x|).
  *   The tensor scale is 1 when amax == 0.
  * cast: RNE (E4M3 or E2M1) or stochastic rounding (E2M1 only) with the bits
  * of orc_sr_u16 for element index L = r*K + k.
@@ -387,7 +391,7 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
     if (block != fmt_block(fmt))
         return ORC_ERR_UNSUPPORTED;
     const int elem = fmt_elem(fmt);
-    if (hadamard && !(fmt == ORC_FMT_MXFP8 || fmt == ORC_FMT_MXFP4))
+    if (hadamard && !(fmt == ORC_FMT_MXFP8 || fmt == ORC_FMT_MXFP4 || fmt == ORC_FMT_NVFP4))
         return ORC_ERR_UNSUPPORTED;
     if (fmt_is_nvfp4(fmt) && rule != ORC_RULE_DEFAULT)
         return ORC_ERR_UNSUPPORTED; /* NVFP4 block scales are E4M3, not powers of two */
@@ -395,9 +399,12 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
         rule = (fmt == ORC_FMT_MOSS) ? ORC_RULE_CEIL : ORC_RULE_FLOOR;
     const int64_t rows = (dir == ORC_ROWWISE) ? R : C;
     const int64_t K = (dir == ORC_ROWWISE) ? C : R;
-    if (K % block != 0)
+    if (K % block != 0 || (hadamard && K % 32 != 0))
         return ORC_ERR_ARG;
     const int64_t kblocks = K / block;
+    /* Elements transformed together along K: 32 with the Hadamard transform
+     * (one MX block, two NVFP4 blocks), else one scale block. */
+    const int group = hadamard ? 32 : block;
 
     /* Tensor scales.  One per tensor, except ORC_FMT_NVFP4_LOCAL: one per
      * region of ORC_LOCAL_REGION consecutive operand rows (all of K), the
@@ -429,6 +436,20 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
                 }
             amaxv[g] = m;
         }
+    } else if (fmt == ORC_FMT_NVFP4 && hadamard && !amax_in) {
+        /* max |H32 x| over every 32-element group of the operand along K */
+        float m = 0.0f;
+        for (int64_t rr = 0; rr < rows; ++rr)
+            for (int64_t k0 = 0; k0 < K; k0 += 32) {
+                float y[32];
+                for (int i = 0; i < 32; ++i)
+                    y[i] = orc_bf16_to_f32((dir == ORC_ROWWISE) ? x[rr * ld + k0 + i] : x[(k0 + i) * ld + rr]);
+                orc_fwht32(y);
+                for (int i = 0; i < 32; ++i)
+                    if (fabsf(y[i]) > m)
+                        m = fabsf(y[i]);
+            }
+        amaxv[0] = m;
     } else if (fmt == ORC_FMT_MOSS || fmt == ORC_FMT_NVFP4 || amax_out) {
         amaxv[0] = amax_in ? *amax_in : orc_amax_bf16(x, R, C, ld);
     }
@@ -448,16 +469,21 @@ int orc_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ld, int dir, i
     int64_t r;
 #pragma omp parallel for schedule(dynamic, 16)
     for (r = 0; r < rows; ++r) {
-        float y[32];
+        float yg[32];
         for (int64_t kb = 0; kb < kblocks; ++kb) {
             const int64_t k0 = kb * block;
-            for (int i = 0; i < block; ++i) {
-                int64_t k = k0 + i;
-                uint16_t h = (dir == ORC_ROWWISE) ? x[r * ld + k] : x[k * ld + r];
-                y[i] = orc_bf16_to_f32(h);
+            if (k0 % group == 0) { /* load (and transform) the next group */
+                for (int i = 0; i < group; ++i) {
+                    int64_t k = k0 + i;
+                    uint16_t h = (dir == ORC_ROWWISE) ? x[r * ld + k] : x[k * ld + r];
+                    yg[i] = orc_bf16_to_f32(h);
+                }
+                if (hadamard)
+                    orc_fwht32(yg);
             }
-            if (hadamard)
-                orc_fwht32(y);
+            float y[32];
+            for (int i = 0; i < block; ++i)
+                y[i] = yg[k0 % group + i];
             const float ts = tsv[local ? r / ORC_LOCAL_REGION : 0];
             const float nv_denom = 6.0f * ts;
             if (fmt == ORC_FMT_MOSS)

@@ -378,8 +378,11 @@ def test_nvfp4_scales():
 
 def test_quantize_rejects_unsupported():
     x = _bits(workloads.draw("normal", (32, 32), 1))
-    with pytest.raises(ValueError):
-        orc.quantize(x, "nvfp4", hadamard=True)
+    for fmt in ("moss", "nvfp4_local"):  # the transform is offered on the MX formats and NVFP4
+        with pytest.raises(ValueError):
+            orc.quantize(x, fmt, hadamard=True)
+    with pytest.raises(ValueError):  # NVFP4 blocks of 16, but the transform needs whole 32-groups
+        orc.quantize(_bits(workloads.draw("normal", (32, 48), 1)), "nvfp4", hadamard=True)
     with pytest.raises(ValueError):
         orc.quantize(_bits(workloads.draw("normal", (32, 24), 1)), "mxfp8")
 

@@ -383,3 +383,47 @@ def test_moss_oracle_matches_page_reading_on_stress_tensors():
                 separated.add(variant)
     # each alternative reading gives other bytes on some stress tensor
     assert separated == {"reciprocal", "inverse_scale"}, separated
+
+
+# ------------------------------------------------- NVFP4 with Hadamard-32 ---
+def _exact_transform_input(shape, seed):
+    """bf16 values k / 16, |k| <= 8: every butterfly of the 32-point transform
+    is exact in fp32, so the transformed block equals H32 x computed in fp64."""
+    rng = np.random.default_rng(seed)
+    return (rng.integers(-8, 9, size=shape) / 16.0).astype(np.float32)
+
+
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_nvfp4_hadamard_is_the_page_reading_on_transformed_blocks(direction):
+    """NVFP4 with the transform: y = H32 x per 32 operand elements along K
+    (scipy's Sylvester matrix, fp64), the tensor amax over all y, then the
+    NVFP4 reading on y.  The oracle must give the same bytes, and its amax must
+    be the transformed one (larger than max |x| here)."""
+    from scipy.linalg import hadamard
+    H = hadamard(32).astype(np.float64)
+    x = _exact_transform_input((64, 128), 51)
+    xb = to_bf16_bits(x)
+    q = orc.quantize(xb, "nvfp4", direction, hadamard=True)
+    op = x if direction == "row" else x.T  # operand rows along K
+    y = (op.reshape(op.shape[0], -1, 32).astype(np.float64) @ H.T).reshape(op.shape).astype(np.float32)
+    assert np.float32(q.amax) == np.abs(y).max() > np.abs(x).max()
+    rc, rs = nvfp4_reference(y)
+    assert np.array_equal(q.sf_logical, rs)
+    assert np.array_equal(unpack_fp4(q.codes), rc)
+    # a caller amax is taken as the transformed tensor's amax, as given
+    q2 = orc.quantize(xb, "nvfp4", direction, hadamard=True, amax_in=float(np.abs(y).max()) * 2)
+    rc2, rs2 = nvfp4_reference(y, amax=np.abs(y).max() * 2)
+    assert np.array_equal(q2.sf_logical, rs2) and np.array_equal(unpack_fp4(q2.codes), rc2)
+
+
+def test_nvfp4_hadamard_wgrad_identity():
+    """(H a)^T (H b) = 32 a^T b: the weight gradient from transformed NVFP4
+    operands, scaled by 1/32, estimates dY^T X (quantization error only)."""
+    dy = workloads.draw("student_t3", (256, 128), 52, 1e-3)
+    xx = workloads.draw("normal", (256, 96), 53)
+    ra = orc.quantize(dy.contiguous().view(torch.int16).numpy().view(np.uint16), "nvfp4", "col", hadamard=True)
+    rb = orc.quantize(xx.contiguous().view(torch.int16).numpy().view(np.uint16), "nvfp4", "col", hadamard=True)
+    c, _ = orc.gemm(ra, rb, extra_alpha=1.0 / 32)
+    exact = dy.double().t().numpy() @ xx.double().numpy()
+    rel = np.linalg.norm(c - exact) / np.linalg.norm(exact)
+    assert rel < 0.25
