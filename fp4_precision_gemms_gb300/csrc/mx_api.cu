@@ -131,7 +131,7 @@ int check_direction(int fmt, int rounding, int hadamard)
 {
     if (rounding != MX_ROUND_RNE && rounding != MX_ROUND_SR)
         return MX_ERR_INVALID_ARG;
-    if (hadamard && !(fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MXFP4_E2M1))
+    if (hadamard && !(fmt == MX_FMT_MXFP8_E4M3 || fmt == MX_FMT_MXFP4_E2M1 || fmt == MX_FMT_NVFP4))
         return MX_ERR_UNSUPPORTED;
     return MX_OK;
 }
@@ -181,6 +181,8 @@ int prepare_amax(const void* x, int64_t R, int64_t C, int64_t ld, const float* a
             return MX_ERR_CUDA;
         return MX_OK;
     }
+    if (out->hadamard)  // the tensor scale covers the transformed values
+        return launch_had_amax(x, R, C, ld, dir, out->amax, d, s);
     return launch_amax(x, R, C, ld, out->amax, d, s);
 }
 
@@ -206,7 +208,7 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         return rc;
     const int64_t rows = dir == MX_ROWWISE ? R : C;
     const int64_t k = dir == MX_ROWWISE ? C : R;
-    if (k % block != 0 || (dir == MX_COLWISE && R % 32 != 0))
+    if (k % block != 0 || (dir == MX_COLWISE && R % 32 != 0) || (hadamard && k % 32 != 0))
         return MX_ERR_ALIGNMENT;
     if (rule == MX_SCALE_DEFAULT)
         rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
@@ -216,8 +218,11 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         return rc;
     if (R == 0 || C == 0)
         return (ts && !fmt_is_local(fmt)) ? set_unit_scale(out, s) : MX_OK;
-    // the direct producers have no region scales: NVFP4_LOCAL always takes the tile producer
-    const bool tile = g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE) || fmt_is_local(fmt);
+    // the direct producers have no region scales: NVFP4_LOCAL always takes the tile
+    // producer; the tile producer has no NVFP4 transform: NVFP4 with the
+    // Hadamard transform always takes the direct producers
+    const bool nv_had = fmt == MX_FMT_NVFP4 && hadamard;
+    const bool tile = (g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE) || fmt_is_local(fmt)) && !nv_had;
     if (tile) {
         TileArgs t = {};
         t.x = x;
@@ -283,6 +288,19 @@ int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt,
         return rc;
     if (C % block != 0 || R % 32 != 0)
         return MX_ERR_ALIGNMENT;
+    if (fmt == MX_FMT_NVFP4 && (row_hadamard || col_hadamard)) {
+        // A transformed direction has a tensor amax of its own (that of its
+        // transformed values), so the two operands get separate scales, each
+        // from its own pass over x; one caller amax cannot serve both.
+        if (amax_in)
+            return MX_ERR_UNSUPPORTED;
+        rc = quantize_impl(x, R, C, ld, MX_ROWWISE, fmt, block, row_rounding, rule, seed, stream_id, row_hadamard,
+                           nullptr, row_out, d, s);
+        if (rc != MX_OK)
+            return rc;
+        return quantize_impl(x, R, C, ld, MX_COLWISE, fmt, block, col_rounding, rule, seed, stream_id, col_hadamard,
+                             nullptr, col_out, d, s);
+    }
     if (rule == MX_SCALE_DEFAULT)
         rule = fmt == MX_FMT_MOSS_FP8 ? MX_SCALE_CEIL : MX_SCALE_FLOOR;
     fill_meta(row_out, R, C, fmt, row_hadamard);

@@ -88,6 +88,11 @@ inline void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_re
 
 int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, const Device& d,
                 cudaStream_t s);
+// Tensor amax of the Hadamard-transformed operand of x along `dir` (max |H32 y|
+// over every 32 consecutive operand elements along K); C % 32 == 0 rowwise,
+// R % 32 == 0 colwise.
+int launch_had_amax(const void* x, int64_t R, int64_t C, int64_t ld, int dir, float* amax, const Device& d,
+                    cudaStream_t s);
 // NVFP4_LOCAL region maxima of bf16 x [R, C]: amax_rows[g] = max |x| over rows
 // 128 g .. 128 g + 127, amax_cols[g] over columns 128 g .. (either may be null).
 int launch_region_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax_rows, float* amax_cols,

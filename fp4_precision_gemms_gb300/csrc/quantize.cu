@@ -471,6 +471,77 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const uint16_t* __restri
 
 // Rowwise producer.  One work item = one row and 256*U consecutive 8-element
 // chunks of it; a thread handles U chunks (U loads in flight).
+// Tensor amax of the Hadamard-transformed operand (NVFP4 with the transform):
+// max |H32 y| over every 32 consecutive operand elements along K, each group
+// transformed with the same butterflies, in the same order, as the producers
+// use, so the amax is the exact maximum of the values they encode.
+//   ROWWISE (K along the columns of x, C % 32 == 0): a warp takes 32
+//   consecutive 8-element chunks; four lanes hold one 32-element group and
+//   transform it with in-thread stages h = 1, 2, 4 and lane stages h = 8, 16.
+//   COLWISE (K along the rows, R % 32 == 0): a lane holds two adjacent columns
+//   over 32 rows (a warp reads 128 contiguous bytes per row) and transforms
+//   each column in registers.
+__global__ void __launch_bounds__(kThreads) had_amax_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C,
+                                                            int64_t ld, int dir, unsigned* __restrict__ out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    float m = 0.0f;
+    if (dir == MX_ROWWISE) {
+        const int64_t cpr = C / 8, total = R * cpr;  // 8-element chunks, 4 per group (cpr % 4 == 0)
+        for (int64_t t0 = warp * 32; t0 < total; t0 += nwarps * 32) {  // warp-uniform bound
+            const int64_t t = t0 + lane;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (t < total) {
+                const int64_t r = t / cpr, c8 = t - r * cpr;
+                w = __ldg(reinterpret_cast<const uint4*>(x + r * ld + c8 * 8));
+            }
+            float v[8];
+            unpack8(w, v);
+            fwht_local<8>(v);
+            fwht_lanes(v, 1, (lane & 1) != 0);
+            fwht_lanes(v, 2, (lane & 2) != 0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m = fmaxf(m, fabsf(v[i]));
+        }
+    } else {
+        const int64_t cpairs = (C + 1) / 2, rgroups = R / 32;
+        const int64_t ctasks = (cpairs + 31) / 32, tasks = rgroups * ctasks;
+        for (int64_t task = warp; task < tasks; task += nwarps) {
+            const int64_t rg = task / ctasks, cp = (task - rg * ctasks) * 32 + lane;
+            const int64_t c = 2 * cp;
+            if (c < C) {
+                float v0[32], v1[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const uint16_t* src = x + (rg * 32 + i) * ld + c;
+                    const uint32_t w = c + 1 < C ? *reinterpret_cast<const uint32_t*>(src) : static_cast<uint32_t>(*src);
+                    v0[i] = bf16_lo(w);
+                    v1[i] = bf16_hi(w);
+                }
+                fwht_local<32>(v0);
+                fwht_local<32>(v1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    m = fmaxf(m, fmaxf(fabsf(v0[i]), fabsf(v1[i])));
+            }
+        }
+    }
+    unsigned mu = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));  // m >= 0: bits order like values
+    __shared__ unsigned wmax[kThreads / 32];
+    if (lane == 0)
+        wmax[threadIdx.x >> 5] = mu;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        mu = threadIdx.x < kThreads / 32 ? wmax[threadIdx.x] : 0u;
+        mu = __reduce_max_sync(0xFFFFFFFFu, mu);
+        if (threadIdx.x == 0)
+            atomicMax(out, mu);
+    }
+}
+
 template <int FMT, bool SR, bool HAD>
 __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
 {
@@ -590,14 +661,22 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
         const int64_t c = c0 + threadIdx.x;
         if (c < C) {
             uint32_t out[8];
+            // the transform covers 32 rows: one MX block, two NVFP4 blocks
+            constexpr int G = HAD ? 32 : BLOCK;
+            float grp[G];
 #pragma unroll
             for (int b = 0; b < SEG / BLOCK; ++b) {
+                if (b % (G / BLOCK) == 0) {
+#pragma unroll
+                    for (int i = 0; i < G; ++i)
+                        grp[i] = __uint_as_float(static_cast<uint32_t>(tile[b * BLOCK + i][threadIdx.x]) << 16);
+                    if constexpr (HAD)
+                        fwht_local<G>(grp);
+                }
                 float blk[BLOCK];
 #pragma unroll
                 for (int i = 0; i < BLOCK; ++i)
-                    blk[i] = __uint_as_float(static_cast<uint32_t>(tile[b * BLOCK + i][threadIdx.x]) << 16);
-                if constexpr (HAD)
-                    fwht_local<BLOCK>(blk);
+                    blk[i] = grp[(b % (G / BLOCK)) * BLOCK + i];
                 float bmax = 0.0f;
 #pragma unroll
                 for (int i = 0; i < BLOCK; ++i)
@@ -1190,6 +1269,22 @@ int launch_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, co
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+int launch_had_amax(const void* x, int64_t R, int64_t C, int64_t ld, int dir, float* amax, const Device& d,
+                    cudaStream_t s)
+{
+    if (cudaMemsetAsync(amax, 0, sizeof(float), s) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (R == 0 || C == 0)
+        return MX_OK;
+    const int64_t warps = dir == MX_ROWWISE ? (R * (C / 8) + 31) / 32 : (R / 32) * (((C + 1) / 2 + 31) / 32);
+    const int grid = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>((warps + kThreads / 32 - 1) / (kThreads / 32), static_cast<int64_t>(d.sms) * 8)));
+    had_amax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), R, C, ld, dir,
+                                              reinterpret_cast<unsigned*>(amax));
+    count_launch();
+    return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
 int launch_region_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax_rows, float* amax_cols,
                        const Device& d, cudaStream_t s)
 {
@@ -1236,7 +1331,9 @@ int launch_quantize(const QuantArgs& q, const Device& d, cudaStream_t s)
         return had ? launch_q<MX_FMT_MXFP4_E2M1, false, true>(q, d, s)
                    : launch_q<MX_FMT_MXFP4_E2M1, false, false>(q, d, s);
     case MX_FMT_NVFP4:
-        return sr ? launch_q<MX_FMT_NVFP4, true, false>(q, d, s) : launch_q<MX_FMT_NVFP4, false, false>(q, d, s);
+        if (sr)
+            return had ? launch_q<MX_FMT_NVFP4, true, true>(q, d, s) : launch_q<MX_FMT_NVFP4, true, false>(q, d, s);
+        return had ? launch_q<MX_FMT_NVFP4, false, true>(q, d, s) : launch_q<MX_FMT_NVFP4, false, false>(q, d, s);
     case MX_FMT_MOSS_FP8:
         return sr ? launch_q<MX_FMT_MOSS_FP8, true, false>(q, d, s) : launch_q<MX_FMT_MOSS_FP8, false, false>(q, d, s);
     default:

@@ -156,10 +156,13 @@ int mx_amax(const void* x, int64_t R, int64_t C, int64_t ld, float* amax, void* 
  *   rounding   MX_ROUND_RNE or MX_ROUND_SR (every format).
  *   hadamard   1: multiply every 32-element K-block by the fixed-sign
  *              Sylvester H32 (unnormalised, five fp32 butterfly stages in
- *              the order h = 1, 2, 4, 8, 16) before scaling; MX formats only
- *              ([FAF] 两个关键的数值技巧).
- *   amax_in    optional device float holding max |x| (skips the amax pass of
- *              NVFP4/MOSS; it is copied to out->amax); NULL = compute it.
+ *              the order h = 1, 2, 4, 8, 16) before scaling ([FAF]
+ *              两个关键的数值技巧); MX formats and NVFP4 (K % 32 == 0).  For
+ *              NVFP4 the tensor amax is that of the transformed operand,
+ *              max |H32 y| over its 32-element groups along K.
+ *   amax_in    optional device float holding the tensor amax (max |x|, or
+ *              the transformed operand's with hadamard) (skips the amax pass
+ *              of NVFP4/MOSS; it is copied to out->amax); NULL = compute it.
  *   seed, stream_id  the SR Philox key and third counter word.
  * Alignment: x 16-byte aligned, ld % 8 == 0, K % block == 0; for COLWISE also
  * R % 32 == 0.  out->codes 16-byte aligned. */
@@ -174,8 +177,11 @@ int mx_quantize(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int fm
  * transposed operand its backward pass needs come from one pass over memory
  * ([FAF] FP4加速为何常常"纸上富贵": operand packing, layout construction and
  * saving backward state are the costs around the GEMM).  Both outputs share
- * the tensor amax and tensor scale (written to both).  Requires
- * C % block == 0 and R % 32 == 0; other rules as mx_quantize. */
+ * the tensor amax and tensor scale (written to both), except NVFP4 with the
+ * Hadamard transform on either side: each operand then gets the amax and scale
+ * of its own (transformed or plain) values, from a pass of its own over x, and
+ * amax_in must be NULL (MX_ERR_UNSUPPORTED).  Requires C % block == 0 and
+ * R % 32 == 0; other rules as mx_quantize. */
 int mx_quantize_dual(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block,
                      int scale_rule, uint64_t seed, uint32_t stream_id, int row_rounding,
                      int row_hadamard, int col_rounding, int col_hadamard, const float* amax_in,
@@ -247,9 +253,9 @@ int mx_linear_fwd_noalloc(const void* X, const void* W, int64_t T, int64_t Kin, 
 
 /* Backward options ([FAF] 两个关键的数值技巧: stochastic rounding of the
  * gradient and a fixed-sign Hadamard-32 preconditioning of the weight
- * gradient, both on the mxfp route). */
+ * gradient, both on the mxfp route; the same options are offered on NVFP4). */
 typedef struct mx_bwd_opts {
-    int32_t wgrad_hadamard;   /* 1: H32 along tokens on both wgrad operands (MX formats) */
+    int32_t wgrad_hadamard;   /* 1: H32 along tokens on both wgrad operands (MX formats, NVFP4) */
     int32_t wgrad_dy_rounding;/* mx_rounding for dY^T in wgrad */
     uint64_t seed;            /* SR Philox key */
     uint32_t stream_id;       /* SR Philox counter word 2 */

@@ -90,7 +90,7 @@ def test_random_gemm(mx, fmt, mnk, out_dtype):
         assert_gemm_close(c, ref, cabs, f"{fmt} {mnk} {variant}")
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 def test_hadamard_alpha(mx, fmt):
     mx.set_gemm_variant("auto")
     """Both operands transformed: the epilogue applies the 1/32 of (Ha)^T(Hb) = 32 a^T b."""

@@ -46,19 +46,21 @@ def test_backward(mx, fmt):
     assert_gemm_close(dW, ref, cabs, f"wgrad {fmt}")
 
 
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
 @pytest.mark.parametrize("seed,sid", [(42, 0), (1234, 5)])
-def test_mxfp4_wgrad_hadamard_sr(mx, seed, sid):
-    """The mxfp route's weight gradient: H32 on both operands along tokens, SR on dY."""
+def test_fp4_wgrad_hadamard_sr(mx, fmt, seed, sid):
+    """The weight gradient with H32 on both operands along tokens and SR on dY
+    (the mxfp route of the pages, and the same options on NVFP4)."""
     T, Kin, Nout = 512, 256, 384
     X = workloads.draw("normal", (T, Kin), 81)
     W = workloads.draw("normal", (Nout, Kin), 82, 0.02)
     dY = workloads.draw("student_t3", (T, Nout), 83, 1e-3)
-    _, dW = mx.linear_bwd(dY.cuda(), X.cuda(), W.cuda(), "mxfp4", wgrad_hadamard=True,
+    _, dW = mx.linear_bwd(dY.cuda(), X.cuda(), W.cuda(), fmt, wgrad_hadamard=True,
                           wgrad_dy_rounding="sr", seed=seed, stream_id=sid, need_dx=False)
-    ra = orc.quantize(bits(dY), "mxfp4", "col", rounding="sr", seed=seed, stream_id=sid, hadamard=True)
-    rb = orc.quantize(bits(X), "mxfp4", "col", hadamard=True)
+    ra = orc.quantize(bits(dY), fmt, "col", rounding="sr", seed=seed, stream_id=sid, hadamard=True)
+    rb = orc.quantize(bits(X), fmt, "col", hadamard=True)
     ref, cabs = orc.gemm(ra, rb, extra_alpha=1.0 / 32)
-    assert_gemm_close(dW, ref, cabs, "wgrad mxfp4 H32+SR")
+    assert_gemm_close(dW, ref, cabs, f"wgrad {fmt} H32+SR")
     # and the result estimates the exact dY^T X
     exact = (dY.double().t() @ X.double()).numpy()
     rel = np.linalg.norm(dW.cpu().double().numpy() - exact) / np.linalg.norm(exact)
@@ -96,8 +98,8 @@ def test_saved_state_path_equals_the_plain_layer(mx, fmt, hadamard, rounding):
     """mx_linear_fwd_save + mx_linear_bwd_saved read X, W and dY once each and
     give bit for bit what mx_linear_fwd + mx_linear_bwd give, and the oracle's
     composition of the same quantizations and GEMMs."""
-    if hadamard and fmt not in ("mxfp8", "mxfp4"):
-        pytest.skip("the Hadamard transform is offered on the MX formats")
+    if hadamard and fmt not in ("mxfp8", "mxfp4", "nvfp4"):
+        pytest.skip("the Hadamard transform is offered on the MX formats and NVFP4")
     T, Kin, Nout = 512, 256, 768
     X = workloads.draw("student_t3", (T, Kin), 171).cuda()
     W = workloads.draw("normal", (Nout, Kin), 172, 0.02).cuda()

@@ -80,7 +80,7 @@ def test_stochastic_rounding(mx, fmt, direction, seed, stream_id):
     assert_quant_equal(q, ref, f"SR {fmt}/{direction}/{seed}")
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("direction", ["row", "col"])
 def test_hadamard(mx, fmt, direction):
     x = workloads.draw("outliers", (416, 544), 6)
@@ -140,7 +140,13 @@ def test_zero_tensor_and_empty(mx):
 def test_argument_errors(mx):
     x = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(mx.MXError) as e:
-        mx.quantize(x, "nvfp4", hadamard=True)
+        mx.quantize(x, "moss", hadamard=True)
+    assert e.value.code == mx.MX_ERR_UNSUPPORTED
+    with pytest.raises(mx.MXError) as e:  # NVFP4 blocks of 16, but the transform needs whole 32-groups
+        mx.quantize(torch.zeros(64, 48, dtype=torch.bfloat16, device="cuda"), "nvfp4", hadamard=True)
+    assert e.value.code == mx.MX_ERR_ALIGNMENT
+    with pytest.raises(mx.MXError) as e:  # one caller amax cannot serve two differently transformed operands
+        mx.quantize_dual(x, "nvfp4", col_hadamard=True, amax_in=torch.ones(1, device="cuda"))
     assert e.value.code == mx.MX_ERR_UNSUPPORTED
     with pytest.raises(mx.MXError) as e:
         mx.quantize(torch.zeros(48, 64, dtype=torch.bfloat16, device="cuda"), "mxfp8", "col")
@@ -179,10 +185,11 @@ def test_dual_producer_matches_two_single_passes(mx, fmt, shape):
 @pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8", "nvfp4"])
 def test_dual_producer_direction_options(mx, fmt):
     """The weight-gradient pattern: dY rowwise with RNE for dgrad and colwise
-    with SR (+ Hadamard on the mxfp route) for wgrad, from one pass."""
+    with SR and the Hadamard transform for wgrad, from one call (NVFP4: each
+    direction with its own tensor amax)."""
     x = workloads.draw("student_t3", (512, 384), 31, 1e-3)
     sr = "sr"
-    had = fmt != "nvfp4"
+    had = True
     qr, qc = mx.quantize_dual(x.cuda(), fmt, seed=42, stream_id=1, col_rounding=sr, col_hadamard=had)
     torch.cuda.synchronize()
     assert_quant_equal(qr, orc.quantize(bits(x), fmt, "row"), f"dual row {fmt}")
@@ -283,3 +290,17 @@ def test_nvfp4_local_sr_and_amax_in(mx, direction):
     with pytest.raises(mx.MXError) as e:  # the dual pass computes its own region maxima
         mx.quantize_dual(x.cuda(), "nvfp4_local", amax_in=ain.cuda())
     assert e.value.code == mx.MX_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("direction", ["row", "col"])
+def test_nvfp4_hadamard_amax_is_of_the_transformed_operand(mx, direction):
+    """NVFP4 with the transform: the tensor amax is max |H32 x| over the operand
+    (not max |x|), and a caller amax is taken as given."""
+    x = workloads.draw("student_t3", (512, 640), 41)
+    q, ref = run_both(mx, x, "nvfp4", direction, hadamard=True)
+    assert_quant_equal(q, ref, f"nvfp4 H32 {direction}")
+    assert ref.amax > float(x.float().abs().max())
+    big = torch.tensor([ref.amax * 3], dtype=torch.float32, device="cuda")
+    q2 = mx.quantize(x.cuda(), "nvfp4", direction, hadamard=True, amax_in=big)
+    assert_quant_equal(q2, orc.quantize(bits(x), "nvfp4", direction, hadamard=True, amax_in=ref.amax * 3),
+                       f"nvfp4 H32 caller amax {direction}")
