@@ -45,57 +45,59 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v)
     v[4] = bf16_lo(w.z), v[5] = bf16_hi(w.z), v[6] = bf16_lo(w.w), v[7] = bf16_hi(w.w);
 }
 
-// Stochastic rounding onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}: up iff
-// u16 < p * 2^16, p = (|s| - lo) / (hi - lo); every step below is exact.
-__device__ __forceinline__ uint32_t e2m1_sr(float s, uint32_t u16)
+// Stochastic rounding of 8 values onto the E2M1 grid {0, .5, 1, 1.5, 2, 3,
+// 4, 6}: a value rounds up iff u16 < p * 2^16, p = (|s| - lo) / (hi - lo),
+// saturating at 6; the codes come packed as cvt_e2m1x8 packs them.  lo is
+// |s| with its significand cut to one bit (|s| >= 1), or 0.5 or 0 below 1;
+// the grid spacing above lo is 2^(E - 1) (E the exponent of |s|, at least 0),
+// so p * 2^16 = (|s| - lo) * 2^(17 - E) exactly.  No branches: the whole
+// warp takes one path whatever the values.  lo's code (exact, on the grid)
+// comes from the hardware conversion; the round-up bit and the sign are added
+// per nibble (lo's code is at most 6, so nothing carries).
+__device__ __forceinline__ uint32_t e2m1_sr8(const float* s, const uint32_t (&u)[8])
 {
-    const uint32_t sign = (__float_as_uint(s) >> 31) << 3;
-    const float a = fabsf(s);
-    if (a >= 6.0f)
-        return sign | 7u;
-    float lo, inv_step;
-    uint32_t code;
-    if (a < 2.0f) {
-        lo = floorf(a * 2.0f) * 0.5f;
-        inv_step = 2.0f;
-        code = static_cast<uint32_t>(lo * 2.0f);
-    } else if (a < 4.0f) {
-        lo = floorf(a);
-        inv_step = 1.0f;
-        code = static_cast<uint32_t>(lo) + 2u;
-    } else {
-        lo = 4.0f;
-        inv_step = 0.5f;
-        code = 6u;
+    float lo[8];
+    uint32_t extra = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = fminf(fabsf(s[i]), 6.0f);
+        const uint32_t ab = __float_as_uint(a);
+        const float l = a >= 1.0f ? __uint_as_float(ab & 0xFFC00000u) : (a >= 0.5f ? 0.5f : 0.0f);
+        const int E = max(static_cast<int>(ab >> 23) - 127, 0);
+        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(static_cast<uint32_t>(144 - E) << 23));
+        lo[i] = l;
+        const uint32_t up = static_cast<float>(u[i]) < t ? 1u : 0u;
+        extra |= (up | ((__float_as_uint(s[i]) >> 31) << 3)) << (4 * i);
     }
-    if (a == lo)
-        return sign | code;
-    const float p16 = __fmul_rn(__fsub_rn(a, lo), inv_step * 65536.0f);
-    return sign | (static_cast<float>(u16) < p16 ? code + 1u : code);
+    return cvt_e2m1x8(lo) + extra;
 }
 
-// Stochastic rounding onto the E4M3 grid with the same rule (up iff
-// u16 < p * 2^16, p = (|s| - lo) / (hi - lo)), saturating at 448.  lo is |s|
-// with its significand cut to 3 bits (normal range) or a multiple of 2^-9
-// (subnormal range); the step is a power of two, so every operation is exact.
-__device__ __forceinline__ uint32_t e4m3_sr(float s, uint32_t u16)
+// Stochastic rounding of 8 values onto the E4M3 grid with the same rule (up
+// iff u16 < p * 2^16, p = (|s| - lo) / (hi - lo)), saturating at 448; codes
+// packed one per byte, element 0 in the low byte of out[0].  lo is |s| with
+// its significand cut to 3 bits (normal range) or a multiple of 2^-9
+// (subnormal range, |s| < 2^-6); the spacing above lo is 2^(E' - 3), E' the
+// exponent of |s| but at least -6, so p * 2^16 = (|s| - lo) * 2^(19 - E')
+// exactly.  Branch-free, like e2m1_sr8; lo's code is at most 0x7E - 1 when a
+// round-up can happen, so adding the up bit never carries into the sign.
+__device__ __forceinline__ void e4m3_sr8(const float* s, const uint32_t (&u)[8], uint32_t* out)
 {
-    const uint32_t sign = (__float_as_uint(s) >> 31) << 7;
-    const float a = fabsf(s);
-    if (a >= 448.0f)
-        return sign | 0x7Eu;
-    float lo, inv_step;  // inv_step = 2^16 / (hi - lo)
-    if (a < 0x1p-6f) {
-        lo = __fmul_rn(floorf(__fmul_rn(a, 512.0f)), 0x1p-9f);
-        inv_step = 0x1p25f;
-    } else {
-        lo = __uint_as_float(__float_as_uint(a) & 0xFFF00000u);
-        const int e = static_cast<int>((__float_as_uint(lo) >> 23) & 0xFFu) - 127;  // -6 .. 8
-        inv_step = __uint_as_float(static_cast<uint32_t>(127 + 19 - e) << 23);   // 2^(16 - (e - 3))
+    float lo[8];
+    uint32_t extra[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = fminf(fabsf(s[i]), 448.0f);
+        const uint32_t ab = __float_as_uint(a);
+        const int E = max(static_cast<int>(ab >> 23) - 127, -6);
+        const float l = a >= 0x1p-6f ? __uint_as_float(ab & 0xFFF00000u)
+                                      : __fmul_rn(floorf(__fmul_rn(a, 512.0f)), 0x1p-9f);
+        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(static_cast<uint32_t>(146 - E) << 23));
+        lo[i] = l;
+        const uint32_t up = static_cast<float>(u[i]) < t ? 1u : 0u;
+        extra[i >> 2] |= (up | ((__float_as_uint(s[i]) >> 31) << 7)) << (8 * (i & 3));
     }
-    const uint32_t code = cvt_e4m3x2(lo, 0.0f) & 0x7Fu;  // lo is on the grid
-    const float t = __fmul_rn(__fsub_rn(a, lo), inv_step);
-    return sign | (static_cast<float>(u16) < t ? code + 1u : code);
+    out[0] = (cvt_e4m3x2(lo[0], lo[1]) | (cvt_e4m3x2(lo[2], lo[3]) << 16)) + extra[0];
+    out[1] = (cvt_e4m3x2(lo[4], lo[5]) | (cvt_e4m3x2(lo[6], lo[7]) << 16)) + extra[1];
 }
 
 // ------------------------------------------------------------- Philox4x32-10
@@ -387,12 +389,7 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
             for (int g = 0; g < N / 8; ++g) {
                 uint32_t u[8];
                 sr_bits8(seed, sid, L8 + g, u);
-                uint32_t b[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    b[i] = e4m3_sr(v[8 * g + i], u[i]);
-                out[2 * g] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                out[2 * g + 1] = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+                e4m3_sr8(&v[8 * g], u, &out[2 * g]);
             }
         } else {
 #pragma unroll
@@ -410,9 +407,7 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
             } else if constexpr (SR) {
                 uint32_t u[8];
                 sr_bits8(seed, sid, L8 + w, u);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    word |= e2m1_sr(v[8 * w + i], u[i]) << (4 * i);
+                word = e2m1_sr8(&v[8 * w], u);
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -747,12 +742,9 @@ __device__ __forceinline__ uint32_t nvfp4_local_encode(float (&v)[N], float bmax
 #pragma unroll
     for (int w = 0; w < N / 8; ++w) {
         if constexpr (SR) {
-            uint32_t u[8], word = 0;
+            uint32_t u[8];
             sr_bits8(seed, sid, L8 + w, u);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                word |= e2m1_sr(v[8 * w + i], u[i]) << (4 * i);
-            out[w] = word;
+            out[w] = e2m1_sr8(&v[8 * w], u);
         } else {
             float q[8];
 #pragma unroll
