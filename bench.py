@@ -445,14 +445,26 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
     pinned-host -> device copies of every input, mx.linear_fwd_save (which keeps
     X^T and W^T for the backward) and mx.linear_bwd_saved, so X, W and dY are
     each read once on the device, as in the kernel-level step; device ->
-    pinned-host copies of every output; all inside the timed region (copies
-    overlap the compute of neighbouring layers on their own streams)."""
+    pinned-host copies of every output; all inside the timed region.  Copies
+    run on their own streams and overlap the compute of neighbouring layers;
+    the device buffers alternate between two sets by step parity, so a step's
+    copies overlap the previous step's as well."""
     host_in = {k: v.cpu().pin_memory() for k, v in dev_inputs.items()}
-    bufs = []
-    for fmt in wl.formats:
-        for g in wl.gemms:
+    units = [(fmt, g) for fmt in wl.formats for g in wl.gemms]
+    host_out = []
+    for fmt, g in units:  # one pinned host copy of each result (each step overwrites it)
+        T, Kin, Nout = g.tokens, g.k_in, g.n_out
+        host_out.append(dict(hY=torch.empty(T, Nout, dtype=torch.bfloat16).pin_memory(),
+                             hdX=torch.empty(T, Kin, dtype=torch.bfloat16).pin_memory(),
+                             hdW=torch.empty(Nout, Kin, dtype=torch.float32).pin_memory()))
+    compute = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    sets = []
+    for _ in range(2):
+        bufs = []
+        for u, (fmt, g) in enumerate(units):
             T, Kin, Nout = g.tokens, g.k_in, g.n_out
-            b = dict(g=g, fmt=fmt)
+            b = dict(g=g, fmt=fmt, host=host_out[u])
             b["X"], b["W"], b["dY"] = (torch.empty_like(dev_inputs[g.x.name]), torch.empty_like(dev_inputs[g.w.name]),
                                        torch.empty_like(dev_inputs[g.dy.name]))
             b["Y"] = torch.empty(T, Nout, dtype=torch.bfloat16, device=device)
@@ -462,31 +474,20 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
             b["wsb"] = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "bwd_saved"), dtype=torch.uint8,
                                    device=device)
             b["saved"] = torch.empty(mx.saved_bytes(T, Kin, Nout, fmt), dtype=torch.uint8, device=device)
-            b["hY"] = torch.empty(b["Y"].shape, dtype=b["Y"].dtype).pin_memory()
-            b["hdX"] = torch.empty(b["dX"].shape, dtype=b["dX"].dtype).pin_memory()
-            b["hdW"] = torch.empty(b["dW"].shape, dtype=b["dW"].dtype).pin_memory()
+            b["in_ready"], b["computed"], b["out_done"] = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            b["computed"].record(compute)
+            b["out_done"].record(compute)
             bufs.append(b)
-    h2d = sum(host_in[b["g"].x.name].nbytes + host_in[b["g"].w.name].nbytes + host_in[b["g"].dy.name].nbytes
-              for b in bufs)
-    d2h = sum(b["Y"].nbytes + b["dX"].nbytes + b["dW"].nbytes for b in bufs)
-    flops = sum(6.0 * b["g"].tokens * b["g"].k_in * b["g"].n_out for b in bufs)
+        sets.append(bufs)
+    h2d = sum(host_in[g.x.name].nbytes + host_in[g.w.name].nbytes + host_in[g.dy.name].nbytes for _, g in units)
+    d2h = sum(b["Y"].nbytes + b["dX"].nbytes + b["dW"].nbytes for b in sets[0])
+    flops = sum(6.0 * g.tokens * g.k_in * g.n_out for _, g in units)
 
-    # Three streams: host->device copies, compute, device->host copies.  Unit
-    # u's inputs land while unit u-1 computes and its outputs leave while unit
-    # u+1 computes; events keep a buffer from being overwritten before the
-    # previous step is done with it.
-    compute = torch.cuda.current_stream()
-    h2d_s, d2h_s = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    for b in bufs:
-        b["in_ready"], b["computed"], b["out_done"] = ev(), ev(), ev()
-        b["computed"].record(compute)
-        b["out_done"].record(compute)
-
-    def step():
+    def step(k):
+        bufs = sets[k % 2]
         for b in bufs:
             g = b["g"]
-            h2d_s.wait_event(b["computed"])  # the previous step no longer reads these inputs
+            h2d_s.wait_event(b["computed"])  # this set's previous step no longer reads these inputs
             with torch.cuda.stream(h2d_s):
                 b["X"].copy_(host_in[g.x.name], non_blocking=True)
                 b["W"].copy_(host_in[g.w.name], non_blocking=True)
@@ -494,30 +495,36 @@ def run_e2e(mx, wl, dev_inputs, device, args, world):
             b["in_ready"].record(h2d_s)
         for b in bufs:
             compute.wait_event(b["in_ready"])
-            compute.wait_event(b["out_done"])  # the previous step's outputs have left
+            compute.wait_event(b["out_done"])  # this set's previous outputs have left
             mx.linear_fwd_save(b["X"], b["W"], b["fmt"], workspace=b["wsf"], saved=b["saved"], out=b["Y"])
             mx.linear_bwd_saved(b["dY"], b["saved"], b["g"].k_in, b["fmt"], workspace=b["wsb"], dX=b["dX"],
                                 dW=b["dW"])
             b["computed"].record(compute)
             d2h_s.wait_event(b["computed"])
+            h = b["host"]
             with torch.cuda.stream(d2h_s):
-                b["hY"].copy_(b["Y"], non_blocking=True)
-                b["hdX"].copy_(b["dX"], non_blocking=True)
-                b["hdW"].copy_(b["dW"], non_blocking=True)
+                h["hY"].copy_(b["Y"], non_blocking=True)
+                h["hdX"].copy_(b["dX"], non_blocking=True)
+                h["hdW"].copy_(b["dW"], non_blocking=True)
             b["out_done"].record(d2h_s)
-        for b in bufs:  # the step ends when its last result is on the host
-            compute.wait_event(b["out_done"])
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        step()
+    def drain():  # every result of every step issued so far is on the host
+        for bufs in sets:
+            for b in bufs:
+                compute.wait_event(b["out_done"])
+
+    for k in range(max(2, min(args.warmup, 4))):
+        step(k)
+    drain()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for k in range(args.steps):
+        step(k)
+    drain()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = reduce_max(t0.elapsed_time(t1) / args.steps, world)
