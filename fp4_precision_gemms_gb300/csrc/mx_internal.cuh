@@ -80,6 +80,8 @@ struct TileArgs {
     // x for the colwise one).
     const float* row_ts_v;
     const float* col_ts_v;
+    // set by the launcher: 1 when the codes leave through TMA tensor stores
+    int tma_st;
 };
 
 // Number of kernels this library has launched in the process.

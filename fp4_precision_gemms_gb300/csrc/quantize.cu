@@ -781,27 +781,43 @@ __device__ __forceinline__ uint32_t nvfp4_encode_fast(const float (&v)[N], float
 }
 
 template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
-__global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const TileArgs a)
+__global__ void __launch_bounds__(kThreads, 2)
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
+                      const __grid_constant__ CUtensorMap tmcol, const TileArgs a)
 {
     constexpr int BLOCK = fmt_block(FMT);
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     constexpr bool HAD_OK = FMT == MX_FMT_MXFP8_E4M3 || FMT == MX_FMT_MXFP4_E2M1;
-    constexpr int CW = BLOCK == 16 ? 4 : 2;  // colwise: columns per thread
+    // colwise task: two adjacent columns x 32 rows (one or two scale blocks per column)
+    constexpr int CW = 2, CROWS = 32, GPB = CROWS / BLOCK;
     constexpr int kColGroups = kTC / CW;
-    static_assert(kColGroups * (kTR / BLOCK) == kThreads, "one colwise task per encoding thread");
-    constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // 32-bit code words per colwise block
+    static_assert(kColGroups * (kTR / CROWS) == kThreads, "one colwise task per encoding thread");
+    constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // 32-bit code words per scale block
+    constexpr int CWW = GPB * WPB;                     // code words per column of a task
+    constexpr int CBB = CROWS * (FP4 ? 1 : 2) / 2;     // code bytes per column of a task
+    constexpr int RB_T = kTC * (FP4 ? 1 : 2) / 2;      // rowwise code bytes per tile row
+    constexpr int ROWREG = kTR * RB_T;                 // staged rowwise codes of a tile
+    static_assert(ROWREG + kTC * (kTR / CROWS) * CBB <= kTileBytes, "staged codes fit the stage");
+    // rowwise task: one scale block of one tile row per lane and step
+    constexpr int CH = BLOCK / 8;             // 8-element chunks per block
+    constexpr int BPR = kTC / BLOCK;          // blocks per tile row
+    constexpr int RPS = 32 / BPR;             // tile rows per warp step
+    constexpr int STEPS = kTR / (RPS * (kThreads / 32));
+    constexpr int CB = FP4 ? 4 : 8;           // code bytes per chunk
     extern __shared__ uint8_t smem_raw[];
     // 128-byte aligned stage base, by pointer arithmetic on the shared array so
     // that the tile reads stay shared-memory loads
     uint8_t* base = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const uint32_t sbase = smem_u32(base);
     const uint32_t full0 = sbase + kTStages * kTileBytes;
+    const uint32_t staged0 = full0 + 8u * kTStages;  // the stage holds the tile's codes (one arrival per warp)
     __shared__ float2 nv_tab[128];
     __shared__ float2 nv_q[128];
     __shared__ int stage_out[kTStages];  // warps done with the stage's current tile
     __shared__ int64_t issued;           // tiles whose copy has been issued
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t R = a.R, C = a.C;
+    const bool tma_st = a.tma_st != 0;
     const ScaleCtx sc = make_scale_ctx<FMT>(a.amax, nv_tab, nv_q, a.rule);
     if ((FMT == MX_FMT_NVFP4 || FMT == MX_FMT_MOSS_FP8) && blockIdx.x == 0 && tid == 0) {
         *a.tensor_scale = sc.ts;
@@ -823,10 +839,17 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     if (tid == 0) {
         for (int st = 0; st < kTStages; ++st) {
             mbar_init(full0 + 8u * st, 1);
+            mbar_init(staged0 + 8u * st, kThreads / 32);
             stage_out[st] = 0;
         }
         fence_mbar_init();
         prefetch_tmap(&tmx);
+        if (tma_st) {
+            if (DO_ROW)
+                prefetch_tmap(&tmrow);
+            if (DO_COL)
+                prefetch_tmap(&tmcol);
+        }
         const int64_t first = my_n < kTStages ? my_n : kTStages;
         for (int64_t i = 0; i < first; ++i)
             issue(i);
@@ -838,44 +861,46 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
     const bool row_had = HAD_OK && a.row_had, col_had = HAD_OK && a.col_had;
     const int64_t kg_row = sf_kgroups(C / BLOCK), kg_col = sf_kgroups(R / BLOCK);
     const int64_t col_row_bytes = FP4 ? R / 2 : R;
-    const int cg = tid % kColGroups, rb = tid / kColGroups;
+    const int cg = tid % kColGroups, rh = tid / kColGroups;
+    bool timed_out = false;
     for (int64_t i = 0; i < my_n; ++i) {
         const int st = static_cast<int>(i % kTStages);
         if (!mbar_wait_bounded(full0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns)) {
             if (lane == 0)
                 atomicExch(a.status, MX_ERR_TIMEOUT);
-            break;
+            timed_out = true;
         }
-        const uint16_t* tile = reinterpret_cast<const uint16_t*>(base + st * kTileBytes);  // [kTR][kTC]
+        // the staged path synchronises the CTA below, so every thread leaves together
+        if (tma_st ? __syncthreads_or(timed_out) : timed_out)
+            break;
+        uint8_t* stage = base + st * kTileBytes;
+        const uint16_t* tile = reinterpret_cast<const uint16_t*>(stage);  // [kTR][kTC]
         const int64_t t = blockIdx.x + i * gridDim.x;
         const int64_t rt = t / ctiles, ct = t - rt * ctiles;
         const int64_t r0 = rt * kTR, c0 = ct * kTC;
+
+        // Rowwise: lane = one scale block of one tile row, read as CH 16-byte
+        // chunks.  Plain round-to-nearest passes take the chunks in a
+        // lane-rotated order (slot i holds chunk (i + rot) % CH), which makes
+        // each quarter-warp's loads hit 32 distinct banks; the codes go back to
+        // their own positions when stored.  SR and the Hadamard transform need
+        // the natural order.
+        const int kbl = lane % BPR;
+        const int rot = (ROW_SR || row_had) ? 0 : (CH == 2 ? (lane >> 2) & 1 : (CH == 4 ? (lane >> 1) & 3 : 0));
+        uint32_t rout[DO_ROW ? STEPS : 1][FP4 ? BLOCK / 8 : BLOCK / 4];
         if constexpr (DO_ROW) {
-            // Lane = one scale block of one tile row, read as BLOCK / 8 16-byte
-            // chunks.  Plain round-to-nearest passes take the chunks in a
-            // lane-rotated order (slot i holds chunk (i + rot) % CH), which makes
-            // each quarter-warp's loads hit 32 distinct banks; codes are stored
-            // chunk by chunk at their own positions, so the order never needs
-            // undoing.  SR and the Hadamard transform need the natural order.
-            constexpr int CH = BLOCK / 8;                              // chunks per block
-            constexpr int BPR = kTC / BLOCK;                           // blocks per tile row
-            constexpr int RPS = 32 / BPR;                              // tile rows per warp step
-            constexpr int STEPS = kTR / (RPS * (kThreads / 32));
-            constexpr int CB = FP4 ? 4 : 8;                            // code bytes per chunk
-            const int kbl = lane % BPR;
             const int64_t col = c0 + kbl * BLOCK;
             const int64_t kb = col / BLOCK;
             const int64_t sf_in_row = (kb >> 2) * 512 + (kb & 3);
-            const int rot = (ROW_SR || row_had) ? 0 : (CH == 2 ? (lane >> 2) & 1 : (lane >> 1) & 3);
-#pragma unroll 1
+#pragma unroll
             for (int s2 = 0; s2 < STEPS; ++s2) {
                 const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
                 const int64_t row = r0 + rr;
                 const uint16_t* src = tile + rr * kTC + kbl * BLOCK;
                 float v[BLOCK];
 #pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    unpack8(*reinterpret_cast<const uint4*>(src + ((i + rot) & (CH - 1)) * 8), v + 8 * i);
+                for (int c = 0; c < CH; ++c)
+                    unpack8(*reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8), v + 8 * c);
                 if constexpr (HAD_OK) {
                     if (row_had)
                         fwht_local<BLOCK>(v);
@@ -886,7 +911,8 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                     bmax = fmaxf(bmax, fabsf(v[e]));
                 if constexpr (FMT == MX_FMT_MOSS_FP8)
                     bmax = moss_block(v, bmax, sc);
-                uint32_t out[FP4 ? BLOCK / 8 : BLOCK / 4], sfb;
+                uint32_t* out = rout[s2];
+                uint32_t sfb;
                 if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
                     const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
                     sfb = nvfp4_local_encode<ROW_SR, BLOCK>(v, bmax, a.row_ts_v[r0 >> 7], a.seed, a.stream_id, L8, out);
@@ -900,132 +926,168 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tile_kernel(const __grid_co
                     sfb = encode_block<FMT, ROW_SR, BLOCK>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
                 }
                 if (row < R && col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
-                    uint8_t* dst = a.row_codes + row * (FP4 ? C / 2 : C) + (FP4 ? col / 2 : col);
+                    if (!tma_st) {
+                        uint8_t* dst = a.row_codes + row * (FP4 ? C / 2 : C) + (FP4 ? col / 2 : col);
 #pragma unroll
-                    for (int i = 0; i < CH; ++i) {
-                        const int c = (i + rot) & (CH - 1);
-                        if constexpr (FP4)
-                            *reinterpret_cast<uint32_t*>(dst + c * CB) = out[i];
-                        else
-                            *reinterpret_cast<uint2*>(dst + c * CB) = make_uint2(out[2 * i], out[2 * i + 1]);
+                        for (int c = 0; c < CH; ++c) {
+                            const int cc = (c + rot) & (CH - 1);
+                            if constexpr (FP4)
+                                *reinterpret_cast<uint32_t*>(dst + cc * CB) = out[c];
+                            else
+                                *reinterpret_cast<uint2*>(dst + cc * CB) = make_uint2(out[2 * c], out[2 * c + 1]);
+                        }
                     }
                     const int64_t sf_row = ((row >> 7) * kg_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
                     a.row_sf[sf_row + sf_in_row] = static_cast<uint8_t>(sfb);
                 }
             }
         }
+
+        // Colwise: thread = two adjacent columns x 32 rows.  Each shared-memory
+        // load brings both columns of one row (a warp reads 128 contiguous bytes
+        // of that row: no bank conflicts); each column's 32 values are one MX
+        // block or two NVFP4 blocks, encoded in registers.
+        const int64_t kabs = r0 + rh * CROWS;  // first row (K) of this task
+        uint32_t cout[DO_COL ? CW : 1][CWW];
         if constexpr (DO_COL) {
-            // Thread = CW adjacent columns x one scale block of rows: each
-            // shared-memory load brings CW columns of one row (a warp reads
-            // 32 * CW contiguous elements of that row: no bank conflicts), and
-            // each column's block is encoded in registers.
-            const int64_t kabs = r0 + rb * BLOCK;
-            if (kabs < R) {  // R % 32 == 0: a row block is wholly in or out
-                uint32_t pk[BLOCK][CW / 2];  // bf16 pairs: pk[e][p] = columns 2p, 2p + 1 of row e
+            if (kabs < R) {  // R % 32 == 0: a task's rows are wholly in or out
+                uint32_t pk[CROWS];  // bf16 pairs: columns 2 cg, 2 cg + 1 of row e
 #pragma unroll
-                for (int e = 0; e < BLOCK; ++e) {
-                    const uint16_t* src = tile + (rb * BLOCK + e) * kTC + cg * CW;
-                    if constexpr (CW == 4) {
-                        const uint2 w = *reinterpret_cast<const uint2*>(src);
-                        pk[e][0] = w.x;
-                        pk[e][CW / 2 - 1] = w.y;
-                    } else {
-                        pk[e][0] = *reinterpret_cast<const uint32_t*>(src);
-                    }
-                }
-                auto unpack = [&](int j, float (&blk)[BLOCK]) {
-#pragma unroll
-                    for (int e = 0; e < BLOCK; ++e)
-                        blk[e] = (j & 1) ? bf16_hi(pk[e][j / 2]) : bf16_lo(pk[e][j / 2]);
-                };
+                for (int e = 0; e < CROWS; ++e)
+                    pk[e] = *reinterpret_cast<const uint32_t*>(tile + (rh * CROWS + e) * kTC + cg * CW);
                 const int64_t cbase = c0 + cg * CW;
-                const int64_t sf_col = sf_offset(cbase, kabs / BLOCK, kg_col);  // + 16 j for column cbase + j
-                auto store = [&](int j, const uint32_t (&out)[WPB], uint32_t sfb) {
-                    const int64_t c = cbase + j;
-                    if (c < C) {
-                        uint8_t* dst = a.col_codes + c * col_row_bytes + (FP4 ? kabs / 2 : kabs);
-                        if constexpr (WPB == 2) {
-                            *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < WPB / 4; ++q)
-                                reinterpret_cast<uint4*>(dst)[q] =
-                                    make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-                        }
-                        a.col_sf[sf_col + 16 * j] = static_cast<uint8_t>(sfb);
-                    }
-                };
-                uint32_t redo_mask = 0;
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
-                    float blk[BLOCK];
-                    unpack(j, blk);
-                    if constexpr (HAD_OK) {
-                        if (col_had)
-                            fwht_local<BLOCK>(blk);
-                    }
-                    float bmax = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < BLOCK; ++e)
-                        bmax = fmaxf(bmax, fabsf(blk[e]));
-                    if constexpr (FMT == MX_FMT_MOSS_FP8)
-                        bmax = moss_block(blk, bmax, sc);
-                    uint32_t out[WPB], sfb;
-                    if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
-                        const uint64_t L8 = static_cast<uint64_t>(cbase + j) * (R / 8) + kabs / 8;
-                        const float ts = cbase < C ? a.col_ts_v[cbase >> 7] : 1.0f;  // past C: zero fill, not stored
-                        sfb = nvfp4_local_encode<COL_SR, BLOCK>(blk, bmax, ts, a.seed, a.stream_id, L8, out);
-                    } else if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
-                        bool redo;
-                        sfb = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out, redo);
-                        redo_mask |= (redo ? 1u : 0u) << j;
-                    } else {
-                        const uint64_t L8 = static_cast<uint64_t>(cbase + j) * (R / 8) + kabs / 8;
-                        sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
-                    }
-                    store(j, out, sfb);
-                }
-                if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
-                    if (redo_mask) {  // rare: a block whose divisor is not certified
+                    for (int g = 0; g < GPB; ++g) {
+                        float blk[BLOCK];
 #pragma unroll
-                        for (int j = 0; j < CW; ++j) {
-                            if (redo_mask & (1u << j)) {
-                                float blk[BLOCK];  // re-read from the stage (still held by this warp)
-#pragma unroll
-                                for (int e = 0; e < BLOCK; ++e)
-                                    blk[e] = __uint_as_float(static_cast<uint32_t>(tile[(rb * BLOCK + e) * kTC + cg * CW + j]) << 16);
-                                float bmax = 0.0f;
-#pragma unroll
-                                for (int e = 0; e < BLOCK; ++e)
-                                    bmax = fmaxf(bmax, fabsf(blk[e]));
-                                uint32_t out[WPB];
-                                const uint32_t sfb = encode_block<FMT, false, BLOCK>(blk, bmax, sc, a.rule, 0, 0, 0, out);
-                                store(j, out, sfb);
-                            }
+                        for (int e = 0; e < BLOCK; ++e)
+                            blk[e] = j ? bf16_hi(pk[g * BLOCK + e]) : bf16_lo(pk[g * BLOCK + e]);
+                        if constexpr (HAD_OK) {
+                            if (col_had)
+                                fwht_local<BLOCK>(blk);
                         }
+                        float bmax = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < BLOCK; ++e)
+                            bmax = fmaxf(bmax, fabsf(blk[e]));
+                        if constexpr (FMT == MX_FMT_MOSS_FP8)
+                            bmax = moss_block(blk, bmax, sc);
+                        const int64_t kblk = kabs + g * BLOCK;
+                        const uint64_t L8 = static_cast<uint64_t>(cbase + j) * (R / 8) + kblk / 8;
+                        uint32_t* out = &cout[j][g * WPB];
+                        uint32_t sfb;
+                        if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
+                            const float ts = cbase < C ? a.col_ts_v[cbase >> 7] : 1.0f;  // past C: zero fill, not stored
+                            sfb = nvfp4_local_encode<COL_SR, BLOCK>(blk, bmax, ts, a.seed, a.stream_id, L8, out);
+                        } else if constexpr (FMT == MX_FMT_NVFP4 && !COL_SR) {
+                            bool redo;
+                            sfb = nvfp4_encode_fast<BLOCK>(blk, bmax, sc, out, redo);  // leaves blk unchanged
+                            if (redo)  // rare: this block's divisor is not certified
+                                sfb = encode_block<FMT, false, BLOCK>(blk, bmax, sc, a.rule, 0, 0, 0, out);
+                        } else {
+                            sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
+                        }
+                        if (cbase + j < C)
+                            a.col_sf[sf_offset(cbase + j, kblk / BLOCK, kg_col)] = static_cast<uint8_t>(sfb);
+                    }
+                    if (!tma_st && cbase + j < C) {
+                        uint8_t* dst = a.col_codes + (cbase + j) * col_row_bytes + (FP4 ? kabs / 2 : kabs);
+#pragma unroll
+                        for (int q = 0; q < CWW / 4; ++q)
+                            reinterpret_cast<uint4*>(dst)[q] =
+                                make_uint4(cout[j][4 * q], cout[j][4 * q + 1], cout[j][4 * q + 2], cout[j][4 * q + 3]);
                     }
                 }
             }
         }
-        __syncwarp();  // every lane of this warp is done reading the stage
-        if (lane == 0) {
-            __threadfence_block();  // release this warp's reads before counting out
-            if (atomicAdd(&stage_out[st], 1) == kThreads / 32 - 1) {  // last warp out refills
-                __threadfence_block();
-                stage_out[st] = 0;
-                if (i + kTStages < my_n) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(i + kTStages);
-                    atomicMax(reinterpret_cast<unsigned long long*>(&issued),
-                              static_cast<unsigned long long>(i + kTStages + 1));
+
+        if (tma_st) {
+            // The codes of the tile go out through TMA tensor stores from the
+            // stage the tile came in on: once every thread is done reading it
+            // (a barrier of the CTA), the codes are written over it (rowwise
+            // [64 rows][row bytes], then colwise [32-row half][256 columns]
+            // [column bytes]) and each warp signals the stage's "staged"
+            // barrier; thread 0 waits for it, stores, and refills the stage of
+            // the previous tile, whose stores have had a tile's time to read it.
+            named_barrier_sync(1, kThreads);
+            if constexpr (DO_ROW) {
+#pragma unroll
+                for (int s2 = 0; s2 < STEPS; ++s2) {
+                    const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
+                    uint8_t* dst = stage + rr * RB_T + kbl * BLOCK * (FP4 ? 1 : 2) / 2;
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) {
+                        const int cc = (c + rot) & (CH - 1);
+                        if constexpr (FP4)
+                            *reinterpret_cast<uint32_t*>(dst + cc * CB) = rout[s2][c];
+                        else
+                            *reinterpret_cast<uint2*>(dst + cc * CB) = make_uint2(rout[s2][2 * c], rout[s2][2 * c + 1]);
+                    }
+                }
+            }
+            if constexpr (DO_COL) {
+#pragma unroll
+                for (int j = 0; j < CW; ++j) {
+                    uint8_t* dst = stage + ROWREG + (rh * kTC + cg * CW + j) * CBB;
+#pragma unroll
+                    for (int q = 0; q < CWW / 4; ++q)
+                        reinterpret_cast<uint4*>(dst)[q] =
+                            make_uint4(cout[j][4 * q], cout[j][4 * q + 1], cout[j][4 * q + 2], cout[j][4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(staged0 + 8u * st);
+            if (tid == 0) {
+                if (!mbar_wait_bounded(staged0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns)) {
+                    atomicExch(a.status, MX_ERR_TIMEOUT);  // the other warps stop at the next tile's check
+                    timed_out = true;
+                } else {
+                    const uint32_t s = sbase + st * kTileBytes;
+                    if constexpr (DO_ROW)
+                        tma_store_2d(&tmrow, s, static_cast<int32_t>(FP4 ? c0 / 2 : c0), static_cast<int32_t>(r0));
+                    if constexpr (DO_COL)
+                        for (int h = 0; h < kTR / CROWS; ++h)
+                            if (r0 + h * CROWS < R)
+                                tma_store_2d(&tmcol, s + ROWREG + h * kTC * CBB,
+                                             static_cast<int32_t>(FP4 ? (r0 + h * CROWS) / 2 : r0 + h * CROWS),
+                                             static_cast<int32_t>(c0));
+                    bulk_commit();
+                    // the previous tile's stores have read its stage: refill it
+                    if (i >= 1 && i - 1 + kTStages < my_n) {
+                        bulk_wait_read_1();
+                        issue(i - 1 + kTStages);
+                        issued = i - 1 + kTStages + 1;
+                    }
+                }
+            }
+        } else {
+            __syncwarp();  // every lane of this warp is done reading the stage
+            if (lane == 0) {
+                __threadfence_block();  // release this warp's reads before counting out
+                if (atomicAdd(&stage_out[st], 1) == kThreads / 32 - 1) {  // last warp out refills
+                    __threadfence_block();
+                    stage_out[st] = 0;
+                    if (i + kTStages < my_n) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue(i + kTStages);
+                        atomicMax(reinterpret_cast<unsigned long long*>(&issued),
+                                  static_cast<unsigned long long>(i + kTStages + 1));
+                    }
                 }
             }
         }
     }
     // Leave only when no copy into this CTA's shared memory can still be in
-    // flight (after a timeout some issued tiles were never consumed).
+    // flight (after a timeout some issued tiles were never consumed) and the
+    // TMA stores have completed.
     __syncthreads();
     if (tid == 0) {
+        if (tma_st)
+            bulk_wait_all();
         const int64_t n = issued;
         for (int64_t j = n > kTStages ? n - kTStages : 0; j < n; ++j)
             (void)mbar_wait_bounded(full0 + 8u * static_cast<int>(j % kTStages),
@@ -1182,11 +1244,29 @@ EncodeTiledFnQ encode_fn_q()
     return fn;
 }
 
+// 2-D map over a row-major byte matrix [rows, row_bytes] for TMA stores of
+// box_bytes x box_rows boxes; false where the map cannot describe it (row
+// stride not a multiple of 16 bytes).
+bool make_code_store_map(CUtensorMap* m, void* base, int64_t rows, int64_t row_bytes, int box_bytes, int box_rows)
+{
+    EncodeTiledFnQ enc = encode_fn_q();
+    if (!enc || row_bytes % 16 != 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
-int launch_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
+int launch_tile(const TileArgs& t_in, int64_t ld, const Device& d, cudaStream_t s)
 {
     auto kernel = quant_tile_kernel<FMT, DO_ROW, DO_COL, ROW_SR, COL_SR>;
     constexpr int smem = kTStages * kTileBytes + kTStages * 8 + 128;
+    constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     static int configured_device = -1;
     if (configured_device != d.id) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -1196,6 +1276,7 @@ int launch_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
     EncodeTiledFnQ enc = encode_fn_q();
     if (!enc)
         return MX_ERR_CUDA;
+    TileArgs t = t_in;
     CUtensorMap m;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(t.C), static_cast<cuuint64_t>(t.R)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
@@ -1205,9 +1286,20 @@ int launch_tile(const TileArgs& t, int64_t ld, const Device& d, cudaStream_t s)
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return MX_ERR_CUDA;
+    // The codes leave through TMA stores when both code arrays can be
+    // described by tensor maps (row strides that are multiples of 16 bytes),
+    // else through direct stores.
+    CUtensorMap mrow = m, mcol = m;
+    const int64_t row_bytes = FP4 ? t.C / 2 : t.C, col_bytes = FP4 ? t.R / 2 : t.R;
+    bool ok = true;
+    if (DO_ROW)
+        ok = ok && make_code_store_map(&mrow, t.row_codes, t.R, row_bytes, FP4 ? kTC / 2 : kTC, kTR);
+    if (DO_COL)
+        ok = ok && make_code_store_map(&mcol, t.col_codes, t.C, col_bytes, FP4 ? 16 : 32, kTC);
+    t.tma_st = ok ? 1 : 0;
     const int64_t tiles = ((t.R + kTR - 1) / kTR) * ((t.C + kTC - 1) / kTC);
     const int grid = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(d.sms) * 2));
-    kernel<<<grid, kThreads, smem, s>>>(m, t);
+    kernel<<<grid, kThreads, smem, s>>>(m, mrow, mcol, t);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
