@@ -780,6 +780,122 @@ __device__ __forceinline__ uint32_t nvfp4_encode_fast(const float (&v)[N], float
     return sb;
 }
 
+// ------------------------------------------------ packed-pair block encoding
+// Round-to-nearest encodes of the MX formats in the tile producer, on element
+// pairs: the block maxima come from the raw bf16 words by the bf16x2 absolute
+// maximum (a compare, so exact), and the power-of-two scaling uses the paired
+// FP32 multiply (two independent IEEE products, each rounded to nearest with
+// no flushing, exactly as __fmul_rn rounds).  The codes are those of
+// encode_block.  Both paired instructions issue at half the scalar rate, so
+// they save issue slots, not pipe time: measured, this pays for the MX
+// formats and not for NVFP4 and MOSS, whose products are dependent pairs.
+
+// max(|a|, |b|) per bf16 half; the result's sign bits are the xor of the
+// inputs' and are cleared by the caller.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// max |x| per half over W words (W a power of two), sign bits cleared.
+template <int W>
+__device__ __forceinline__ uint32_t absmax_words(const uint32_t* w)
+{
+    uint32_t m[W / 2];
+#pragma unroll
+    for (int i = 0; i < W / 2; ++i)
+        m[i] = absmax_bf16x2(w[i], w[i + W / 2]);
+#pragma unroll
+    for (int h = W / 4; h >= 1; h >>= 1)
+#pragma unroll
+        for (int i = 0; i < h; ++i)
+            m[i] = absmax_bf16x2(m[i], m[i + h]);
+    return m[0] & 0x7FFF7FFFu;
+}
+
+// {lo, hi} bf16 halves of w times {s.x, s.y}, by one paired multiply.
+__device__ __forceinline__ float2 scale_pair(uint32_t w, float2 s)
+{
+    const float lo = bf16_lo(w), hi = bf16_hi(w);
+    float2 d;
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(lo), "f"(hi), "f"(s.x), "f"(s.y));
+    return d;
+}
+
+// One MX block of N consecutive elements given as N/2 bf16 words (element 2i
+// in the low half of word i): its scale byte and codes (packed as
+// encode_block packs them).
+template <int FMT, int N>
+__device__ __forceinline__ uint32_t row_encode_packed(const uint32_t (&w)[N / 2], int rule, uint32_t* out)
+{
+    const uint32_t mw = absmax_words<N / 2>(w);
+    const int e = pow2_exponent<elem_of(FMT)>(fmaxf(bf16_lo(mw), bf16_hi(mw)), rule);
+    const float2 s2 = make_float2(exp2_neg(e), exp2_neg(e));
+    if constexpr (elem_of(FMT) == kElemE4M3) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            const float2 a = scale_pair(w[2 * i], s2), b = scale_pair(w[2 * i + 1], s2);
+            out[i] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 8; ++i) {
+            float q[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 a = scale_pair(w[4 * i + j], s2);
+                q[2 * j] = a.x;
+                q[2 * j + 1] = a.y;
+            }
+            out[i] = cvt_e2m1x8(q);
+        }
+    }
+    return static_cast<uint32_t>(e + 127);
+}
+
+// Two MX colwise blocks at once: N words, word e holding row e of column A
+// (low half) and of column B (high half).  Scale bytes and codes per column.
+template <int FMT, int N>
+__device__ __forceinline__ void col_encode_packed(const uint32_t* pk, int rule, uint32_t* outA, uint32_t* outB,
+                                                  uint32_t& sfA, uint32_t& sfB)
+{
+    const uint32_t mw = absmax_words<N>(pk);
+    const int eA = pow2_exponent<elem_of(FMT)>(bf16_lo(mw), rule);
+    const int eB = pow2_exponent<elem_of(FMT)>(bf16_hi(mw), rule);
+    const float2 s2 = make_float2(exp2_neg(eA), exp2_neg(eB));
+    sfA = static_cast<uint32_t>(eA + 127);
+    sfB = static_cast<uint32_t>(eB + 127);
+    if constexpr (elem_of(FMT) == kElemE4M3) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            float2 q[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                q[j] = scale_pair(pk[4 * i + j], s2);
+            outA[i] = cvt_e4m3x2(q[0].x, q[1].x) | (cvt_e4m3x2(q[2].x, q[3].x) << 16);
+            outB[i] = cvt_e4m3x2(q[0].y, q[1].y) | (cvt_e4m3x2(q[2].y, q[3].y) << 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 8; ++i) {
+            float qa[8], qb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 q = scale_pair(pk[8 * i + j], s2);
+                qa[j] = q.x;
+                qb[j] = q.y;
+            }
+            outA[i] = cvt_e2m1x8(qa);
+            outB[i] = cvt_e2m1x8(qb);
+        }
+    }
+}
+
 template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
@@ -798,6 +914,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr int RB_T = kTC * (FP4 ? 1 : 2) / 2;      // rowwise code bytes per tile row
     constexpr int ROWREG = kTR * RB_T;                 // staged rowwise codes of a tile
     static_assert(ROWREG + kTC * (kTR / CROWS) * CBB <= kTileBytes, "staged codes fit the stage");
+    // MX round-to-nearest encodes without the transform take the packed-pair
+    // path (measured: faster for the MX formats; NVFP4 and MOSS, whose
+    // products are pairs of dependent operations, run faster on the scalar path)
+    constexpr bool ROW_PACKED = HAD_OK && !ROW_SR;
+    constexpr bool COL_PACKED = HAD_OK && !COL_SR;
+    static_assert(CW == 2, "the packed colwise encode takes two columns");
     // rowwise task: one scale block of one tile row per lane and step
     constexpr int CH = BLOCK / 8;             // 8-element chunks per block
     constexpr int BPR = kTC / BLOCK;          // blocks per tile row
@@ -897,33 +1019,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
                 const int64_t row = r0 + rr;
                 const uint16_t* src = tile + rr * kTC + kbl * BLOCK;
-                float v[BLOCK];
-#pragma unroll
-                for (int c = 0; c < CH; ++c)
-                    unpack8(*reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8), v + 8 * c);
-                if constexpr (HAD_OK) {
-                    if (row_had)
-                        fwht_local<BLOCK>(v);
-                }
-                float bmax = 0.0f;
-#pragma unroll
-                for (int e = 0; e < BLOCK; ++e)
-                    bmax = fmaxf(bmax, fabsf(v[e]));
-                if constexpr (FMT == MX_FMT_MOSS_FP8)
-                    bmax = moss_block(v, bmax, sc);
                 uint32_t* out = rout[s2];
-                uint32_t sfb;
-                if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
+                uint32_t sfb = 0;
+                bool scalar = true;  // encode on the scalar path (SR, the transform, or not an MX format)
+                if constexpr (ROW_PACKED) {
+                    if (!row_had) {
+                        uint32_t w[BLOCK / 2];
+#pragma unroll
+                        for (int c = 0; c < CH; ++c) {
+                            const uint4 q = *reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8);
+                            w[4 * c] = q.x, w[4 * c + 1] = q.y, w[4 * c + 2] = q.z, w[4 * c + 3] = q.w;
+                        }
+                        sfb = row_encode_packed<FMT, BLOCK>(w, a.rule, out);
+                        scalar = false;
+                    }
+                }
+                if (scalar) {
+                    float v[BLOCK];
+#pragma unroll
+                    for (int c = 0; c < CH; ++c)
+                        unpack8(*reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8), v + 8 * c);
+                    if constexpr (HAD_OK) {
+                        if (row_had)
+                            fwht_local<BLOCK>(v);
+                    }
+                    float bmax = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < BLOCK; ++e)
+                        bmax = fmaxf(bmax, fabsf(v[e]));
+                    if constexpr (FMT == MX_FMT_MOSS_FP8)
+                        bmax = moss_block(v, bmax, sc);
                     const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
-                    sfb = nvfp4_local_encode<ROW_SR, BLOCK>(v, bmax, a.row_ts_v[r0 >> 7], a.seed, a.stream_id, L8, out);
-                } else if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
-                    bool redo;
-                    sfb = nvfp4_encode_fast<BLOCK>(v, bmax, sc, out, redo);
-                    if (redo)  // rare: this block's divisor is not certified
-                        sfb = encode_block<FMT, false, BLOCK>(v, bmax, sc, a.rule, 0, 0, 0, out);
-                } else {
-                    const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
-                    sfb = encode_block<FMT, ROW_SR, BLOCK>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
+                    if constexpr (FMT == MX_FMT_NVFP4_LOCAL) {
+                        sfb = nvfp4_local_encode<ROW_SR, BLOCK>(v, bmax, a.row_ts_v[r0 >> 7], a.seed, a.stream_id, L8,
+                                                                out);
+                    } else if constexpr (FMT == MX_FMT_NVFP4 && !ROW_SR) {
+                        bool redo;
+                        sfb = nvfp4_encode_fast<BLOCK>(v, bmax, sc, out, redo);
+                        if (redo)  // rare: this block's divisor is not certified
+                            sfb = encode_block<FMT, false, BLOCK>(v, bmax, sc, a.rule, 0, 0, 0, out);
+                    } else {
+                        sfb = encode_block<FMT, ROW_SR, BLOCK>(v, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
+                    }
                 }
                 if (row < R && col < C) {  // whole scale blocks are in or out (C % BLOCK == 0)
                     if (!tma_st) {
@@ -956,10 +1093,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int e = 0; e < CROWS; ++e)
                     pk[e] = *reinterpret_cast<const uint32_t*>(tile + (rh * CROWS + e) * kTC + cg * CW);
                 const int64_t cbase = c0 + cg * CW;
+                // blocks left to the scalar path: bit j * GPB + g (column j, block g)
+                uint32_t scalar = (1u << (CW * GPB)) - 1u;
+                if constexpr (COL_PACKED) {
+                    if (!col_had) {
+                        scalar = 0;
+#pragma unroll
+                        for (int g = 0; g < GPB; ++g) {
+                            uint32_t sfA, sfB;
+                            col_encode_packed<FMT, BLOCK>(&pk[g * BLOCK], a.rule, &cout[0][g * WPB], &cout[1][g * WPB],
+                                                          sfA, sfB);
+                            const int64_t kb = kabs / BLOCK + g;
+                            if (cbase < C)
+                                a.col_sf[sf_offset(cbase, kb, kg_col)] = static_cast<uint8_t>(sfA);
+                            if (cbase + 1 < C)
+                                a.col_sf[sf_offset(cbase + 1, kb, kg_col)] = static_cast<uint8_t>(sfB);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
 #pragma unroll
                     for (int g = 0; g < GPB; ++g) {
+                        if (!((scalar >> (j * GPB + g)) & 1u))
+                            continue;
                         float blk[BLOCK];
 #pragma unroll
                         for (int e = 0; e < BLOCK; ++e)
