@@ -11,7 +11,7 @@
 //                      R): a CTA stages SEG x 256 of the input in shared memory
 //                      with 16-byte loads, then each thread encodes one column's
 //                      SEG values into 32 bytes of output codes.
-//   quant_tile_kernel  TMA-pipelined 64 x 256 tiles; rowwise, colwise or both
+//   quant_tile_kernel  TMA-pipelined 64-row tiles; rowwise, colwise or both
 //                      operands from one read of x (the dual-direction pass).
 // Both write the block scales straight into the tensor core's scale-factor
 // layout ("格式感知融合:让FP4预训练提速两倍的工程实践", section
@@ -695,23 +695,40 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
 }
 
 // ------------------------------------------------------------ tile producer
-// Persistent producer over 64 x 256 tiles of x staged in shared memory by TMA
-// through a three-stage mbarrier pipeline.  The eight warps consume the
-// stages without any CTA-wide barrier: each warp counts itself out of a stage
-// when it is done with it, and the last one out refills the stage.  From each
-// staged tile it can emit the rowwise operand (blocks along the 256 columns:
-// a warp encodes two rows per step, 8 elements per lane, block maxima
-// combined with shuffles), the colwise operand (blocks along the 64 rows: a
-// thread encodes one scale block of 4 adjacent columns for 16-row blocks, or
-// of 2 for 32-row blocks, read with 8- or 4-byte shared-memory loads), or both:
-// one read of x then serves the forward operand and the transposed operand a
-// backward pass needs ("格式感知融合:让FP4预训练提速两倍的工程实践", section
+// Persistent producer over 64-row tiles of x (128 or 256 columns, see
+// TileShape) staged in shared memory by TMA through a three-stage mbarrier
+// pipeline.  From each staged tile it emits the rowwise operand (blocks along
+// the columns: a lane encodes one block of one row per step, its 16-byte
+// chunks read in a lane-rotated order that keeps a quarter-warp's loads on
+// distinct banks), the colwise operand (blocks along the 64 rows: a thread
+// encodes two adjacent columns over 32 rows, one or two blocks per column,
+// read as bf16 pairs with conflict-free 4-byte loads), or both: one read of x
+// then serves the forward operand and the transposed operand a backward pass
+// needs ("格式感知融合:让FP4预训练提速两倍的工程实践", section
 // FP4加速为何常常"纸上富贵": operand packing, layout construction and saving
-// backward state are the costs around the GEMM).  Rounding is a compile-time
-// choice per direction and the Hadamard transform is compiled only for the MX
-// formats, so a kernel holds only the code it runs.
-constexpr int kTR = 64, kTC = 256, kTStages = 3;
-constexpr int kTileBytes = kTR * kTC * 2;
+// backward state are the costs around the GEMM).  When the code arrays can be
+// described by tensor maps, the codes are written over the consumed stage
+// (after a CTA barrier) and leave through TMA tensor stores issued by one
+// thread, which also refills the previous tile's stage once its stores have
+// read it; otherwise each thread stores its codes and the last warp out of a
+// stage refills it.  Scale bytes go straight to the consumer layout.
+// Rounding is a compile-time choice per direction and the Hadamard transform
+// is compiled only for the MX formats, so a kernel holds only the code it
+// runs.
+constexpr int kTR = 64, kTStages = 3;
+
+// Tile width, threads and CTAs per SM of one tile-producer instance: 128
+// columns with four CTAs of 128 threads per SM for the round-to-nearest
+// passes (shorter barriers, four independent pipelines per SM), 256 columns
+// with two CTAs of 256 threads for the arithmetic-heavy ones (stochastic
+// rounding, NVFP4_LOCAL's exact divisions), where the per-tile costs weigh
+// more.  One thread per tile column; three stages of kTR x cols bf16.
+template <int FMT, bool ROW_SR, bool COL_SR>
+struct TileShape {
+    static constexpr int cols = (FMT == MX_FMT_NVFP4_LOCAL || ROW_SR || COL_SR) ? 256 : 128;
+    static constexpr int threads = cols, ctas = cols == 128 ? 4 : 2;
+    static constexpr int bytes = kTR * cols * 2;
+};
 
 // NVFP4 block encode under a region's own FP32 scale ts (NVFP4_LOCAL): the
 // NVFP4 steps with exact IEEE quotients (the shared-divisor division), since
@@ -897,17 +914,19 @@ __device__ __forceinline__ void col_encode_packed(const uint32_t* pk, int rule, 
 }
 
 template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileShape<FMT, ROW_SR, COL_SR>::ctas)
     quant_tile_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmrow,
                       const __grid_constant__ CUtensorMap tmcol, const TileArgs a)
 {
+    using TS = TileShape<FMT, ROW_SR, COL_SR>;
+    constexpr int kTC = TS::cols, kTT = TS::threads, kTileBytes = TS::bytes;
     constexpr int BLOCK = fmt_block(FMT);
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     constexpr bool HAD_OK = FMT == MX_FMT_MXFP8_E4M3 || FMT == MX_FMT_MXFP4_E2M1;
     // colwise task: two adjacent columns x 32 rows (one or two scale blocks per column)
     constexpr int CW = 2, CROWS = 32, GPB = CROWS / BLOCK;
     constexpr int kColGroups = kTC / CW;
-    static_assert(kColGroups * (kTR / CROWS) == kThreads, "one colwise task per encoding thread");
+    static_assert(kColGroups * (kTR / CROWS) == kTT, "one colwise task per encoding thread");
     constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // 32-bit code words per scale block
     constexpr int CWW = GPB * WPB;                     // code words per column of a task
     constexpr int CBB = CROWS * (FP4 ? 1 : 2) / 2;     // code bytes per column of a task
@@ -924,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     constexpr int CH = BLOCK / 8;             // 8-element chunks per block
     constexpr int BPR = kTC / BLOCK;          // blocks per tile row
     constexpr int RPS = 32 / BPR;             // tile rows per warp step
-    constexpr int STEPS = kTR / (RPS * (kThreads / 32));
+    constexpr int STEPS = kTR / (RPS * (kTT / 32));
     constexpr int CB = FP4 ? 4 : 8;           // code bytes per chunk
     extern __shared__ uint8_t smem_raw[];
     // 128-byte aligned stage base, by pointer arithmetic on the shared array so
@@ -961,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
         for (int st = 0; st < kTStages; ++st) {
             mbar_init(full0 + 8u * st, 1);
-            mbar_init(staged0 + 8u * st, kThreads / 32);
+            mbar_init(staged0 + 8u * st, kTT / 32);
             stage_out[st] = 0;
         }
         fence_mbar_init();
@@ -1016,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int64_t sf_in_row = (kb >> 2) * 512 + (kb & 3);
 #pragma unroll
             for (int s2 = 0; s2 < STEPS; ++s2) {
-                const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
+                const int rr = (s2 * (kTT / 32) + warp) * RPS + lane / BPR;
                 const int64_t row = r0 + rr;
                 const uint16_t* src = tile + rr * kTC + kbl * BLOCK;
                 uint32_t* out = rout[s2];
@@ -1164,15 +1183,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             // The codes of the tile go out through TMA tensor stores from the
             // stage the tile came in on: once every thread is done reading it
             // (a barrier of the CTA), the codes are written over it (rowwise
-            // [64 rows][row bytes], then colwise [32-row half][256 columns]
+            // [64 rows][row bytes], then colwise [32-row half][tile columns]
             // [column bytes]) and each warp signals the stage's "staged"
             // barrier; thread 0 waits for it, stores, and refills the stage of
             // the previous tile, whose stores have had a tile's time to read it.
-            named_barrier_sync(1, kThreads);
+            named_barrier_sync(1, kTT);
             if constexpr (DO_ROW) {
 #pragma unroll
                 for (int s2 = 0; s2 < STEPS; ++s2) {
-                    const int rr = (s2 * (kThreads / 32) + warp) * RPS + lane / BPR;
+                    const int rr = (s2 * (kTT / 32) + warp) * RPS + lane / BPR;
                     uint8_t* dst = stage + rr * RB_T + kbl * BLOCK * (FP4 ? 1 : 2) / 2;
 #pragma unroll
                     for (int c = 0; c < CH; ++c) {
@@ -1225,7 +1244,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();  // every lane of this warp is done reading the stage
             if (lane == 0) {
                 __threadfence_block();  // release this warp's reads before counting out
-                if (atomicAdd(&stage_out[st], 1) == kThreads / 32 - 1) {  // last warp out refills
+                if (atomicAdd(&stage_out[st], 1) == kTT / 32 - 1) {  // last warp out refills
                     __threadfence_block();
                     stage_out[st] = 0;
                     if (i + kTStages < my_n) {
@@ -1422,7 +1441,9 @@ template <int FMT, bool DO_ROW, bool DO_COL, bool ROW_SR, bool COL_SR>
 int launch_tile(const TileArgs& t_in, int64_t ld, const Device& d, cudaStream_t s)
 {
     auto kernel = quant_tile_kernel<FMT, DO_ROW, DO_COL, ROW_SR, COL_SR>;
-    constexpr int smem = kTStages * kTileBytes + kTStages * 8 + 128;
+    using TS = TileShape<FMT, ROW_SR, COL_SR>;
+    constexpr int kTC = TS::cols;
+    constexpr int smem = kTStages * TS::bytes + 2 * kTStages * 8 + 128;
     constexpr bool FP4 = elem_of(FMT) == kElemE2M1;
     static int configured_device = -1;
     if (configured_device != d.id) {
@@ -1455,8 +1476,8 @@ int launch_tile(const TileArgs& t_in, int64_t ld, const Device& d, cudaStream_t 
         ok = ok && make_code_store_map(&mcol, t.col_codes, t.C, col_bytes, FP4 ? 16 : 32, kTC);
     t.tma_st = ok ? 1 : 0;
     const int64_t tiles = ((t.R + kTR - 1) / kTR) * ((t.C + kTC - 1) / kTC);
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(d.sms) * 2));
-    kernel<<<grid, kThreads, smem, s>>>(m, mrow, mcol, t);
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, static_cast<int64_t>(d.sms) * TS::ctas));
+    kernel<<<grid, TS::threads, smem, s>>>(m, mrow, mcol, t);
     count_launch();
     return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }

@@ -6,7 +6,7 @@ import torch
 
 import oracle as orc
 import workloads
-from parity import assert_quant_equal, bits
+from parity import assert_quant_equal, bits, sf_valid_mask
 
 pytestmark = pytest.mark.gpu
 
@@ -180,6 +180,35 @@ def test_dual_producer_matches_two_single_passes(mx, fmt, shape):
     torch.cuda.synchronize()
     assert_quant_equal(qr, orc.quantize(bits(x), fmt, "row"), f"dual row {fmt} {shape}")
     assert_quant_equal(qc, orc.quantize(bits(x), fmt, "col"), f"dual col {fmt} {shape}")
+
+
+@pytest.mark.parametrize("fmt", FMTS + ["nvfp4_local"])
+@pytest.mark.parametrize("shape", [(416, 544), (96, 288)])
+def test_scale_padding_is_left_unwritten(mx, fmt, shape):
+    """Ragged tiles (rows past R, columns and K-blocks past C) write only the
+    real positions of the scale-factor layout: a sentinel in every padding
+    byte survives both producers and the dual pass."""
+    x = workloads.draw("student_t3", shape, 77).cuda()
+    R, Cc = shape
+    pairs = []
+    qr, qc = mx.MXTensor(fmt, R, Cc), mx.MXTensor(fmt, Cc, R)
+    for q in (qr, qc):
+        q.sf.fill_(0xA5)
+    mx.quantize_dual(x, fmt, row_out=qr, col_out=qc)
+    pairs += [(qr, "dual row"), (qc, "dual col")]
+    for d in ("row", "col"):
+        q = mx.MXTensor(fmt, *((R, Cc) if d == "row" else (Cc, R)))
+        q.sf.fill_(0xA5)
+        mx.quantize(x, fmt, d, out=q)
+        pairs.append((q, d))
+    torch.cuda.synchronize()
+    for q, what in pairs:
+        mask = sf_valid_mask(q.rows, q.k // q.block)
+        got = q.sf.cpu().numpy()
+        real = np.zeros(got.size, dtype=bool)
+        real[:mask.size] = mask
+        assert (got[~real] == 0xA5).all(), f"{fmt} {shape} {what}: padding bytes written"
+        assert (got[real] != 0xA5).any()
 
 
 @pytest.mark.parametrize("fmt", ["mxfp4", "mxfp8", "nvfp4"])
