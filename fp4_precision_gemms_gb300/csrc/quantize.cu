@@ -209,7 +209,9 @@ __device__ __forceinline__ float tensor_scale_of(int fmt, const float* amax)
 // with a 2^-44 margin (bf16 values are 2^-8 apart, so a random D fails with
 // probability near 2^-30).  D must lie in
 // [2^-100, 2^100], so that x near a boundary is a normal bf16 value and x * lo
-// does not underflow there; callers guard the overflow side per block.
+// does not underflow there; callers guard the overflow side per block.  The
+// argument needs x on the bf16 lattice: fp32 values (Hadamard-transformed
+// blocks) could sit within 2^-46 of a midpoint, so those divide exactly.
 struct Recip2 {
     float hi, lo;
 };
@@ -340,18 +342,23 @@ __device__ __forceinline__ float moss_block(float (&v)[N], float xmax, const Sca
 
 // NVFP4 block scale byte: UE4M3_RNE(fl32(bmax / fl32(6 s_t))).  A quotient of
 // 2^100 or more saturates either way (clamping also absorbs an overflowed
-// product).
+// product).  The certified product holds for bmax a bf16 value; the maxima of
+// Hadamard-transformed blocks (BF16_IN false) are fp32 and divide exactly.
+template <bool BF16_IN = true>
 __device__ __forceinline__ uint32_t nvfp4_scale_byte(float bmax, const ScaleCtx& sc)
 {
-    const float qb = sc.den2_ok ? fminf(quot2(bmax, sc.den2), 0x1p100f) : div_shared(bmax, sc.nv_denom, sc.rden);
+    const float qb = (BF16_IN && sc.den2_ok) ? fminf(quot2(bmax, sc.den2), 0x1p100f)
+                                             : div_shared(bmax, sc.nv_denom, sc.rden);
     return cvt_e4m3x2(qb, 0.0f) & 0x7Fu;
 }
 
 // Encodes one scale block held as N consecutive values in registers (the
 // block's max |v| is `bmax`).  Produces the scale byte and N codes packed
 // little-endian into `out` (E4M3: N bytes; E2M1: N/2 bytes).  `L8` is the
-// Philox counter of the first 8 elements (used only for SR).
-template <int FMT, bool SR, int N>
+// Philox counter of the first 8 elements (used only for SR).  The certified
+// NVFP4 products hold for bf16 values; BF16_IN false (Hadamard-transformed
+// fp32 values) takes the exact division.
+template <int FMT, bool SR, int N, bool BF16_IN = true>
 __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, const ScaleCtx& sc, int rule,
                                                  uint64_t seed, uint32_t sid, uint64_t L8, uint32_t* out)
 {
@@ -359,13 +366,13 @@ __device__ __forceinline__ uint32_t encode_block(float (&v)[N], float bmax, cons
     uint32_t sfbyte;
     bool zero = false;
     if constexpr (FMT == MX_FMT_NVFP4) {
-        const uint32_t sb = nvfp4_scale_byte(bmax, sc);
+        const uint32_t sb = nvfp4_scale_byte<BF16_IN>(bmax, sc);
         const float2 drd = sc.nv_tab[sb];  // {fl32(dec(sb) * ts), RN(1/d)}
         const float2 q2 = sc.nv_q[sb];     // certified {hi, lo}, or hi < 0
         sfbyte = sb;
         if (drd.x == 0.0f) {
             zero = true;
-        } else if (!SR && q2.x > 0.0f && __fmul_rn(bmax, q2.x) < 0x1p100f) {  // certified
+        } else if (!SR && BF16_IN && q2.x > 0.0f && __fmul_rn(bmax, q2.x) < 0x1p100f) {  // certified
             const Recip2 r{q2.x, q2.y};
 #pragma unroll
             for (int i = 0; i < N; ++i)
@@ -592,8 +599,8 @@ __global__ void __launch_bounds__(kThreads) quant_row_kernel(QuantArgs a)
                 bmax = moss_block(v, bmax, sc);
             if (c8 < cpr) {
                 uint32_t out[2];
-                const uint32_t sfb = encode_block<FMT, SR, 8>(v, bmax, sc, a.rule, a.seed,
-                                                              a.stream_id, r * cpr + c8, out);
+                const uint32_t sfb = encode_block<FMT, SR, 8, !HAD>(v, bmax, sc, a.rule, a.seed,
+                                                                    a.stream_id, r * cpr + c8, out);
                 if constexpr (FP4)
                     *reinterpret_cast<uint32_t*>(a.codes + r * (C / 2) + c8 * 4) = out[0];
                 else
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kThreads) quant_col_kernel(QuantArgs a)
                     bmax = moss_block(blk, bmax, sc);
                 constexpr int WPB = FP4 ? BLOCK / 8 : BLOCK / 4;  // output words per block
                 const uint64_t L8 = static_cast<uint64_t>(c) * (R / 8) + (k0 + b * BLOCK) / 8;
-                const uint32_t sfb = encode_block<FMT, SR, BLOCK>(blk, bmax, sc, a.rule, a.seed,
+                const uint32_t sfb = encode_block<FMT, SR, BLOCK, !HAD>(blk, bmax, sc, a.rule, a.seed,
                                                                   a.stream_id, L8, out + b * WPB);
                 if (b * BLOCK < nk)
                     a.sf[sf_offset(c, (k0 + b * BLOCK) / BLOCK, kgroups)] = static_cast<uint8_t>(sfb);
