@@ -1018,14 +1018,24 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                 atomicExch(a.status, MX_ERR_TIMEOUT);
             timed_out = true;
         }
-        // the staged path synchronises the CTA below, so every thread leaves together
-        if (tma_st ? __syncthreads_or(timed_out) : timed_out)
+        // The staged path votes on timeouts at its CTA barrier below, so that
+        // every thread leaves together (a thread that gave up encodes whatever
+        // the stage holds: in-bounds stores of values the error status voids).
+        if (!tma_st && timed_out)
             break;
         uint8_t* stage = base + st * kTileBytes;
         const uint16_t* tile = reinterpret_cast<const uint16_t*>(stage);  // [kTR][kTC]
         const int64_t t = blockIdx.x + i * gridDim.x;
         const int64_t rt = t / ctiles, ct = t - rt * ctiles;
         const int64_t r0 = rt * kTR, c0 = ct * kTC;
+        // Scale-byte positions: a 64-bit base per tile (its 512-byte chunks)
+        // plus small offsets.  Tiles start on 64 rows and 128 columns, so a
+        // tile's K-blocks never cross a group of four and its rows stay in one
+        // 128-row chunk.
+        const int64_t kb_r0 = c0 / BLOCK, kb_c0 = r0 / BLOCK;  // first K-block: rowwise, colwise
+        uint8_t* const row_sf_tile = DO_ROW ? a.row_sf + ((r0 >> 7) * kg_row + (kb_r0 >> 2)) * 512 : nullptr;
+        uint8_t* const col_sf_tile = DO_COL ? a.col_sf + ((c0 >> 7) * kg_col + (kb_c0 >> 2)) * 512 + (kb_c0 & 3) : nullptr;
+        const int row_q0 = static_cast<int>((r0 >> 5) & 3);  // 32-row quarter of the tile's first row
 
         // Rowwise: lane = one scale block of one tile row, read as CH 16-byte
         // chunks.  Plain round-to-nearest passes take the chunks in a
@@ -1038,8 +1048,7 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
         uint32_t rout[DO_ROW ? STEPS : 1][FP4 ? BLOCK / 8 : BLOCK / 4];
         if constexpr (DO_ROW) {
             const int64_t col = c0 + kbl * BLOCK;
-            const int64_t kb = col / BLOCK;
-            const int64_t sf_in_row = (kb >> 2) * 512 + (kb & 3);
+            const int sf_in_row = (kbl >> 2) * 512 + (kbl & 3);
 #pragma unroll
             for (int s2 = 0; s2 < STEPS; ++s2) {
                 const int rr = (s2 * (kTT / 32) + warp) * RPS + lane / BPR;
@@ -1100,8 +1109,7 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                                 *reinterpret_cast<uint2*>(dst + cc * CB) = make_uint2(out[2 * c], out[2 * c + 1]);
                         }
                     }
-                    const int64_t sf_row = ((row >> 7) * kg_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
-                    a.row_sf[sf_row + sf_in_row] = static_cast<uint8_t>(sfb);
+                    row_sf_tile[sf_in_row + (rr & 31) * 16 + (row_q0 + (rr >> 5)) * 4] = static_cast<uint8_t>(sfb);
                 }
             }
         }
@@ -1111,6 +1119,10 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
         // of that row: no bank conflicts); each column's 32 values are one MX
         // block or two NVFP4 blocks, encoded in registers.
         const int64_t kabs = r0 + rh * CROWS;  // first row (K) of this task
+        // scale byte of tile column ml, tile K-block lk
+        auto col_sf_at = [&](int ml, int lk) {
+            return col_sf_tile + ((ml >> 7) ? kg_col * 512 : 0) + ((ml & 31) * 16 + ((ml >> 5) & 3) * 4 + lk);
+        };
         uint32_t cout[DO_COL ? CW : 1][CWW];
         if constexpr (DO_COL) {
             if (kabs < R) {  // R % 32 == 0: a task's rows are wholly in or out
@@ -1129,11 +1141,10 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                             uint32_t sfA, sfB;
                             col_encode_packed<FMT, BLOCK>(&pk[g * BLOCK], a.rule, &cout[0][g * WPB], &cout[1][g * WPB],
                                                           sfA, sfB);
-                            const int64_t kb = kabs / BLOCK + g;
                             if (cbase < C)
-                                a.col_sf[sf_offset(cbase, kb, kg_col)] = static_cast<uint8_t>(sfA);
+                                *col_sf_at(cg * CW, rh * GPB + g) = static_cast<uint8_t>(sfA);
                             if (cbase + 1 < C)
-                                a.col_sf[sf_offset(cbase + 1, kb, kg_col)] = static_cast<uint8_t>(sfB);
+                                *col_sf_at(cg * CW + 1, rh * GPB + g) = static_cast<uint8_t>(sfB);
                         }
                     }
                 }
@@ -1173,7 +1184,7 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                             sfb = encode_block<FMT, COL_SR, BLOCK>(blk, bmax, sc, a.rule, a.seed, a.stream_id, L8, out);
                         }
                         if (cbase + j < C)
-                            a.col_sf[sf_offset(cbase + j, kblk / BLOCK, kg_col)] = static_cast<uint8_t>(sfb);
+                            *col_sf_at(cg * CW + j, rh * GPB + g) = static_cast<uint8_t>(sfb);
                     }
                     if (!tma_st && cbase + j < C) {
                         uint8_t* dst = a.col_codes + (cbase + j) * col_row_bytes + (FP4 ? kabs / 2 : kabs);
@@ -1194,7 +1205,8 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
             // [column bytes]) and each warp signals the stage's "staged"
             // barrier; thread 0 waits for it, stores, and refills the stage of
             // the previous tile, whose stores have had a tile's time to read it.
-            named_barrier_sync(1, kTT);
+            if (named_barrier_or(1, kTT, timed_out))  // every thread is done reading the stage
+                break;
             if constexpr (DO_ROW) {
 #pragma unroll
                 for (int s2 = 0; s2 < STEPS; ++s2) {
