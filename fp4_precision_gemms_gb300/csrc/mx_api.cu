@@ -108,6 +108,7 @@ size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
 // rowwise, tile producer colwise), 1 direct loads, 2 tile producer.  Per host
 // thread, like the GEMM variant override.
 thread_local int g_quant_impl = 0;
+thread_local int64_t g_tile_fail_at = -1;  // test hook: tile producer's forced wait failure
 
 // Shared argument checks of the single and dual producers.
 int check_quantize_args(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int rule)
@@ -249,6 +250,7 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         }
         t.status = d.status;
         t.wait_ns = kWaitLimitNs;
+        t.fail_at = g_tile_fail_at;
         return launch_quantize_tile(t, ld, d, s);
     }
     QuantArgs q;
@@ -355,6 +357,7 @@ int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt,
     t.col_had = col_hadamard ? 1 : 0;
     t.status = d.status;
     t.wait_ns = kWaitLimitNs;
+    t.fail_at = g_tile_fail_at;
     return launch_quantize_tile(t, ld, d, s);
 }
 
@@ -790,6 +793,8 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
 
 // Test hook: producer implementation (0 automatic, 1 direct loads, 2 tile producer).
 void mx_debug_set_quant_impl(int impl) { g_quant_impl = (impl >= 0 && impl <= 2) ? impl : 0; }
+
+void mx_debug_set_tile_fail_at(int64_t tile) { g_tile_fail_at = tile >= 0 ? tile : -1; }
 
 // Test hook: force one GEMM kernel variant (0 = automatic).
 void mx_debug_set_gemm_variant(int variant) { set_gemm_variant(variant); }

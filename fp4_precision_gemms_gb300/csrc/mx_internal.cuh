@@ -82,6 +82,9 @@ struct TileArgs {
     const float* col_ts_v;
     // set by the launcher: 1 when the codes leave through TMA tensor stores
     int tma_st;
+    // test hook: on this tile (of each CTA) the CTA's last thread gives up its
+    // stage wait as if its limit had run out; -1 never
+    int64_t fail_at;
 };
 
 // Number of kernels this library has launched in the process.

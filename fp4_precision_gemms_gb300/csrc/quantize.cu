@@ -1013,9 +1013,9 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
     bool timed_out = false;
     for (int64_t i = 0; i < my_n; ++i) {
         const int st = static_cast<int>(i % kTStages);
-        if (!mbar_wait_bounded(full0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns)) {
-            if (lane == 0)
-                atomicExch(a.status, MX_ERR_TIMEOUT);
+        if (!mbar_wait_bounded(full0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns) ||
+            (i == a.fail_at && tid == kTT - 1)) {
+            atomicExch(a.status, MX_ERR_TIMEOUT);
             timed_out = true;
         }
         // The staged path votes on timeouts at its CTA barrier below, so that
@@ -1238,7 +1238,7 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                 mbar_arrive(staged0 + 8u * st);
             if (tid == 0) {
                 if (!mbar_wait_bounded(staged0 + 8u * st, static_cast<uint32_t>(i / kTStages) & 1u, a.wait_ns)) {
-                    atomicExch(a.status, MX_ERR_TIMEOUT);  // the other warps stop at the next tile's check
+                    atomicExch(a.status, MX_ERR_TIMEOUT);  // the CTA stops at the next tile's barrier vote
                     timed_out = true;
                 } else {
                     const uint32_t s = sbase + st * kTileBytes;

@@ -340,6 +340,15 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
  * for both directions.  Outputs are identical; only the speed differs. */
 void mx_debug_set_quant_impl(int impl);
 
+/* Test hook for the tile producer's bounded waits: for later quantize calls
+ * made by the calling host thread, the last thread of every producer CTA
+ * treats its wait for that CTA's tile number `tile` (0-based, in the CTA's own
+ * order) as timed out.  The pass then stops, waits for its own copies in
+ * flight and reports MX_ERR_TIMEOUT through the status word
+ * (mx_last_device_status); outputs of such a pass are unspecified.  -1 (the
+ * initial value) turns it off.  Nothing faults or hangs. */
+void mx_debug_set_tile_fail_at(int64_t tile);
+
 /* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
  * calls made by the calling host thread (other threads keep their own choice,
  * initially 0): 0 automatic, 1 single-CTA 128 x 128 tiles, 2 single-CTA

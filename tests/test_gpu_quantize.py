@@ -168,6 +168,32 @@ def test_bounded_wait_gives_up_and_reports(mx):
     assert_quant_equal(q, ref, "after timeout")
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_tile_producer_wait_gives_up_and_reports(mx, request, fmt):
+    """A stage wait of the tile producer that runs out (forced by the test hook
+    on one thread of every CTA, at its third tile) ends the pass with
+    MX_ERR_TIMEOUT in the status word, with no fault and no hang: the CTA
+    leaves together after its barrier vote, once its copies have landed.  The
+    next pass is exact."""
+    if request.node.callspec.params.get("mx") == "direct":
+        pytest.skip("the direct producers have no stage waits")
+    x = workloads.draw("normal", (4096, 4096), 5).cuda()
+    assert mx.last_device_status() == mx.MX_OK
+    mx.set_tile_fail_at(2)
+    try:
+        mx.quantize_dual(x, fmt)
+        torch.cuda.synchronize()
+    finally:
+        mx.set_tile_fail_at(-1)
+    assert mx.last_device_status() == mx.MX_ERR_TIMEOUT
+    assert mx.last_device_status() == mx.MX_OK
+    xs = workloads.draw("student_t3", (256, 512), 6)
+    qr, qc = mx.quantize_dual(xs.cuda(), fmt)
+    torch.cuda.synchronize()
+    assert_quant_equal(qr, orc.quantize(bits(xs), fmt, "row"), f"{fmt} row after a forced timeout")
+    assert_quant_equal(qc, orc.quantize(bits(xs), fmt, "col"), f"{fmt} col after a forced timeout")
+
+
 # ------------------------------------------------------------ dual producer
 DUAL_SHAPES = [(416, 544), (256, 4096), (4096, 96), (96, 288)]
 
