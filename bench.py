@@ -619,7 +619,7 @@ def run_case(args):
     step), gemm:<fmt>:MxNxK, gemmq:<fmt>:<out fmt>:MxNxK (quantized epilogue) or
     quant:<fmt>:<row|col|dual>[+had][+sr]:RxC (bf16 Student-t inputs; +had
     applies Hadamard-32, +sr stochastic rounding with seed 42, to the colwise
-    operand of a dual call)."""
+    operand of a dual call) or amax:RxC (the tensor-amax pass)."""
     import fp4_precision_gemms_gb300 as mx
     mx.build()
     mx.set_gemm_variant(args.gemm_variant)
@@ -656,6 +656,12 @@ def run_case(args):
         q = mx.MXTensor(ofmt, M, N, dev)
         fn = lambda: mx.gemm_quantized(a, b, ofmt, out=q)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif parts[0] == "amax":  # the tensor-amax pass alone: amax:RxC
+        R, Cc = (int(v) for v in parts[1].split("x"))
+        x = workloads.draw("student_t3", (R, Cc), 1, device=dev)
+        am = torch.empty(1, dtype=torch.float32, device=dev)
+        fn = lambda: mx.amax(x, out=am)  # noqa: E731
+        work, unit = 2.0 * R * Cc, "GB/s"
     else:  # direction row, col or dual, optionally +had (Hadamard-32) and +sr (stochastic rounding)
         fmt, dopts = parts[1], parts[2].split("+")
         direction = dopts[0]

@@ -219,11 +219,13 @@ int quantize_impl(const void* x, int64_t R, int64_t C, int64_t ld, int dir, int 
         return rc;
     if (R == 0 || C == 0)
         return (ts && !fmt_is_local(fmt)) ? set_unit_scale(out, s) : MX_OK;
-    // the direct producers have no region scales: NVFP4_LOCAL always takes the tile
+    // The tile producer is the automatic choice in both directions (measured
+    // faster than the direct producers for rowwise passes as well).  The direct
+    // producers have no region scales: NVFP4_LOCAL always takes the tile
     // producer; the tile producer has no NVFP4 transform: NVFP4 with the
-    // Hadamard transform always takes the direct producers
+    // Hadamard transform always takes the direct producers.
     const bool nv_had = fmt == MX_FMT_NVFP4 && hadamard;
-    const bool tile = (g_quant_impl == 2 || (g_quant_impl == 0 && dir == MX_COLWISE) || fmt_is_local(fmt)) && !nv_had;
+    const bool tile = (g_quant_impl != 1 || fmt_is_local(fmt)) && !nv_had;
     if (tile) {
         TileArgs t = {};
         t.x = x;

@@ -336,7 +336,8 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
 
 /* Test hook: choose the producer implementation for later calls made by the
  * calling host thread (other threads keep their own choice, initially 0):
- * 0 automatic, 1 direct-load row/col kernels, 2 the shared-memory tile producer
+ * 0 automatic (the tile producer, except for NVFP4 with the Hadamard
+ * transform), 1 direct-load row/col kernels, 2 the shared-memory tile producer
  * for both directions.  Outputs are identical; only the speed differs. */
 void mx_debug_set_quant_impl(int impl);
 
