@@ -1071,17 +1071,26 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                 }
                 if (scalar) {
                     float v[BLOCK];
+                    uint32_t w[BLOCK / 2];
 #pragma unroll
-                    for (int c = 0; c < CH; ++c)
-                        unpack8(*reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8), v + 8 * c);
-                    if constexpr (HAD_OK) {
-                        if (row_had)
-                            fwht_local<BLOCK>(v);
+                    for (int c = 0; c < CH; ++c) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(src + ((c + rot) & (CH - 1)) * 8);
+                        w[4 * c] = q.x, w[4 * c + 1] = q.y, w[4 * c + 2] = q.z, w[4 * c + 3] = q.w;
+                        unpack8(q, v + 8 * c);
                     }
                     float bmax = 0.0f;
+                    if constexpr (FMT == MX_FMT_NVFP4) {  // from the bf16 words, two at a time (measured faster for NVFP4 only)
+                        const uint32_t mw = absmax_words<BLOCK / 2>(w);
+                        bmax = fmaxf(bf16_lo(mw), bf16_hi(mw));
+                    } else {
+                        if constexpr (HAD_OK) {
+                            if (row_had)
+                                fwht_local<BLOCK>(v);
+                        }
 #pragma unroll
-                    for (int e = 0; e < BLOCK; ++e)
-                        bmax = fmaxf(bmax, fabsf(v[e]));
+                        for (int e = 0; e < BLOCK; ++e)
+                            bmax = fmaxf(bmax, fabsf(v[e]));
+                    }
                     if constexpr (FMT == MX_FMT_MOSS_FP8)
                         bmax = moss_block(v, bmax, sc);
                     const uint64_t L8 = static_cast<uint64_t>(row) * (C / 8) + col / 8;
@@ -1148,6 +1157,11 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
                         }
                     }
                 }
+                // NVFP4: block maxima of both columns from the bf16 words, two at a time
+                uint32_t mwg[GPB];
+#pragma unroll
+                for (int g = 0; g < GPB; ++g)
+                    mwg[g] = FMT == MX_FMT_NVFP4 ? absmax_words<BLOCK>(&pk[g * BLOCK]) : 0u;
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
 #pragma unroll
@@ -1158,14 +1172,16 @@ __global__ void __launch_bounds__(TileShape<FMT, ROW_SR, COL_SR>::threads, TileS
 #pragma unroll
                         for (int e = 0; e < BLOCK; ++e)
                             blk[e] = j ? bf16_hi(pk[g * BLOCK + e]) : bf16_lo(pk[g * BLOCK + e]);
-                        if constexpr (HAD_OK) {
-                            if (col_had)
-                                fwht_local<BLOCK>(blk);
-                        }
-                        float bmax = 0.0f;
+                        float bmax = j ? bf16_hi(mwg[g]) : bf16_lo(mwg[g]);
+                        if constexpr (FMT != MX_FMT_NVFP4) {
+                            if constexpr (HAD_OK) {
+                                if (col_had)
+                                    fwht_local<BLOCK>(blk);
+                            }
 #pragma unroll
-                        for (int e = 0; e < BLOCK; ++e)
-                            bmax = fmaxf(bmax, fabsf(blk[e]));
+                            for (int e = 0; e < BLOCK; ++e)
+                                bmax = fmaxf(bmax, fabsf(blk[e]));
+                        }
                         if constexpr (FMT == MX_FMT_MOSS_FP8)
                             bmax = moss_block(blk, bmax, sc);
                         const int64_t kblk = kabs + g * BLOCK;
