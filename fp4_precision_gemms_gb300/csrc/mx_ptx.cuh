@@ -132,8 +132,6 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the source buffers of all committed bulk stores may be reused
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// the source buffers of all but the most recent committed bulk store group may be reused
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // all committed bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -428,19 +426,6 @@ __device__ __forceinline__ void mma_bs_pair(uint32_t d_tmem, uint64_t adesc, uin
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Named barrier that also ORs a predicate over its nthreads threads.
-__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
 }
 
 }  // namespace mx
