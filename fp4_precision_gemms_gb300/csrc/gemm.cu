@@ -23,6 +23,7 @@
 // records MX_ERR_TIMEOUT, stops issuing, drains what is in flight and frees
 // TMEM before the CTA exits.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 
 #include <cuda.h>
@@ -385,19 +386,27 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_b
 }
 
 // Tile raster: the group size in M-tiles of the grouped order (tiles walk M
-// within a group, then N).  When all of B fits comfortably in L2 (129 MB),
-// N-fastest order (groups of one M-tile) keeps B resident and streams A
-// once; when A fits, one group of all M-tiles keeps A resident and streams B
-// once; otherwise a group holds about 16 MiB of A row tiles.
-int raster_group_m(int64_t M, int64_t N, int64_t kbytes, int bm, int m_tiles)
+// within a group, then N).  `wave` tiles run at once, and what a wave reads
+// should stay in L2 (129 MB, of which 96 MB is budgeted for operand tiles).
+// When all of one operand plus the other operand's tiles one wave touches fit
+// the budget, that operand stays resident and the other streams once: B with
+// N-fastest order (groups of one M-tile), A with one group of all M-tiles
+// (the smaller resident set when both fit).  Otherwise a wave of groups of g
+// M-tiles touches g A tiles and wave / g B tiles, and g near
+// sqrt(wave * b_tile / a_tile) makes that set smallest.
+int raster_group_m(int64_t M, int64_t N, int64_t kbytes, int bm, int bn, int m_tiles, int n_tiles, int wave)
 {
-    constexpr int64_t kResident = int64_t(48) << 20;
-    if (N * kbytes <= kResident)
+    constexpr int64_t kBudget = int64_t(96) << 20;
+    const int64_t a_tile = static_cast<int64_t>(bm) * kbytes, b_tile = static_cast<int64_t>(bn) * kbytes;
+    const int64_t b_resident = N * kbytes + (wave + n_tiles - 1) / n_tiles * a_tile;
+    const int64_t a_resident = M * kbytes + (wave + m_tiles - 1) / m_tiles * b_tile;
+    const bool b_fits = b_resident <= kBudget, a_fits = a_resident <= kBudget;
+    if (b_fits && (!a_fits || N <= M))
         return 1;
-    if (M * kbytes <= kResident)
+    if (a_fits)
         return m_tiles;
-    const int64_t a_tile_bytes = static_cast<int64_t>(bm) * kbytes;
-    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(m_tiles, (int64_t(16) << 20) / a_tile_bytes)));
+    const double g = std::sqrt(static_cast<double>(wave) * static_cast<double>(b_tile) / static_cast<double>(a_tile));
+    return std::max(1, std::min(m_tiles, static_cast<int>(g + 0.5)));
 }
 
 template <int KIND, int BN, int STAGES>
@@ -437,7 +446,7 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.wait_ns = kWaitLimitNs;
     p.m_tiles = static_cast<int>((M + G::BM - 1) / G::BM);
     p.n_tiles = static_cast<int>((N + BN - 1) / BN);
-    p.group_m = raster_group_m(M, N, kbytes, G::BM, p.m_tiles);
+    p.group_m = raster_group_m(M, N, kbytes, G::BM, BN, p.m_tiles, p.n_tiles, d.sms);
     const dim3 grid(static_cast<unsigned>(p.m_tiles) * static_cast<unsigned>(p.n_tiles));
     bs_gemm_kernel<KIND, BN, STAGES><<<grid, 192, G::SMEM_ALLOC, s>>>(ta, tb, p);
     count_launch();
@@ -1062,7 +1071,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.m_tiles = static_cast<int>((M + 255) / 256);
     p.n_tiles = static_cast<int>((N + 255) / 256);
-    p.group_m = raster_group_m(M, N, kbytes, 256, p.m_tiles);
+    p.group_m = raster_group_m(M, N, kbytes, 256, 256, p.m_tiles, p.n_tiles, max_clusters);
     p.status = d.status;
     p.wait_ns = kWaitLimitNs;
     const int tiles = p.m_tiles * p.n_tiles;
@@ -1572,7 +1581,7 @@ int launch_ws(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int6
     p.kgroups = sf_kgroups(K / G::BLOCK);
     p.m_tiles = static_cast<int>((M + 255) / 256);
     p.n_tiles = static_cast<int>((N + 255) / 256);
-    p.group_m = raster_group_m(M, N, kbytes, 256, p.m_tiles);
+    p.group_m = raster_group_m(M, N, kbytes, 256, 256, p.m_tiles, p.n_tiles, max_clusters);
     p.status = d.status;
     p.wait_ns = kWaitLimitNs;
     const int tiles = p.m_tiles * p.n_tiles;
