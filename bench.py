@@ -381,6 +381,34 @@ def time_calls(calls, steps, warmup, stream, clk=None, count=None):
     return t0.elapsed_time(t1) / steps, per, counted
 
 
+def graph_time(calls, steps, warmup, stream, clk=None, count=None):
+    """One step captured as a CUDA graph (every call launches on the capture
+    stream; operands and outputs are preallocated, so the graph replays the
+    same work), then `warmup` untimed and `steps` timed replays with CUDA
+    events on `stream`.  Returns (ms per step, library launches per step)."""
+    g = torch.cuda.CUDAGraph()
+    c0 = count() if count else None
+    with torch.cuda.graph(g):
+        for c in calls:
+            c[2]()
+    per_step = count() - c0 if count else None
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clk is not None:
+        clk.start_window()
+    t0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.end_window()
+    del g
+    return t0.elapsed_time(t1) / steps, per_step
+
+
 def run_ours(args, world, rank, local):
     import fp4_precision_gemms_gb300 as mx
     device = torch.device("cuda", local)
@@ -406,11 +434,21 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         assert mx.last_device_status() == mx.MX_OK
         barrier(world)
-        ms, per, launches = time_calls(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count)
+        # per-class CUDA-event times of the step launched call by call (the roofline
+        # and the class fractions), then the step itself as one CUDA graph
+        ms_eager, per, launches = time_calls(calls, args.steps, args.warmup, stream,
+                                             None if args.graph else clk, count=mx.launch_count)
+        ms = ms_eager
+        if args.graph:
+            torch.cuda.synchronize()
+            barrier(world)
+            ms, per_step = graph_time(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count)
+            launches = per_step * args.steps
     barrier(world)
     status = mx.last_device_status()
     ms = reduce_max(ms, world)
-    result = dict(ms=ms, gemm_flops=gemm_flops, per=per, launches=launches, clocks=clk.summary(),
+    ms_eager = reduce_max(ms_eager, world)
+    result = dict(ms=ms, ms_eager=ms_eager, gemm_flops=gemm_flops, per=per, launches=launches, clocks=clk.summary(),
                   gemm_kernels=gemm_kernels, status=status, calls_per_step=len(calls))
     if not args.no_side:
         result["side"] = run_side_workloads(mx, device, stream, args)
@@ -434,7 +472,10 @@ def run_side_workloads(mx, device, stream, args):
             calls += [(fmt,) + c for c in Plan(mx, wl, fmt, device, wgrad=wg).calls(inputs)]
         flops = sum(c[3] for c in calls if c[1] == "gemm")
         ms, per, _ = time_calls(calls, args.side_steps, args.warmup, stream)
-        out[wl.name] = dict(ms=ms, gemm_flops=flops, per=per, wgrad=wg, index=idx)
+        ms_eager = ms
+        if args.graph:
+            ms, _ = graph_time(calls, args.side_steps, args.warmup, stream)
+        out[wl.name] = dict(ms=ms, ms_eager=ms_eager, gemm_flops=flops, per=per, wgrad=wg, index=idx)
         del inputs
     torch.cuda.synchronize()
     return out
@@ -718,6 +759,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time the step launched call by call instead of as one CUDA graph")
     ap.add_argument("--no-side", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--side-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -774,12 +817,17 @@ def main():
                                    definition="(sum of quantize bytes / HBM peak + sum of GEMM flops / tensor peak) "
                                               "/ measured step time"),
             "kernels": class_rates(r["per"], pk),
-            "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "device_status": int(r["status"])}
+            "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "device_status": int(r["status"]),
+            "launch": {"mode": "cuda_graph" if args.graph else "eager",
+                       "eager_ms_per_step": round(r["ms_eager"], 3),
+                       "note": ("the step replayed as one CUDA graph; per-class times (kernels, roofline) come "
+                                "from the same step launched call by call with CUDA events around each call")}}
     if "side" in r:
         side = {}
         for name, w in r["side"].items():
             side[name] = {"TFLOP/s": round(w["gemm_flops"] / (w["ms"] * 1e-3) / 1e12, 1),
-                          "ms_per_step": round(w["ms"], 3), "gemm_tflop_per_step": round(w["gemm_flops"] / 1e12, 4),
+                          "ms_per_step": round(w["ms"], 3), "eager_ms_per_step": round(w["ms_eager"], 3),
+                          "gemm_tflop_per_step": round(w["gemm_flops"] / 1e12, 4),
                           "wgrad_options": w["wgrad"],
                           "fused_roofline": fused_fraction(w["per"], pk, w["ms"]),
                           "kernels": class_rates(w["per"], pk, w["index"])}
