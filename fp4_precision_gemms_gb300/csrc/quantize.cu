@@ -12,12 +12,16 @@
 //                      with 16-byte loads, then each thread encodes one column's
 //                      SEG values into 32 bytes of output codes.
 //   quant_tile_kernel  TMA-pipelined 64-row tiles; rowwise, colwise or both
-//                      operands from one read of x (the dual-direction pass).
-// Both write the block scales straight into the tensor core's scale-factor
+//                      operands from one read of x (the dual-direction pass);
+//                      the automatic producer in both directions.  The row and
+//                      col kernels serve NVFP4 with the Hadamard transform and
+//                      the `direct` test choice.
+// All write the block scales straight into the tensor core's scale-factor
 // layout ("格式感知融合:让FP4预训练提速两倍的工程实践", section
-// 格式感知融合的设计思路: the producer writes the consumer's layout), and both
-// can apply the fixed-sign 32-point Hadamard transform and Philox stochastic
-// rounding (same page, section 两个关键的数值技巧).
+// 格式感知融合的设计思路: the producer writes the consumer's layout), and all
+// can apply the fixed-sign 32-point Hadamard transform (the tile producer for
+// the MX formats) and Philox stochastic rounding (same page, section
+// 两个关键的数值技巧).
 //
 // Bit-exactness: every step is an exactly specified fp32 operation (products
 // with __fmul_rn, correctly rounded quotients, adds in a fixed butterfly order) or
