@@ -536,6 +536,19 @@ struct CfgPair {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
+// One 32-bit TMEM column per lane of the calling warp's lane quarter.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t saddr)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+    return v;
+}
+
 struct PairParams {
     const float* tsa;
     const float* tsb;
@@ -1347,6 +1360,13 @@ __global__ void __launch_bounds__(512, 1)
         // line l of every 512-byte chunk (the scales of rows l, l + 32, l + 64,
         // l + 96); A's chunks fill the slot's SFA columns in order, B's chunk c
         // of row tile r fills columns 8c + 4r .. 8c + 4r + 3 of its SFB columns.
+        // Lane quarter q computes output rows 32q .. 32q + 31, so of A's chunk
+        // it reads only word q (the scales of its own rows, column 4c + q):
+        // NVFP4, with four A chunks per stage, stores just that word (measured:
+        // the same results, 0.4-1.4 % faster; for MXFP8 no difference).  B's
+        // chunks are read by every quarter (each computes all N columns) and
+        // must be complete in all four (measured: storing word q alone gives
+        // wrong products).
         const int q = warp & 3;
         const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t full0_r0 = mapa_shared(full(0), 0);
@@ -1365,17 +1385,26 @@ __global__ void __launch_bounds__(512, 1)
             tc_fence_after();
             const uint32_t sfa_s = s0 + G::OFF_SFA + qs * G::SFA_BYTES + lane * 16;
             const uint32_t sfb_s = s0 + G::OFF_SFB + qs * G::SFB_BYTES + lane * 16;
-            uint4 va[G::NCHUNK];
+            constexpr bool A_WORD = KIND == 2;  // A's scales: only the word this quarter reads
+            uint4 va[A_WORD ? 1 : G::NCHUNK];
+            if constexpr (!A_WORD) {
 #pragma unroll
-            for (int c = 0; c < G::NCHUNK; ++c)
-                va[c] = lds128(sfa_s + c * 512);
+                for (int c = 0; c < G::NCHUNK; ++c)
+                    va[c] = lds128(sfa_s + c * 512);
+            }
             uint4 vb[2 * G::NCHUNK];
 #pragma unroll
             for (int c = 0; c < G::NCHUNK; ++c)
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
                     vb[2 * c + r] = lds128(sfb_s + (r * G::NCHUNK + c) * 512);
-            tmem_st_wide<G::NCHUNK>(tmem + lanes + G::TM_SFA + s * G::SFA_COLS, va);
+            if constexpr (A_WORD) {
+#pragma unroll
+                for (int c = 0; c < G::NCHUNK; ++c)
+                    tmem_st1(tmem + lanes + G::TM_SFA + s * G::SFA_COLS + 4 * c + q, lds32(sfa_s + c * 512 + 4 * q));
+            } else {
+                tmem_st_wide<G::NCHUNK>(tmem + lanes + G::TM_SFA + s * G::SFA_COLS, va);
+            }
             tmem_st_wide<2 * G::NCHUNK>(tmem + lanes + G::TM_SFB + s * G::SFB_COLS, vb);
             tmem_st_wait();
             tc_fence_before();
