@@ -309,29 +309,34 @@ class Plan:
 
     def calls(self, inputs):
         """The step as a list of (kind, fn, flops_or_bytes) in issue order."""
+        return [c[:3] for c in self.roles(inputs)]
+
+    def roles(self, inputs):
+        """The step's calls with their place in the layer: (kind, fn, work,
+        layer index, role), role one of qx, qw, fwd, qdy, dgrad, wgrad."""
         mx, out = self.mx, []
         wg = self.wgrad
         had = dict(col_hadamard=True) if wg["hadamard"] else {}
         dy_col = dict(col_rounding=wg["rounding"], seed=wg["seed"], **had) if (wg["rounding"] != "rne" or had) else {}
-        for e in self.gemms:
+        for li, e in enumerate(self.gemms):
             g = e["g"]
             T, Kin, Nout = e["T"], e["Kin"], e["Nout"]
             flops = 2.0 * T * Kin * Nout
             if g.x is not None and ("xq" in e or "xtq" in e):
                 fn, b = self._quant(inputs[g.x.name], "xq", "xtq", e, had)
-                out.append(("quant", fn, b))
+                out.append(("quant", fn, b, li, "qx"))
             if g.w is not None and ("wq" in e or "wtq" in e):
                 fn, b = self._quant(inputs[g.w.name], "wq", "wtq", e, {})
-                out.append(("quant", fn, b))
+                out.append(("quant", fn, b, li, "qw"))
             if "Y" in e:
-                out.append(("gemm", lambda e=e: mx.gemm(e["xq"], e["wq"], out=e["Y"]), flops))
+                out.append(("gemm", lambda e=e: mx.gemm(e["xq"], e["wq"], out=e["Y"]), flops, li, "fwd"))
             if g.dy is not None and ("dyq" in e or "dytq" in e):
                 fn, b = self._quant(inputs[g.dy.name], "dyq", "dytq", e, dy_col)
-                out.append(("quant", fn, b))
+                out.append(("quant", fn, b, li, "qdy"))
             if "dX" in e:
-                out.append(("gemm", lambda e=e: mx.gemm(e["dyq"], e["wtq"], out=e["dX"]), flops))
+                out.append(("gemm", lambda e=e: mx.gemm(e["dyq"], e["wtq"], out=e["dX"]), flops, li, "dgrad"))
             if "dW" in e:
-                out.append(("gemm", lambda e=e: mx.gemm(e["dytq"], e["xtq"], out=e["dW"]), flops))
+                out.append(("gemm", lambda e=e: mx.gemm(e["dytq"], e["xtq"], out=e["dW"]), flops, li, "wgrad"))
         return out
 
 
@@ -381,16 +386,47 @@ def time_calls(calls, steps, warmup, stream, clk=None, count=None):
     return t0.elapsed_time(t1) / steps, per, counted
 
 
-def graph_time(calls, steps, warmup, stream, clk=None, count=None):
+def issue_two_streams(role_calls, side):
+    """Issues one step on two streams, for capture: the current stream runs each
+    layer's X and W producers and its fwd and dgrad GEMMs, `side` runs its dY
+    producer and wgrad GEMM; events carry the two cross-stream dependencies
+    (dgrad reads dY's rowwise operand, wgrad reads X's colwise one).  Layers are
+    independent of one another, so the graph may run either stream's kernels
+    in the other's idle SMs (the tail of a GEMM's last wave)."""
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    ev = {}
+    for fmt, kind, fn, work, li, role in role_calls:
+        unit = (fmt, li)
+        on_side = role in ("qdy", "wgrad")
+        st = side if on_side else main
+        if role == "dgrad" and (unit, "qdy") in ev:
+            main.wait_event(ev[(unit, "qdy")])
+        if role == "wgrad" and (unit, "qx") in ev:
+            side.wait_event(ev[(unit, "qx")])
+        with torch.cuda.stream(st):
+            fn()
+        if role in ("qx", "qdy"):
+            e = torch.cuda.Event()
+            e.record(st)
+            ev[(unit, role)] = e
+    main.wait_stream(side)
+
+
+def graph_time(calls, steps, warmup, stream, clk=None, count=None, issue=None):
     """One step captured as a CUDA graph (every call launches on the capture
-    stream; operands and outputs are preallocated, so the graph replays the
-    same work), then `warmup` untimed and `steps` timed replays with CUDA
-    events on `stream`.  Returns (ms per step, library launches per step)."""
+    stream, or as `issue` places it; operands and outputs are preallocated, so
+    the graph replays the same work), then `warmup` untimed and `steps` timed
+    replays with CUDA events on `stream`.  Returns (ms per step, library
+    launches per step)."""
     g = torch.cuda.CUDAGraph()
     c0 = count() if count else None
     with torch.cuda.graph(g):
-        for c in calls:
-            c[2]()
+        if issue is not None:
+            issue()
+        else:
+            for c in calls:
+                c[2]()
     per_step = count() - c0 if count else None
     for _ in range(warmup):
         g.replay()
@@ -442,7 +478,12 @@ def run_ours(args, world, rank, local):
         if args.graph:
             torch.cuda.synchronize()
             barrier(world)
-            ms, per_step = graph_time(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count)
+            issue = None
+            if args.streams == 2:
+                side = torch.cuda.Stream(device=device)
+                role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
+                issue = lambda: issue_two_streams(role_calls, side)  # noqa: E731
+            ms, per_step = graph_time(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count, issue=issue)
             launches = per_step * args.steps
     barrier(world)
     status = mx.last_device_status()
@@ -467,14 +508,18 @@ def run_side_workloads(mx, device, stream, args):
     for idx, wg in SIDE_WORKLOADS.items():
         wl = workloads.workloads()[idx]
         inputs = workloads.materialize(wl, device=device)
-        calls = []
-        for fmt in wl.formats:
-            calls += [(fmt,) + c for c in Plan(mx, wl, fmt, device, wgrad=wg).calls(inputs)]
+        plans = [Plan(mx, wl, fmt, device, wgrad=wg) for fmt in wl.formats]
+        calls = [(p.fmt,) + c for p in plans for c in p.calls(inputs)]
         flops = sum(c[3] for c in calls if c[1] == "gemm")
         ms, per, _ = time_calls(calls, args.side_steps, args.warmup, stream)
         ms_eager = ms
         if args.graph:
-            ms, _ = graph_time(calls, args.side_steps, args.warmup, stream)
+            issue = None
+            if args.streams == 2:
+                side = torch.cuda.Stream(device=device)
+                role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
+                issue = lambda: issue_two_streams(role_calls, side)  # noqa: E731
+            ms, _ = graph_time(calls, args.side_steps, args.warmup, stream, issue=issue)
         out[wl.name] = dict(ms=ms, ms_eager=ms_eager, gemm_flops=flops, per=per, wgrad=wg, index=idx)
         del inputs
     torch.cuda.synchronize()
@@ -761,6 +806,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time the step launched call by call instead of as one CUDA graph")
+    ap.add_argument("--streams", type=int, default=2, choices=[1, 2],
+                    help="streams the step's graph is captured on (2: each layer's dY producer and wgrad "
+                         "GEMM on a second stream)")
     ap.add_argument("--no-side", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--side-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -818,10 +866,12 @@ def main():
                                               "/ measured step time"),
             "kernels": class_rates(r["per"], pk),
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "device_status": int(r["status"]),
-            "launch": {"mode": "cuda_graph" if args.graph else "eager",
+            "launch": {"mode": "cuda_graph" if args.graph else "eager", "streams": args.streams if args.graph else 1,
                        "eager_ms_per_step": round(r["ms_eager"], 3),
-                       "note": ("the step replayed as one CUDA graph; per-class times (kernels, roofline) come "
-                                "from the same step launched call by call with CUDA events around each call")}}
+                       "note": ("the step replayed as one CUDA graph (with two streams: each layer's dY producer "
+                                "and weight-gradient GEMM on the second, events for the two cross-stream reads); "
+                                "per-class times (kernels, roofline) come from the same step launched call by call "
+                                "on one stream with CUDA events around each call")}}
     if "side" in r:
         side = {}
         for name, w in r["side"].items():

@@ -58,3 +58,45 @@ def test_graph_replay_equals_eager_launches(mx, fmt):
     g.replay()
     torch.cuda.synchronize()
     same(eager, graphed)
+
+
+def test_two_stream_step_graph_equals_eager_step(mx):
+    """The bench's step captured on two streams (each layer's dY producer and
+    weight-gradient GEMM on a second stream, events for the cross-stream
+    reads) gives bit for bit the outputs of the same calls issued one by one
+    on one stream: small layers, both schemes of the layer-linears workload."""
+    import bench
+
+    gl = []
+    for i, (kin, nout) in enumerate(((512, 768), (768, 512), (512, 1024))):
+        gl.append(workloads.Gemm(f"l{i}", 256, kin, nout, x=workloads._t(f"X{i}", (256, kin), "student_t3"),
+                                 w=workloads._t(f"W{i}", (nout, kin), "normal", 0.02),
+                                 dy=workloads._t(f"dY{i}", (256, nout), "student_t3", 1e-3),
+                                 passes=("fwd", "dgrad", "wgrad")))
+    wl = workloads.Workload(0, "small_layers", ("mxfp8", "nvfp4"), gl)
+    dev = torch.device("cuda", 0)
+    inputs = workloads.materialize(wl, device=dev)
+    plans = [bench.Plan(mx, wl, fmt, dev) for fmt in wl.formats]
+
+    def outputs():
+        return [t.clone() for p in plans for e in p.gemms for t in (e["Y"], e["dX"], e["dW"])]
+
+    for p in plans:
+        for c in p.calls(inputs):
+            c[1]()
+    torch.cuda.synchronize()
+    eager = outputs()
+    for p in plans:  # clear, so that the graph's replay must write everything again
+        for e in p.gemms:
+            for k in ("Y", "dX", "dW"):
+                e[k].fill_(float("nan"))
+    side = torch.cuda.Stream()
+    role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bench.issue_two_streams(role_calls, side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert mx.last_device_status() == mx.MX_OK
+    for a, b in zip(eager, outputs()):
+        assert torch.equal(a, b)
