@@ -386,6 +386,33 @@ def time_calls(calls, steps, warmup, stream, clk=None, count=None):
     return t0.elapsed_time(t1) / steps, per, counted
 
 
+def issue_three_streams(role_calls, s1, s2):
+    """Issues one step on three streams, for capture: the current stream runs
+    each layer's X and W producers and its fwd GEMM, `s1` its dY producer and
+    dgrad GEMM (after W's producer), `s2` its wgrad GEMM (after X's and dY's
+    producers)."""
+    main = torch.cuda.current_stream()
+    s1.wait_stream(main)
+    s2.wait_stream(main)
+    place = {"qx": main, "qw": main, "fwd": main, "qdy": s1, "dgrad": s1, "wgrad": s2}
+    needs = {"dgrad": ("qw",), "wgrad": ("qx", "qdy")}
+    ev = {}
+    for fmt, kind, fn, work, li, role in role_calls:
+        unit = (fmt, li)
+        st = place[role]
+        for dep in needs.get(role, ()):
+            if (unit, dep) in ev:
+                st.wait_event(ev[(unit, dep)])
+        with torch.cuda.stream(st):
+            fn()
+        if role in ("qx", "qw", "qdy"):
+            e = torch.cuda.Event()
+            e.record(st)
+            ev[(unit, role)] = e
+    main.wait_stream(s1)
+    main.wait_stream(s2)
+
+
 def issue_two_streams(role_calls, side):
     """Issues one step on two streams, for capture: the current stream runs each
     layer's X and W producers and its fwd and dgrad GEMMs, `side` runs its dY
@@ -479,10 +506,13 @@ def run_ours(args, world, rank, local):
             torch.cuda.synchronize()
             barrier(world)
             issue = None
+            role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
             if args.streams == 2:
                 side = torch.cuda.Stream(device=device)
-                role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
                 issue = lambda: issue_two_streams(role_calls, side)  # noqa: E731
+            elif args.streams == 3:
+                s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+                issue = lambda: issue_three_streams(role_calls, s1, s2)  # noqa: E731
             ms, per_step = graph_time(calls, args.steps, args.warmup, stream, clk, count=mx.launch_count, issue=issue)
             launches = per_step * args.steps
     barrier(world)
@@ -515,10 +545,13 @@ def run_side_workloads(mx, device, stream, args):
         ms_eager = ms
         if args.graph:
             issue = None
+            role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
             if args.streams == 2:
                 side = torch.cuda.Stream(device=device)
-                role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
                 issue = lambda: issue_two_streams(role_calls, side)  # noqa: E731
+            elif args.streams == 3:
+                s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+                issue = lambda: issue_three_streams(role_calls, s1, s2)  # noqa: E731
             ms, _ = graph_time(calls, args.side_steps, args.warmup, stream, issue=issue)
         out[wl.name] = dict(ms=ms, ms_eager=ms_eager, gemm_flops=flops, per=per, wgrad=wg, index=idx)
         del inputs
@@ -806,9 +839,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time the step launched call by call instead of as one CUDA graph")
-    ap.add_argument("--streams", type=int, default=2, choices=[1, 2],
+    ap.add_argument("--streams", type=int, default=3, choices=[1, 2, 3],
                     help="streams the step's graph is captured on (2: each layer's dY producer and wgrad "
-                         "GEMM on a second stream)")
+                         "GEMM on a second stream; 3: dY producer and dgrad on the second, wgrad on a third)")
     ap.add_argument("--no-side", action="store_true", help="skip the other workloads' lines")
     ap.add_argument("--side-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -868,8 +901,9 @@ def main():
             "gpu_launches": int(r["launches"]), "clocks": r["clocks"], "device_status": int(r["status"]),
             "launch": {"mode": "cuda_graph" if args.graph else "eager", "streams": args.streams if args.graph else 1,
                        "eager_ms_per_step": round(r["ms_eager"], 3),
-                       "note": ("the step replayed as one CUDA graph (with two streams: each layer's dY producer "
-                                "and weight-gradient GEMM on the second, events for the two cross-stream reads); "
+                       "note": ("the step replayed as one CUDA graph (three streams: each layer's X and W producers "
+                                "and fwd GEMM on the first, its dY producer and dgrad GEMM on the second, its wgrad "
+                                "GEMM on the third, events for the cross-stream reads); "
                                 "per-class times (kernels, roofline) come from the same step launched call by call "
                                 "on one stream with CUDA events around each call")}}
     if "side" in r:

@@ -60,11 +60,13 @@ def test_graph_replay_equals_eager_launches(mx, fmt):
     same(eager, graphed)
 
 
-def test_two_stream_step_graph_equals_eager_step(mx):
-    """The bench's step captured on two streams (each layer's dY producer and
-    weight-gradient GEMM on a second stream, events for the cross-stream
-    reads) gives bit for bit the outputs of the same calls issued one by one
-    on one stream: small layers, both schemes of the layer-linears workload."""
+@pytest.mark.parametrize("streams", [2, 3])
+def test_multi_stream_step_graph_equals_eager_step(mx, streams):
+    """The bench's step captured on two or three streams (each layer's dY
+    producer and gradient GEMMs on further streams, events for the
+    cross-stream reads) gives bit for bit the outputs of the same calls issued
+    one by one on one stream: small layers, both schemes of the layer-linears
+    workload."""
     import bench
 
     gl = []
@@ -90,11 +92,14 @@ def test_two_stream_step_graph_equals_eager_step(mx):
         for e in p.gemms:
             for k in ("Y", "dX", "dW"):
                 e[k].fill_(float("nan"))
-    side = torch.cuda.Stream()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
     role_calls = [(p.fmt,) + c for p in plans for c in p.roles(inputs)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        bench.issue_two_streams(role_calls, side)
+        if streams == 2:
+            bench.issue_two_streams(role_calls, s1)
+        else:
+            bench.issue_three_streams(role_calls, s1, s2)
     g.replay()
     torch.cuda.synchronize()
     assert mx.last_device_status() == mx.MX_OK
