@@ -29,7 +29,7 @@ MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_ALIGNMENT = 0, 1, 2, 3
 MX_ERR_CUDA, MX_ERR_TIMEOUT, MX_ERR_NO_DEVICE, MX_ERR_WORKSPACE = 4, 5, 6, 7
 
 EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_scale_count", "mx_amax", "mx_quantize", "mx_quantize_dual", "mx_dequantize", "mx_gemm",
-            "mx_gemm_quantized",
+            "mx_gemm_amax", "mx_gemm_quantized",
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd",
             "mx_linear_saved_bytes", "mx_linear_fwd_save", "mx_linear_bwd_saved", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
@@ -96,6 +96,8 @@ def lib():
             L.mx_dequantize.argtypes = [C.POINTER(_CTensor), p, p]
             L.mx_gemm.restype = i32
             L.mx_gemm.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float, p, i64, i32, p]
+            L.mx_gemm_amax.restype = i32
+            L.mx_gemm_amax.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float, p, i64, i32, p, p]
             L.mx_gemm_quantized.restype = i32
             L.mx_gemm_quantized.argtypes = [C.POINTER(_CTensor), C.POINTER(_CTensor), C.c_float,
                                             C.POINTER(_CTensor), p]
@@ -274,15 +276,24 @@ def dequantize(q: MXTensor, stream=None) -> torch.Tensor:
 
 
 def gemm(a: MXTensor, b: MXTensor, extra_alpha: float = 1.0, out_dtype=torch.float32,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """C[M, N] = alpha * dq(a) dq(b)^T on the tensor cores."""
-    _on_gpu(out)
+         out: torch.Tensor | None = None, stream=None, amax_out: torch.Tensor | None = None) -> torch.Tensor:
+    """C[M, N] = alpha * dq(a) dq(b)^T on the tensor cores.  amax_out: an
+    optional one-element fp32 device tensor that receives max |C| as written,
+    reduced in the GEMM's epilogue."""
+    _on_gpu(out, amax_out)
     out = out if out is not None else torch.empty((a.rows, b.rows), dtype=out_dtype,
                                                   device=a.codes.device)
     ca, cb = a._c(), b._c()
-    rc = lib().mx_gemm(C.byref(ca), C.byref(cb), float(extra_alpha), _ptr(out), out.stride(0),
-                       OUT[out.dtype], _stream(stream))
-    _check(rc, "mx_gemm")
+    if amax_out is None:
+        rc = lib().mx_gemm(C.byref(ca), C.byref(cb), float(extra_alpha), _ptr(out), out.stride(0),
+                           OUT[out.dtype], _stream(stream))
+        _check(rc, "mx_gemm")
+    else:
+        if amax_out.dtype != torch.float32 or amax_out.numel() < 1:
+            raise ValueError("amax_out must be a float32 tensor with at least one element")
+        rc = lib().mx_gemm_amax(C.byref(ca), C.byref(cb), float(extra_alpha), _ptr(out), out.stride(0),
+                                OUT[out.dtype], _ptr(amax_out), _stream(stream))
+        _check(rc, "mx_gemm_amax")
     return out
 
 

@@ -178,9 +178,53 @@ struct GemmParams {
     int64_t q_kgroups;
     int64_t kgroups;  // 4-block SF groups along K (same for A and B)
     int m_tiles, n_tiles, group_m;  // tile grid and the M-extent of a raster group
+    unsigned* amax_out;               // optional: max |C| as written (fp32 bits), zeroed by the caller
     int* status;
     uint64_t wait_ns;
 };
+
+// Output amax of the epilogue.  Rounding is monotone and symmetric, so the
+// largest |value as written| is the largest |accumulator| of the written
+// positions scaled by |alpha| in fp32 (one product per chunk) and, for a bf16
+// output, rounded to bf16 once at the end: max_i |rn(c a_i)| = rn(|c| max_i |a_i|).
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ float as_f32(float x) { return x; }
+__device__ __forceinline__ float as_f32(uint32_t x) { return __uint_as_float(x); }
+
+// max |x[i]| over the first n of a chunk's 32 values (NaN if one of them is).
+template <typename T>
+__device__ __forceinline__ float absmax32(const T (&x)[32], int n)
+{
+    float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (n >= 32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            m[i & 3] = max_nan(m[i & 3], fabsf(as_f32(x[i])));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < n)
+                m[i & 3] = max_nan(m[i & 3], fabsf(as_f32(x[i])));
+    }
+    return max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3]));
+}
+
+// One atomic max per warp of the warp's largest value (called by whole warps);
+// non-negative floats and NaN order like their bit patterns.
+__device__ __forceinline__ void flush_amax(unsigned* out, float m, bool bf16)
+{
+    if (bf16)
+        m = __bfloat162float(__float2bfloat16_rn(m));
+    const uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+    if ((threadIdx.x & 31) == 0 && u != 0)
+        atomicMax(out, u);
+}
 
 __device__ __forceinline__ void record_timeout(const GemmParams& p, volatile int* abort_flag)
 {
@@ -317,6 +361,7 @@ __global__ void __launch_bounds__(192, 1)
         // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = tile rows.
         const int q = warp & 3;
         const int row = m_tile * G::BM + q * 32 + lane;
+        float am = 0.0f;
         if (!mbar_wait_bounded(accf, 0, p.wait_ns)) {
             record_timeout(p, abort_flag);
         } else {
@@ -335,9 +380,15 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __fmul_rn(__uint_as_float(r[i]), al);
+                    if (p.amax_out)
+                        am = max_nan(am, absmax32(v, p.N - col0));
                     store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
+        }
+        if (p.amax_out) {
+            __syncwarp();
+            flush_amax(p.amax_out, am, p.out_mode == EPI_BF16);
         }
     }
     tc_fence_before();
@@ -411,7 +462,7 @@ int raster_group_m(int64_t M, int64_t N, int64_t kbytes, int bm, int bn, int m_t
 
 template <int KIND, int BN, int STAGES>
 int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
-                uint8_t* q_sf, const Device& d, cudaStream_t s)
+                uint8_t* q_sf, const Device& d, cudaStream_t s, unsigned* amax_out = nullptr)
 {
     using G = Cfg<KIND, BN, STAGES>;
     static int configured_device = -1;  // attribute set once per device for this instantiation
@@ -427,6 +478,7 @@ int launch_tile(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     if (!make_code_map(&ta, A->codes, M, kbytes, G::BM) || !make_code_map(&tb, B->codes, N, kbytes, BN))
         return MX_ERR_CUDA;
     GemmParams p;
+    p.amax_out = amax_out;
     p.sfa = A->sf;
     p.sfb = B->sf;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
@@ -562,6 +614,7 @@ struct PairParams {
     int64_t q_kgroups;
     int64_t kgroups;
     int m_tiles, n_tiles, group_m;  // 256 x 256 tiles
+    unsigned* amax_out;             // optional: max |C| as written (fp32 bits), zeroed by the caller
     int* status;
     uint64_t wait_ns;
 };
@@ -855,6 +908,7 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         bool sf_good = true;
         const bool tma_out = G::TMA_OUT && p.out_mode <= EPI_BF16;
         bool stg_busy = false;  // this warp's staging box may still be read by a TMA store
+        float am = 0.0f;        // output amax of this thread's rows (amax_out)
         for (int tile = cluster_id; tile < tiles && sf_good; tile += nclusters, ++titer) {
             int mt, nt;
             grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
@@ -925,6 +979,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
                         break;
                     const float al =
                         (p.ts_region && row < p.M) ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    if (p.amax_out && row < p.M)
+                        am = max_nan(am, __fmul_rn(absmax32(r[j], p.N - col0), fabsf(al)));
                     uint32_t pk[16];
                     if (bf16) {
 #pragma unroll
@@ -955,6 +1011,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
+                    if (p.amax_out)
+                        am = max_nan(am, absmax32(v, p.N - col0));
                     store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 };
                 if constexpr (STAGES <= 3) {
@@ -982,6 +1040,8 @@ __global__ void __launch_bounds__(CfgPair<KIND, STAGES, BKB_, SFS_>::THREADS, 1)
         if (stg_busy && lane == 0)
             bulk_wait_all();  // this warp's output stores have completed
         __syncwarp();
+        if (p.amax_out)
+            flush_amax(p.amax_out, am, p.out_mode == EPI_BF16);
     }
     tc_fence_before();
     __syncthreads();
@@ -1031,7 +1091,7 @@ bool make_out_map(CUtensorMap* m, void* c, int64_t M, int64_t N, int64_t ldc, in
 
 template <int KIND, int STAGES, int BKB_ = 128, int SFS = 4>
 int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
-                uint8_t* q_sf, const Device& d, cudaStream_t s)
+                uint8_t* q_sf, const Device& d, cudaStream_t s, unsigned* amax_out = nullptr)
 {
     using G = CfgPair<KIND, STAGES, BKB_, SFS>;
     auto kernel = bs_gemm_pair_kernel<KIND, STAGES, BKB_, SFS>;
@@ -1069,6 +1129,7 @@ int launch_pair(const mx_tensor* A, const mx_tensor* B, float extra, void* C, in
     if (G::TMA_OUT && out_mode <= EPI_BF16 && !make_out_map(&tc, C, M, N, ldc, out_mode))
         return MX_ERR_CUDA;
     PairParams p;
+    p.amax_out = amax_out;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
     p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
     p.extra = extra;
@@ -1428,6 +1489,7 @@ __global__ void __launch_bounds__(512, 1)
         const bool bf16 = p.out_mode == EPI_BF16;
         const int esz = bf16 ? 2 : 4;
         int titer = 0;
+        float am = 0.0f;  // output amax of this thread's rows (amax_out)
         for (int tile = cluster_id; tile < tiles; tile += nclusters, ++titer) {
             int mt, nt;
             grouped_tile(tile, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
@@ -1501,6 +1563,8 @@ __global__ void __launch_bounds__(512, 1)
                         break;
                     const float al =
                         (p.ts_region && row < p.M) ? region_alpha(p.tsa, p.tsb, p.extra, row, col0) : alpha;
+                    if (p.amax_out && row < p.M)
+                        am = max_nan(am, __fmul_rn(absmax32(r[j], p.N - col0), fabsf(al)));
                     uint32_t pk[16];
                     if (bf16) {
 #pragma unroll
@@ -1534,11 +1598,15 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __fmul_rn(__uint_as_float(r[j][i]), al);
+                    if (p.amax_out)
+                        am = max_nan(am, absmax32(v, p.N - col0));
                     store_chunk(p.out_mode, p.c, p.ldc, p.q_sf, p.q_kgroups, p.N, row, col0, v);
                 }
             }
         }
         __syncwarp();
+        if (p.amax_out)
+            flush_amax(p.amax_out, am, p.out_mode == EPI_BF16);
     }
     tc_fence_before();
     __syncthreads();
@@ -1554,7 +1622,7 @@ __global__ void __launch_bounds__(512, 1)
 
 template <int KIND, int STAGES, int BKB_ = 128, int SFS = 5>
 int launch_ws(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
-              uint8_t* q_sf, const Device& d, cudaStream_t s)
+              uint8_t* q_sf, const Device& d, cudaStream_t s, unsigned* amax_out = nullptr)
 {
     using G = CfgWs<KIND, STAGES, BKB_, SFS>;
     auto kernel = bs_gemm_ws_kernel<KIND, STAGES, BKB_, SFS>;
@@ -1595,6 +1663,7 @@ int launch_ws(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int6
         !make_sf_map(&tsa, A->sf, sfa_bytes, G::NCHUNK) || !make_sf_map(&tsb, B->sf, sfb_bytes, G::NCHUNK))
         return MX_ERR_CUDA;
     PairParams p;
+    p.amax_out = amax_out;
     p.tsa = fmt_has_tensor_scale(A->fmt) ? A->tensor_scale : nullptr;
     p.tsb = fmt_has_tensor_scale(B->fmt) ? B->tensor_scale : nullptr;
     p.extra = extra;
@@ -1623,11 +1692,11 @@ int launch_ws(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int6
 
 template <int KIND>
 int launch_kind(const mx_tensor* A, const mx_tensor* B, float extra, void* C, int64_t ldc, int out_mode,
-                uint8_t* q_sf, const Device& d, cudaStream_t s, int bn)
+                uint8_t* q_sf, const Device& d, cudaStream_t s, int bn, unsigned* amax_out)
 {
     if (bn == 128)
-        return launch_tile<KIND, 128, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s);
-    return launch_tile<KIND, 256, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s);
+        return launch_tile<KIND, 128, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s, amax_out);
+    return launch_tile<KIND, 256, 4>(A, B, extra, C, ldc, out_mode, q_sf, d, s, amax_out);
 }
 
 }  // namespace
@@ -1641,7 +1710,7 @@ static thread_local int g_variant = 0;
 static thread_local int g_last_variant = 0;  // the variant this thread's last launch_gemm chose
 
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_mode,
-                const Device& d, cudaStream_t s, uint8_t* q_sf)
+                const Device& d, cudaStream_t s, uint8_t* q_sf, unsigned* amax_out)
 {
     if (A->rows == 0 || B->rows == 0)
         return MX_OK;
@@ -1663,13 +1732,13 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         switch (kind) {
         case 0:
             if (A->k % 256 == 0)
-                return launch_ws<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_ws<0, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_ws<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+            return launch_ws<0, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
         case 1:
             if (A->k % 512 == 0)
-                return launch_ws<1, 3, 256, 2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_ws<1, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        default: return launch_ws<2, 5, 128, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_ws<1, 3, 256, 2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+            return launch_ws<1, 5, 128, 6>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+        default: return launch_ws<2, 5, 128, 5>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
         }
     }
     if (v == 3) {
@@ -1679,20 +1748,20 @@ int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void*
         // NVFP4, whose stages of eight MMAs do not fit, take five stages of 128.
         case 0:
             if (A->k % 256 == 0)
-                return launch_pair<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_pair<0, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_pair<0, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+            return launch_pair<0, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
         case 1:
             if (A->k % 512 == 0)
-                return launch_pair<1, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-            return launch_pair<1, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
-        default: return launch_pair<2, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s);
+                return launch_pair<1, 3, 256, 4>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+            return launch_pair<1, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
+        default: return launch_pair<2, 5, 128, 8>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, amax_out);
         }
     }
     const int bn = v == 1 ? 128 : 256;
     switch (kind) {
-    case 0: return launch_kind<0>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
-    case 1: return launch_kind<1>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
-    default: return launch_kind<2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn);
+    case 0: return launch_kind<0>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn, amax_out);
+    case 1: return launch_kind<1>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn, amax_out);
+    default: return launch_kind<2>(A, B, extra_alpha, C, ldc, out_mode, q_sf, d, s, bn, amax_out);
     }
 }
 

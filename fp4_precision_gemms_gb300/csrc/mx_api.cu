@@ -364,7 +364,7 @@ int quantize_dual_impl(const void* x, int64_t R, int64_t C, int64_t ld, int fmt,
 }
 
 int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
-              const Device& d, cudaStream_t s)
+              const Device& d, cudaStream_t s, float* amax_out = nullptr)
 {
     int rc = check_operand(A);
     if (rc != MX_OK)
@@ -377,6 +377,12 @@ int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C
     if (out_dtype != MX_OUT_F32 && out_dtype != MX_OUT_BF16)
         return MX_ERR_INVALID_ARG;
     const int64_t M = A->rows, N = B->rows, K = A->k;
+    if (amax_out) {  // zeroed first: an empty product has amax 0
+        if (reinterpret_cast<uintptr_t>(amax_out) % 4 != 0)
+            return MX_ERR_ALIGNMENT;
+        if (cudaMemsetAsync(amax_out, 0, sizeof(float), s) != cudaSuccess)
+            return MX_ERR_CUDA;
+    }
     if (M == 0 || N == 0)
         return MX_OK;
     if (!C || ldc < N)
@@ -389,7 +395,7 @@ int gemm_impl(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C
     if (K == 0)
         return cudaMemset2DAsync(C, ldc * esz, 0, N * esz, M, s) == cudaSuccess ? MX_OK : MX_ERR_CUDA;
     const float extra = A->hadamard ? extra_alpha * (1.0f / 32.0f) : extra_alpha;
-    return launch_gemm(A, B, extra, C, ldc, out_dtype, d, s);
+    return launch_gemm(A, B, extra, C, ldc, out_dtype, d, s, nullptr, reinterpret_cast<unsigned*>(amax_out));
 }
 
 // The GEMM with its output quantized in the epilogue into the rowwise MX
@@ -502,6 +508,18 @@ int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, 
     if (rc != MX_OK)
         return rc;
     return gemm_impl(A, B, extra_alpha, C, ldc, out_dtype, d, static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm_amax(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_dtype,
+                 float* amax_out, void* stream)
+{
+    if (!amax_out)
+        return MX_ERR_INVALID_ARG;
+    Device d;
+    const int rc = current_device(&d);
+    if (rc != MX_OK)
+        return rc;
+    return gemm_impl(A, B, extra_alpha, C, ldc, out_dtype, d, static_cast<cudaStream_t>(stream), amax_out);
 }
 
 int mx_gemm_quantized(const mx_tensor* A, const mx_tensor* B, float extra_alpha, mx_tensor* out, void* stream)

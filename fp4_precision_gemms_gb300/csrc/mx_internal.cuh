@@ -110,9 +110,10 @@ int launch_dequantize(const mx_tensor* A, float* out, const Device& d, cudaStrea
 // out_mode: MX_OUT_F32 / MX_OUT_BF16 into C (row stride ldc elements), or 2 / 3
 // for C quantized in the epilogue into the rowwise MXFP8 / MXFP4 operand
 // (codes at C, row stride ldc bytes; E8M0 scales at q_sf in the tensor-core
-// layout; N % 32 == 0).
+// layout; N % 32 == 0).  amax_out (F32 / BF16 output only): max |C| as
+// written, reduced into the fp32 bit pattern there (the caller zeroes it).
 int launch_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc, int out_mode,
-                const Device& d, cudaStream_t s, uint8_t* q_sf = nullptr);
+                const Device& d, cudaStream_t s, uint8_t* q_sf = nullptr, unsigned* amax_out = nullptr);
 int launch_wait_selftest(uint64_t limit_ns, const Device& d, cudaStream_t s);
 int launch_divide_check(const float* v, const float* dv, int64_t n, float* fast, float* ieee, const Device& d,
                         cudaStream_t s);

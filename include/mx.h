@@ -207,6 +207,20 @@ int mx_dequantize(const mx_tensor* A, float* out, void* stream);
 int mx_gemm(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
             int out_dtype, void* stream);
 
+/* mx_gemm that also returns the output's absolute maximum, reduced in the
+ * epilogue from the values as written (after the bf16 rounding for
+ * MX_OUT_BF16): *amax_out = max |C[i, j]| over the M x N view, NaN if any
+ * element is NaN.  This is the tensor amax that the next quantization of C
+ * needs for its tensor scale ([FAF] nvfp: amax / (448 * 6); [MOSS]
+ * 两级缩放实现, level 1), so the producer that follows can take it through its
+ * amax_in argument instead of a separate reduction pass over C.  amax_out is a
+ * device pointer to one float (4-byte aligned) that the call zeroes on
+ * `stream` before the GEMM; an empty product (M, N or K zero) gives 0.
+ * Errors: MX_ERR_INVALID_ARG for a null amax_out, MX_ERR_ALIGNMENT for a
+ * misaligned one, otherwise as mx_gemm.  Allocates nothing; graph-capturable. */
+int mx_gemm_amax(const mx_tensor* A, const mx_tensor* B, float extra_alpha, void* C, int64_t ldc,
+                 int out_dtype, float* amax_out, void* stream);
+
 /* The block-scaled GEMM with its result quantized in the epilogue into the
  * rowwise MX operand that a following GEMM consumes ([FAF]
  * 格式感知融合的设计思路: the producer writes the consumer's layout, here the
