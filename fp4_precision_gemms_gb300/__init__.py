@@ -33,7 +33,7 @@ EXPORTED = ("mx_codes_bytes", "mx_sf_bytes", "mx_scale_count", "mx_amax", "mx_qu
             "mx_linear_workspace_bytes", "mx_linear_fwd", "mx_linear_fwd_noalloc", "mx_linear_bwd",
             "mx_linear_saved_bytes", "mx_linear_fwd_save", "mx_linear_bwd_saved", "mx_strerror",
             "mx_last_device_status", "mx_selftest_bounded_wait", "mx_launch_count",
-            "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_tile_fail_at", "mx_debug_set_gemm_variant",
+            "mx_debug_divide", "mx_debug_set_quant_impl", "mx_debug_set_tile_fail_at", "mx_debug_set_bwd_fork", "mx_debug_set_gemm_variant",
             "mx_debug_last_gemm_variant")
 
 
@@ -92,6 +92,8 @@ def lib():
             L.mx_debug_set_quant_impl.argtypes = [i32]
             L.mx_debug_set_tile_fail_at.restype = None
             L.mx_debug_set_tile_fail_at.argtypes = [i64]
+            L.mx_debug_set_bwd_fork.restype = None
+            L.mx_debug_set_bwd_fork.argtypes = [i32]
             L.mx_dequantize.restype = i32
             L.mx_dequantize.argtypes = [C.POINTER(_CTensor), p, p]
             L.mx_gemm.restype = i32
@@ -266,6 +268,13 @@ def set_quant_impl(impl: str) -> None:
 def set_tile_fail_at(tile: int) -> None:
     """Test hook: the tile producer gives up its wait on this tile of each CTA (-1: off)."""
     lib().mx_debug_set_tile_fail_at(int(tile))
+
+
+def set_bwd_fork(on: bool) -> None:
+    """Whether linear_bwd / linear_bwd_saved run the weight gradient on the
+    library's side stream (the default) or after the data gradient on the
+    caller's stream.  Per host thread."""
+    lib().mx_debug_set_bwd_fork(int(on))
 
 
 def dequantize(q: MXTensor, stream=None) -> torch.Tensor:

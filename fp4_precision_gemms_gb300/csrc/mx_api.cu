@@ -110,6 +110,60 @@ size_t carve(uint8_t* ws, int fmt, int64_t rows, int64_t k, mx_tensor* t)
 thread_local int g_quant_impl = 0;
 thread_local int64_t g_tile_fail_at = -1;  // test hook: tile producer's forced wait failure
 
+// The backward calls' gradient fork: with both gradients requested, the weight
+// gradient runs on a side stream while the data gradient runs on the caller's
+// stream, joined back by events (in graph capture these become the graph's
+// fork and join edges), so each GEMM's last partial wave leaves SMs to the
+// other.  One non-blocking side stream and two events per host thread and
+// device, created on first use outside capture; a call captured before they
+// exist runs on the caller's stream alone.  The results do not depend on it.
+struct BwdFork {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool failed = false;
+};
+constexpr int kForkDevices = 64;
+thread_local BwdFork g_fork[kForkDevices];
+thread_local int g_bwd_fork = 1;
+
+// A side stream whose next work follows everything issued to s so far, or
+// nullptr (run on s).  Leaves no CUDA error behind either way.
+cudaStream_t fork_begin(const Device& d, cudaStream_t s)
+{
+    if (!g_bwd_fork || d.id < 0 || d.id >= kForkDevices)
+        return nullptr;
+    BwdFork& f = g_fork[d.id];
+    if (!f.side) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (f.failed || cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        if (cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            f.failed = true;
+            f.side = nullptr;
+            return nullptr;
+        }
+    }
+    if (cudaEventRecord(f.fork, s) != cudaSuccess || cudaStreamWaitEvent(f.side, f.fork, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return f.side;
+}
+
+// Makes s wait for everything issued to the side stream.
+int fork_end(const Device& d, cudaStream_t side, cudaStream_t s)
+{
+    BwdFork& f = g_fork[d.id];
+    return cudaEventRecord(f.join, side) == cudaSuccess && cudaStreamWaitEvent(s, f.join, 0) == cudaSuccess
+               ? MX_OK
+               : MX_ERR_CUDA;
+}
+
 // Shared argument checks of the single and dual producers.
 int check_quantize_args(const void* x, int64_t R, int64_t C, int64_t ld, int fmt, int block, int rule)
 {
@@ -610,33 +664,33 @@ int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64
         if (rc != MX_OK)
             return rc;
     }
+    // data gradient on s, weight gradient on the side stream when both are wanted
+    cudaStream_t sw = dX && dW ? fork_begin(d, s) : nullptr;
     if (dX) {
-        if (!dW) {
+        if (!dW)
             rc = quantize_impl(dY, T, Nout, Nout, MX_ROWWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
                                nullptr, &dyr, d, s);
-            if (rc != MX_OK)
-                return rc;
-        }
-        rc = quantize_impl(W, Nout, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
-                           nullptr, &wt, d, s);
-        if (rc != MX_OK)
-            return rc;
-        rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s);
-        if (rc != MX_OK)
-            return rc;
+        if (rc == MX_OK)
+            rc = quantize_impl(W, Nout, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0, 0,
+                               nullptr, &wt, d, s);
+        if (rc == MX_OK)
+            rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s);
     }
-    if (dW) {
-        if (!dX) {
+    if (dW && rc == MX_OK) {
+        cudaStream_t s2 = sw ? sw : s;
+        if (!dX)
             rc = quantize_impl(dY, T, Nout, Nout, MX_COLWISE, fmt, block, o.wgrad_dy_rounding, MX_SCALE_DEFAULT,
-                               o.seed, o.stream_id, o.wgrad_hadamard, nullptr, &dyt, d, s);
-            if (rc != MX_OK)
-                return rc;
-        }
-        rc = quantize_impl(X, T, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0,
-                           o.wgrad_hadamard, nullptr, &xt, d, s);
-        if (rc != MX_OK)
-            return rc;
-        rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s);
+                               o.seed, o.stream_id, o.wgrad_hadamard, nullptr, &dyt, d, s2);
+        if (rc == MX_OK)
+            rc = quantize_impl(X, T, Kin, Kin, MX_COLWISE, fmt, block, MX_ROUND_RNE, MX_SCALE_DEFAULT, 0, 0,
+                               o.wgrad_hadamard, nullptr, &xt, d, s2);
+        if (rc == MX_OK)
+            rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s2);
+    }
+    if (sw) {
+        const int rj = fork_end(d, sw, s);
+        if (rc == MX_OK)
+            rc = rj;
     }
     return rc;
 }
@@ -741,10 +795,17 @@ int mx_linear_bwd_saved(const void* dY, int64_t T, int64_t Kin, int64_t Nout, in
     }
     if (rc != MX_OK)
         return rc;
-    if (dX && (rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s)) != MX_OK)
-        return rc;
-    if (dW)
-        rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, s);
+    // data gradient on s, weight gradient on the side stream when both are wanted
+    cudaStream_t sw = dX && dW ? fork_begin(d, s) : nullptr;
+    if (dX)
+        rc = gemm_impl(&dyr, &wt, 1.0f, dX, Kin, dx_dtype, d, s);
+    if (dW && rc == MX_OK)
+        rc = gemm_impl(&dyt, &xt, 1.0f, dW, Kin, dw_dtype, d, sw ? sw : s);
+    if (sw) {
+        const int rj = fork_end(d, sw, s);
+        if (rc == MX_OK)
+            rc = rj;
+    }
     return rc;
 }
 
@@ -815,6 +876,8 @@ int mx_debug_divide(const float* v, const float* d, int64_t n, float* q_fast, fl
 void mx_debug_set_quant_impl(int impl) { g_quant_impl = (impl >= 0 && impl <= 2) ? impl : 0; }
 
 void mx_debug_set_tile_fail_at(int64_t tile) { g_tile_fail_at = tile >= 0 ? tile : -1; }
+
+void mx_debug_set_bwd_fork(int on) { g_bwd_fork = on ? 1 : 0; }
 
 // Test hook: force one GEMM kernel variant (0 = automatic).
 void mx_debug_set_gemm_variant(int variant) { set_gemm_variant(variant); }

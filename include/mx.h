@@ -280,7 +280,16 @@ typedef struct mx_bwd_opts {
  *   dgrad dX[T, Kin]  = dY[T, Nout] W[Nout, Kin]   (dY rowwise, W colwise)
  *   wgrad dW[Nout, Kin] = dY^T X                    (dY, X colwise)
  * dX or dW may be NULL to skip that GEMM.  Outputs are row-major with row
- * strides Kin, in dx_dtype / dw_dtype. */
+ * strides Kin, in dx_dtype / dw_dtype.
+ * With both dX and dW the weight gradient (X^T's producer and its GEMM) runs
+ * on a side stream of the library that waits for the work issued to `stream`
+ * before the fork and that `stream` waits for before the call returns (an
+ * event join, which graph capture records as a fork and a join), so the two
+ * GEMMs fill each other's last partial wave; the results are the same either
+ * way.  The side stream and its two events are created once per host thread
+ * and device, on the first such call made outside graph capture; a call
+ * captured before then runs on `stream` alone.  Work the caller issues to
+ * `stream` after the call is ordered after both gradients. */
 int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64_t Kin,
                   int64_t Nout, int fmt, const mx_bwd_opts* opts, void* dX, int dx_dtype,
                   void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream);
@@ -321,7 +330,9 @@ int mx_linear_fwd_save(const void* X, const void* W, int64_t T, int64_t Kin, int
  * Results are bit-identical to mx_linear_bwd with the same opts.  `saved` is
  * the buffer mx_linear_fwd_save filled (read only), `opts` must be the ones
  * given to it.  dy_amax as x_amax above.  dX or dW may be NULL to skip that
- * GEMM.  workspace: device, >= mx_linear_workspace_bytes(.., pass 2). */
+ * GEMM.  workspace: device, >= mx_linear_workspace_bytes(.., pass 2).  With
+ * both dX and dW the weight-gradient GEMM runs on the side stream, forked and
+ * joined as in mx_linear_bwd. */
 int mx_linear_bwd_saved(const void* dY, int64_t T, int64_t Kin, int64_t Nout, int fmt, const float* dy_amax,
                         const mx_bwd_opts* opts, const void* saved, size_t saved_bytes, void* dX, int dx_dtype,
                         void* dW, int dw_dtype, void* workspace, size_t ws_bytes, void* stream);
@@ -363,6 +374,12 @@ void mx_debug_set_quant_impl(int impl);
  * (mx_last_device_status); outputs of such a pass are unspecified.  -1 (the
  * initial value) turns it off.  Nothing faults or hangs. */
 void mx_debug_set_tile_fail_at(int64_t tile);
+
+/* Test and tuning hook: 0 runs both gradients of mx_linear_bwd /
+ * mx_linear_bwd_saved on the caller's stream, one after the other; 1 (the
+ * initial setting) forks the weight gradient onto the side stream.  Per host
+ * thread. */
+void mx_debug_set_bwd_fork(int on);
 
 /* Test hook: force one GEMM kernel variant for later mx_gemm / mx_linear_*
  * calls made by the calling host thread (other threads keep their own choice,

@@ -150,3 +150,75 @@ def test_saved_state_buffers_too_small(mx):
     with pytest.raises(mx.MXError) as e:
         mx.linear_bwd_saved(X, sv[:1024], 256, "mxfp8")
     assert e.value.code == mx.MX_ERR_WORKSPACE
+
+
+def _bwd_inputs(T, Kin, Nout, seed):
+    X = workloads.draw("student_t3", (T, Kin), seed).cuda()
+    W = workloads.draw("normal", (Nout, Kin), seed + 1, 0.02).cuda()
+    dY = workloads.draw("student_t3", (T, Nout), seed + 2, 1e-3).cuda()
+    return X, W, dY
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4", "nvfp4"])
+def test_gradient_fork_equals_one_stream(mx, fmt):
+    """The weight gradient on the library's side stream gives bit for bit what
+    the two gradients give one after the other on the caller's stream, for the
+    plain and the saved-state backward, launched eagerly and replayed from a
+    captured graph (many tiles per GEMM, so the two really run side by side)."""
+    T, Kin, Nout = 2048, 1024, 1536
+    X, W, dY = _bwd_inputs(T, Kin, Nout, 181)
+    kw = dict(wgrad_hadamard=fmt == "mxfp4", wgrad_dy_rounding="sr" if fmt == "mxfp4" else "rne", seed=7,
+              stream_id=1)
+    _, saved = mx.linear_fwd_save(X, W, fmt, **kw)
+    mx.set_bwd_fork(False)
+    try:
+        ref = mx.linear_bwd(dY, X, W, fmt, **kw) + mx.linear_bwd_saved(dY, saved, Kin, fmt, **kw)
+    finally:
+        mx.set_bwd_fork(True)
+    got = mx.linear_bwd(dY, X, W, fmt, **kw) + mx.linear_bwd_saved(dY, saved, Kin, fmt, **kw)
+    torch.cuda.synchronize()
+    assert mx.last_device_status() == mx.MX_OK
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    ws = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "bwd_saved"), dtype=torch.uint8, device="cuda")
+    dX = torch.full_like(got[2], float("nan"))
+    dW = torch.full_like(got[3], float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.linear_bwd_saved(dY, saved, Kin, fmt, workspace=ws, dX=dX, dW=dW, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(dX, ref[2]) and torch.equal(dW, ref[3])
+
+
+def test_gradient_fork_first_captured_call_in_a_thread(mx):
+    """A thread whose first backward call is made under graph capture (before
+    its side stream exists) runs both gradients on the capturing stream and
+    gives the same results."""
+    import threading
+
+    T, Kin, Nout, fmt = 1024, 512, 768, "nvfp4"
+    X, W, dY = _bwd_inputs(T, Kin, Nout, 191)
+    ref = mx.linear_bwd(dY, X, W, fmt)
+    ws = torch.empty(mx.workspace_bytes(T, Kin, Nout, fmt, "bwd"), dtype=torch.uint8, device="cuda")
+    dX, dW = torch.empty_like(ref[0]), torch.empty_like(ref[1])
+    torch.cuda.synchronize()
+    out = {}
+
+    def body():
+        try:
+            torch.cuda.set_device(0)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                mx.linear_bwd(dY, X, W, fmt, workspace=ws, dX=dX, dW=dW)
+            g.replay()
+            torch.cuda.synchronize()
+            out["ok"] = True
+        except Exception as e:  # reported below, in the test's own thread
+            out["err"] = e
+
+    t = threading.Thread(target=body)
+    t.start()
+    t.join()
+    assert "err" not in out, out.get("err")
+    assert torch.equal(dX, ref[0]) and torch.equal(dW, ref[1])
