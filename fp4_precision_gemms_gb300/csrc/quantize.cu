@@ -68,56 +68,67 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v)
 // Stochastic rounding of 8 values onto the E2M1 grid {0, .5, 1, 1.5, 2, 3,
 // 4, 6}: a value rounds up iff u16 < p * 2^16, p = (|s| - lo) / (hi - lo),
 // saturating at 6; the codes come packed as cvt_e2m1x8 packs them.  lo is
-// |s| with its significand cut to one bit (|s| >= 1), or 0.5 or 0 below 1;
-// the grid spacing above lo is 2^(E - 1) (E the exponent of |s|, at least 0),
-// so p * 2^16 = (|s| - lo) * 2^(17 - E) exactly.  No branches: the whole
-// warp takes one path whatever the values.  lo's code (exact, on the grid)
-// comes from the hardware conversion; the round-up bit and the sign are added
-// per nibble (lo's code is at most 6, so nothing carries).
+// |s| cut down to the grid: the spacing above it is 2^(E - 1) (E the exponent
+// of |s|, at least 0), so p * 2^16 = (|s| - lo) * 2^(17 - E) exactly.
+//
+// The grid helpers below keep the work on the FMA pipe where they can: the
+// power of two 2^(17 - E) (2^(19 - E') for E4M3) comes from one integer
+// subtraction and a minimum on the exponent field, and lo from adding
+// c = spacing * 2^23 in round-toward-zero (the sum's unit in the last place is
+// the spacing, so the sum is c + lo exactly) and subtracting c again.  For
+// either format c's bit pattern is 0x92800000 minus that of the power of two.
+// lo carries the sign of s into the hardware conversion; the round-up bit is
+// added to the code's magnitude (at most 6 for E2M1, 0x7E - 1 for E4M3 when a
+// round-up can happen, so nothing carries into the sign).  No branches: the
+// whole warp takes one path whatever the values.
+__device__ __forceinline__ float sr_floor(float a, uint32_t mult_bits)
+{
+    const float c = __uint_as_float(0x92800000u - mult_bits);
+    return __fsub_rn(__fadd_rz(a, c), c);
+}
+
+__device__ __forceinline__ float with_sign_of(float l, float s)
+{
+    return __uint_as_float(__float_as_uint(l) | (__float_as_uint(s) & 0x80000000u));
+}
+
 __device__ __forceinline__ uint32_t e2m1_sr8(const float* s, const uint32_t (&u)[8])
 {
     float lo[8];
-    uint32_t extra = 0;
+    uint32_t ups = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float a = fminf(fabsf(s[i]), 6.0f);
-        const uint32_t ab = __float_as_uint(a);
-        const float l = a >= 1.0f ? __uint_as_float(ab & 0xFFC00000u) : (a >= 0.5f ? 0.5f : 0.0f);
-        const int E = max(static_cast<int>(ab >> 23) - 127, 0);
-        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(static_cast<uint32_t>(144 - E) << 23));
-        lo[i] = l;
-        const uint32_t up = static_cast<float>(u[i]) < t ? 1u : 0u;
-        extra |= (up | ((__float_as_uint(s[i]) >> 31) << 3)) << (4 * i);
+        const uint32_t mb = min(0x87800000u - (__float_as_uint(a) & 0x7F800000u), 0x48000000u);  // 2^(17 - E)
+        const float l = sr_floor(a, mb);
+        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(mb));
+        lo[i] = with_sign_of(l, s[i]);
+        ups += static_cast<float>(u[i]) < t ? (1u << (4 * i)) : 0u;
     }
-    return cvt_e2m1x8(lo) + extra;
+    return cvt_e2m1x8(lo) + ups;
 }
 
 // Stochastic rounding of 8 values onto the E4M3 grid with the same rule (up
 // iff u16 < p * 2^16, p = (|s| - lo) / (hi - lo)), saturating at 448; codes
-// packed one per byte, element 0 in the low byte of out[0].  lo is |s| with
-// its significand cut to 3 bits (normal range) or a multiple of 2^-9
-// (subnormal range, |s| < 2^-6); the spacing above lo is 2^(E' - 3), E' the
-// exponent of |s| but at least -6, so p * 2^16 = (|s| - lo) * 2^(19 - E')
-// exactly.  Branch-free, like e2m1_sr8; lo's code is at most 0x7E - 1 when a
-// round-up can happen, so adding the up bit never carries into the sign.
+// packed one per byte, element 0 in the low byte of out[0].  The spacing
+// above lo is 2^(E' - 3), E' the exponent of |s| but at least -6 (the
+// subnormal range's spacing 2^-9), so p * 2^16 = (|s| - lo) * 2^(19 - E')
+// exactly.  lo and the round-up bit as for E2M1 above.
 __device__ __forceinline__ void e4m3_sr8(const float* s, const uint32_t (&u)[8], uint32_t* out)
 {
     float lo[8];
-    uint32_t extra[2] = {0u, 0u};
+    uint32_t ups[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float a = fminf(fabsf(s[i]), 448.0f);
-        const uint32_t ab = __float_as_uint(a);
-        const int E = max(static_cast<int>(ab >> 23) - 127, -6);
-        const float l = a >= 0x1p-6f ? __uint_as_float(ab & 0xFFF00000u)
-                                      : __fmul_rn(floorf(__fmul_rn(a, 512.0f)), 0x1p-9f);
-        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(static_cast<uint32_t>(146 - E) << 23));
-        lo[i] = l;
-        const uint32_t up = static_cast<float>(u[i]) < t ? 1u : 0u;
-        extra[i >> 2] |= (up | ((__float_as_uint(s[i]) >> 31) << 7)) << (8 * (i & 3));
+        const uint32_t mb = min(0x88800000u - (__float_as_uint(a) & 0x7F800000u), 0x4C000000u);  // 2^(19 - E')
+        const float l = sr_floor(a, mb);
+        const float t = __fmul_rn(__fsub_rn(a, l), __uint_as_float(mb));
+        lo[i] = with_sign_of(l, s[i]);
+        ups[i >> 2] += static_cast<float>(u[i]) < t ? (1u << (8 * (i & 3))) : 0u;
     }
-    out[0] = (cvt_e4m3x2(lo[0], lo[1]) | (cvt_e4m3x2(lo[2], lo[3]) << 16)) + extra[0];
-    out[1] = (cvt_e4m3x2(lo[4], lo[5]) | (cvt_e4m3x2(lo[6], lo[7]) << 16)) + extra[1];
+    out[0] = (cvt_e4m3x2(lo[0], lo[1]) | (cvt_e4m3x2(lo[2], lo[3]) << 16)) + ups[0];
+    out[1] = (cvt_e4m3x2(lo[4], lo[5]) | (cvt_e4m3x2(lo[6], lo[7]) << 16)) + ups[1];
 }
 
 // ------------------------------------------------------------- Philox4x32-10
