@@ -67,6 +67,10 @@ def test_calls_without_a_gpu_fail_loudly(lib):
     rc = lib.mx_quantize(None, 0, 0, 0, 0, 0, 32, 0, 0, 0, 0, 0, None, C.byref(t), None)
     assert rc == mx.MX_ERR_NO_DEVICE
     assert lib.mx_gemm(C.byref(t), C.byref(t), 1.0, None, 0, 0, None) == mx.MX_ERR_NO_DEVICE
+    amax = C.c_float(0.0)
+    assert lib.mx_gemm_amax(C.byref(t), C.byref(t), 1.0, None, 0, 0, C.byref(amax), None) == mx.MX_ERR_NO_DEVICE
+    # a missing amax word is an argument error, found before the device is looked at
+    assert lib.mx_gemm_amax(C.byref(t), C.byref(t), 1.0, None, 0, 0, None, None) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_last_device_status(None) == mx.MX_ERR_NO_DEVICE
     with pytest.raises(mx.MXError):
         mx.quantize(torch.zeros(32, 32, dtype=torch.bfloat16), "mxfp8")
