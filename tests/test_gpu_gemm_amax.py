@@ -131,3 +131,18 @@ def test_amax_under_graph_replay(mx):
         g.replay()
         torch.cuda.synchronize()
         assert am.item() == y.abs().max().float().item()
+
+
+def test_amax_word_must_be_aligned(mx):
+    """A misaligned amax word is refused on the host, before anything launches."""
+    import ctypes as C
+
+    qa, qb = _operands(mx, "mxfp8", 128, 128, 256, 360)
+    c = torch.empty(128, 128, device="cuda")
+    buf = torch.zeros(8, dtype=torch.float32, device="cuda")
+    ca, cb = qa._c(), qb._c()
+    rc = mx.lib().mx_gemm_amax(C.byref(ca), C.byref(cb), 1.0, C.c_void_p(c.data_ptr()), 128, 0,
+                               C.c_void_p(buf.data_ptr() + 2), None)
+    assert rc == mx.MX_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert torch.equal(buf, torch.zeros_like(buf))
