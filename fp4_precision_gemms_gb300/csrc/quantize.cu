@@ -769,9 +769,14 @@ struct TileShape {
 };
 
 // NVFP4 block encode under a region's own FP32 scale ts (NVFP4_LOCAL): the
-// NVFP4 steps with exact IEEE quotients (the shared-divisor division), since
-// the scale differs from region to region.  Produces the scale byte and N/8
-// words of codes; `v` is overwritten.
+// NVFP4 steps with IEEE quotients.  The scale differs from region to region,
+// so no table of certified divisors is built per pass; instead each block
+// certifies its own divisor d = fl32(dec(s_b) * ts) (the bf16 inputs make the
+// double-word reciprocal product decide every E2M1 code as the exact quotient
+// would, as for global NVFP4) and falls back to the shared-divisor division
+// when the certificate or the range guard fails, or under stochastic rounding,
+// which needs the exact quotient.  Produces the scale byte and N/8 words of
+// codes; `v` is overwritten.
 template <bool SR, int N>
 __device__ __forceinline__ uint32_t nvfp4_local_encode(float (&v)[N], float bmax, float ts, uint64_t seed, uint32_t sid,
                                                        uint64_t L8, uint32_t* out)
@@ -790,10 +795,24 @@ __device__ __forceinline__ uint32_t nvfp4_local_encode(float (&v)[N], float bmax
         }
         return sb;
     }
-    const float r = recip_for_div(d);
+    bool fast = false;
+    if constexpr (!SR) {
+        if (quot2_certified_e2m1(d)) {
+            const Recip2 r2 = recip2(d);
+            if (__fmul_rn(bmax, r2.hi) < 0x1p100f) {
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-        v[i] = div_shared(v[i], d, r);
+                for (int i = 0; i < N; ++i)
+                    v[i] = quot2(v[i], r2);
+                fast = true;
+            }
+        }
+    }
+    if (!fast) {
+        const float r = recip_for_div(d);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            v[i] = div_shared(v[i], d, r);
+    }
 #pragma unroll
     for (int w = 0; w < N / 8; ++w) {
         if constexpr (SR) {
