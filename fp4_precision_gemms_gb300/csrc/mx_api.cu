@@ -139,14 +139,22 @@ cudaStream_t fork_begin(const Device& d, cudaStream_t s)
             (void)cudaGetLastError();
             return nullptr;
         }
-        if (cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStream_t side = nullptr;
+        if (cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess) {
             (void)cudaGetLastError();
+            if (side)  // release whatever was made; this thread runs on s from now on
+                (void)cudaStreamDestroy(side);
+            if (f.fork)
+                (void)cudaEventDestroy(f.fork);
+            if (f.join)
+                (void)cudaEventDestroy(f.join);
+            f.fork = f.join = nullptr;
             f.failed = true;
-            f.side = nullptr;
             return nullptr;
         }
+        f.side = side;
     }
     if (cudaEventRecord(f.fork, s) != cudaSuccess || cudaStreamWaitEvent(f.side, f.fork, 0) != cudaSuccess) {
         (void)cudaGetLastError();
