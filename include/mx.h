@@ -287,8 +287,9 @@ typedef struct mx_bwd_opts {
  * event join, which graph capture records as a fork and a join), so the two
  * GEMMs fill each other's last partial wave; the results are the same either
  * way.  The side stream and its two events are created once per host thread
- * and device, on the first such call made outside graph capture; a call
- * captured before then runs on `stream` alone.  Work the caller issues to
+ * and device, on the first such call made outside graph capture, and kept
+ * until the process exits; a call captured before then runs on `stream`
+ * alone.  Work the caller issues to
  * `stream` after the call is ordered after both gradients. */
 int mx_linear_bwd(const void* dY, const void* X, const void* W, int64_t T, int64_t Kin,
                   int64_t Nout, int fmt, const mx_bwd_opts* opts, void* dX, int dx_dtype,
